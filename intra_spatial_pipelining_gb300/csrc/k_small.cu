@@ -1,0 +1,326 @@
+// The latency-bound kernels of the layer: RMSNorm, router (RMSNorm + logits + top-k),
+// dispatch (stable counting sort of the routed pairs by expert slot + row gather) and the
+// weighted combine with the residual.  All loads and stores are 16-byte vectors, every
+// reduction has a fixed order, and each token's result depends only on that token.
+#include "kernels.h"
+
+namespace sgp {
+
+namespace {
+
+// ---------------------------------------------------------------------------------------
+// RMSNorm: y = bf16(x * rsqrt(mean(x^2) + eps) * g), one CTA per row
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const NormProblem P, const KCtx ctx) {
+    task_begin(ctx);
+    __shared__ float red[8];
+    const int row = P.row0 + blockIdx.x;
+    const int nv = P.H >> 3;
+    const uint4* x = reinterpret_cast<const uint4*>(P.x + (size_t)row * P.H);
+    const uint4* g = reinterpret_cast<const uint4*>(P.g);
+    uint4* y = reinterpret_cast<uint4*>(P.y + (size_t)row * P.H);
+    float ss = 0.f;
+    for (int v = threadIdx.x; v < nv; v += 256) {
+        float f[8];
+        unpack8(x[v], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float inv = rsqrtf(tot / (float)P.H + P.eps);
+    for (int v = threadIdx.x; v < nv; v += 256) {
+        float f[8], gg[8];
+        unpack8(x[v], f);
+        unpack8(g[v], gg);
+        uint4 o;
+        o.x = pack_bf16x2(f[0] * inv * gg[0], f[1] * inv * gg[1]);
+        o.y = pack_bf16x2(f[2] * inv * gg[2], f[3] * inv * gg[3]);
+        o.z = pack_bf16x2(f[4] * inv * gg[4], f[5] * inv * gg[5]);
+        o.w = pack_bf16x2(f[6] * inv * gg[6], f[7] * inv * gg[7]);
+        y[v] = o;
+    }
+    task_end(ctx);
+}
+
+// ---------------------------------------------------------------------------------------
+// Router.  grid = (token groups of 8, expert groups of 8).  Each CTA normalises its 8 tokens
+// (u = RMSNorm(h; g)), one warp per expert computes the 8 fp32 logits, and the last CTA of
+// a token group selects the top-k of each token (descending logit, ties to the lower
+// index) and the softmax over the selected logits.
+// ---------------------------------------------------------------------------------------
+constexpr int kRouterTok = 8;
+
+__global__ void __launch_bounds__(256) router_kernel(const RouterProblem P, const KCtx ctx) {
+    task_begin(ctx);
+    extern __shared__ uint8_t smem_raw[];
+    uint4* us = reinterpret_cast<uint4*>(smem_raw);  // [8][H/8]
+    __shared__ int sh_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tg = blockIdx.x;
+    const int nv = P.H >> 3;
+    const int ntok = min(kRouterTok, P.nrows - tg * kRouterTok);
+
+    // (1) RMSNorm of this group's tokens, warp w -> token w
+    if (warp < ntok) {
+        const int row = P.row0 + tg * kRouterTok + warp;
+        const uint4* h = reinterpret_cast<const uint4*>(P.h + (size_t)row * P.H);
+        const uint4* g = reinterpret_cast<const uint4*>(P.g);
+        float ss = 0.f;
+        for (int v = lane; v < nv; v += 32) {
+            float f[8];
+            unpack8(h[v], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+        }
+        ss = warp_sum(ss);
+        const float inv = rsqrtf(ss / (float)P.H + P.eps);
+        uint4* uo = reinterpret_cast<uint4*>(P.u + (size_t)row * P.H);
+        for (int v = lane; v < nv; v += 32) {
+            float f[8], gg[8];
+            unpack8(h[v], f);
+            unpack8(g[v], gg);
+            uint4 o;
+            o.x = pack_bf16x2(f[0] * inv * gg[0], f[1] * inv * gg[1]);
+            o.y = pack_bf16x2(f[2] * inv * gg[2], f[3] * inv * gg[3]);
+            o.z = pack_bf16x2(f[4] * inv * gg[4], f[5] * inv * gg[5]);
+            o.w = pack_bf16x2(f[6] * inv * gg[6], f[7] * inv * gg[7]);
+            us[warp * nv + v] = o;
+            if (blockIdx.y == 0) uo[v] = o;
+        }
+    }
+    __syncthreads();
+
+    // (2) logits, warp w -> expert e
+    const int e = blockIdx.y * 8 + warp;
+    if (e < P.E) {
+        const uint4* w = reinterpret_cast<const uint4*>(P.Wr + (size_t)e * P.H);
+        float acc[kRouterTok];
+#pragma unroll
+        for (int i = 0; i < kRouterTok; ++i) acc[i] = 0.f;
+        for (int v = lane; v < nv; v += 32) {
+            float wf[8];
+            unpack8(__ldg(w + v), wf);
+#pragma unroll
+            for (int i = 0; i < kRouterTok; ++i) {
+                if (i < ntok) {
+                    float uf[8];
+                    unpack8(us[i * nv + v], uf);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[i] = fmaf(wf[q], uf[q], acc[i]);
+                }
+            }
+        }
+        const float b = P.bias ? P.bias[e] : 0.f;
+#pragma unroll
+        for (int i = 0; i < kRouterTok; ++i) {
+            const float z = warp_sum(acc[i]);
+            if (lane == 0 && i < ntok)
+                P.logits[(size_t)(tg * kRouterTok + i) * P.E + e] = z + b;
+        }
+    }
+
+    // (3) last CTA of the token group: top-k + softmax over the selection
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t prev = atomicAdd(&P.cnt[tg], 1u);
+        sh_last = (prev == gridDim.y - 1) ? 1 : 0;
+        if (sh_last) P.cnt[tg] = 0;
+    }
+    __syncthreads();
+    if (sh_last && warp < ntok) {
+        __threadfence();
+        const int tl = tg * kRouterTok + warp;
+        const float* z = P.logits + (size_t)tl * P.E;
+        constexpr int kMaxPer = 32;  // E <= 1024
+        float zv[kMaxPer];
+        const int per = (P.E + 31) / 32;
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i) {
+            const int ee = i * 32 + lane;
+            zv[i] = (i < per && ee < P.E) ? __ldcg(z + ee) : -INFINITY;
+        }
+        uint32_t taken = 0;
+        float selz[8];
+        int seli[8];
+        for (int j = 0; j < P.k; ++j) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < kMaxPer; ++i) {
+                const int ee = i * 32 + lane;
+                if (i < per && ee < P.E && !(taken & (1u << i)) &&
+                    (zv[i] > bv || (zv[i] == bv && ee < bi))) {
+                    bv = zv[i];
+                    bi = ee;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            selz[j] = bv;
+            seli[j] = bi;
+        }
+        if (lane == 0) {
+            float den = 0.f, ex[8];
+            for (int j = 0; j < P.k; ++j) {
+                ex[j] = expf(selz[j] - selz[0]);
+                den += ex[j];
+            }
+            const int row = P.row0 + tl;
+            for (int j = 0; j < P.k; ++j) {
+                const float wj = ex[j] / den;
+                P.idx[tl * P.k + j] = seli[j];
+                P.wts[tl * P.k + j] = wj;
+                if (P.user_idx) P.user_idx[(size_t)row * P.k + j] = seli[j];
+                if (P.user_w) P.user_w[(size_t)row * P.k + j] = wj;
+            }
+        }
+    }
+    task_end(ctx);
+}
+
+// ---------------------------------------------------------------------------------------
+// Dispatch.  Every CTA redundantly computes the stable counting sort of the pairs
+// i = t*k + j by slot (order within a slot = pair order), then gathers 8 rows of u into the
+// slot-sorted activation matrix.  CTA 0 also publishes the slot offsets and pair rows.
+// ---------------------------------------------------------------------------------------
+constexpr int kDispRows = 8;
+
+__global__ void __launch_bounds__(256) dispatch_kernel(const DispatchProblem P, const KCtx ctx) {
+    task_begin(ctx);
+    extern __shared__ int sm_i[];
+    const int R = P.nrows * P.k;
+    int* pslot = sm_i;          // [R]
+    int* rank = pslot + R;      // [R]
+    int* row_pair = rank + R;   // [R]
+    int* offs = row_pair + R;   // [E_local + 1]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    for (int i = threadIdx.x; i < R; i += 256) {
+        int gidx = P.idx[i];
+        if (gidx < 0 || gidx >= P.E) {
+            report(ctx, ST_BOUNDS, (uint32_t)gidx);
+            gidx = 0;
+        }
+        pslot[i] = P.slot_map == 0 ? gidx % P.E_local : (int)(((long)gidx * P.E_local) / P.E);
+    }
+    __syncthreads();
+    for (int s = warp; s < P.E_local; s += 8) {
+        int running = 0;
+        for (int c = 0; c < R; c += 32) {
+            const int i = c + lane;
+            const bool is = i < R && pslot[i] == s;
+            const uint32_t m = __ballot_sync(0xffffffffu, is);
+            if (is) rank[i] = running + __popc(m & ((1u << lane) - 1u));
+            running += __popc(m);
+        }
+        if (lane == 0) offs[s + 1] = running;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        offs[0] = 0;
+        for (int s = 0; s < P.E_local; ++s) offs[s + 1] += offs[s];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < R; i += 256) {
+        const int pos = offs[pslot[i]] + rank[i];
+        row_pair[pos] = i;
+        if (blockIdx.x == 0) P.pair_pos[i] = pos;
+    }
+    if (blockIdx.x == 0)
+        for (int s = threadIdx.x; s <= P.E_local; s += 256) P.offsets[s] = offs[s];
+    __syncthreads();
+    const int nv = P.H >> 3;
+    const int rbeg = blockIdx.x * kDispRows;
+    const int rend = min(R, rbeg + kDispRows);
+    for (int r = rbeg; r < rend; ++r) {
+        const int t = row_pair[r] / P.k;
+        const uint4* src = reinterpret_cast<const uint4*>(P.u + (size_t)(P.row0 + t) * P.H);
+        uint4* dst = reinterpret_cast<uint4*>(P.xperm + (size_t)r * P.H);
+        for (int v = threadIdx.x; v < nv; v += 256) dst[v] = src[v];
+    }
+    task_end(ctx);
+}
+
+// ---------------------------------------------------------------------------------------
+// Combine: out[t] = bf16(h[t] + sum_j w[t][j] * Y[pair_pos[t k + j]]), j in pick order
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, const KCtx ctx) {
+    task_begin(ctx);
+    const int tl = blockIdx.x;
+    const int row = P.row0 + tl;
+    const int n4 = P.H >> 2;
+    int pos[8];
+    float w[8];
+    for (int j = 0; j < P.k; ++j) {
+        pos[j] = P.pair_pos[tl * P.k + j];
+        w[j] = P.wts[tl * P.k + j];
+        if (pos[j] < 0 || pos[j] >= P.nrows * P.k) {
+            if (threadIdx.x == 0) report(ctx, ST_BOUNDS, (uint32_t)pos[j]);
+            pos[j] = 0;
+            w[j] = 0.f;
+        }
+    }
+    const uint2* h = reinterpret_cast<const uint2*>(P.h + (size_t)row * P.H);
+    uint2* out = reinterpret_cast<uint2*>(P.out + (size_t)row * P.H);
+    for (int v = threadIdx.x; v < n4; v += 256) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < P.k; ++j) {
+            const float4 y = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
+            acc[0] = fmaf(w[j], y.x, acc[0]);
+            acc[1] = fmaf(w[j], y.y, acc[1]);
+            acc[2] = fmaf(w[j], y.z, acc[2]);
+            acc[3] = fmaf(w[j], y.w, acc[3]);
+        }
+        const uint2 hv = h[v];
+        const float2 h01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.x));
+        const float2 h23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.y));
+        uint2 o;
+        o.x = pack_bf16x2(h01.x + acc[0], h01.y + acc[1]);
+        o.y = pack_bf16x2(h23.x + acc[2], h23.y + acc[3]);
+        out[v] = o;
+    }
+    task_end(ctx);
+}
+
+}  // namespace
+
+int enqueue_rmsnorm(Launcher& L, const NormProblem& p, const KCtx& c) {
+    void* args[] = {(void*)&p, (void*)&c};
+    return L.launch((const void*)rmsnorm_kernel, dim3(p.nrows), dim3(256), 0, args);
+}
+
+int enqueue_router(Launcher& L, const RouterProblem& p, const KCtx& c) {
+    void* args[] = {(void*)&p, (void*)&c};
+    dim3 grid((p.nrows + kRouterTok - 1) / kRouterTok, (p.E + 7) / 8);
+    return L.launch((const void*)router_kernel, grid, dim3(256),
+                    (size_t)kRouterTok * p.H * sizeof(bf16), args);
+}
+
+int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c) {
+    void* args[] = {(void*)&p, (void*)&c};
+    const int R = p.nrows * p.k;
+    dim3 grid((R + kDispRows - 1) / kDispRows);
+    return L.launch((const void*)dispatch_kernel, grid, dim3(256),
+                    (size_t)(3 * R + p.E_local + 1) * sizeof(int), args);
+}
+
+int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c) {
+    void* args[] = {(void*)&p, (void*)&c};
+    return L.launch((const void*)combine_kernel, dim3(p.nrows), dim3(256), 0, args);
+}
+
+}  // namespace sgp

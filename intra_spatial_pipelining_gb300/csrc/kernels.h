@@ -1,0 +1,149 @@
+// Problem descriptions of the layer's kernels and the host-side enqueue functions.
+// Each kernel translation unit owns its kernels; the runtime only sees these functions,
+// which compute the launch shape and hand the launch to a Launcher (a stream, or a CUDA
+// graph under construction bound to one SM pool).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace sgp {
+
+// Receives launches.  args points to one pointer per kernel parameter (cudaLaunchKernel
+// convention); the launcher copies the values before returning.  Returns a cudaError_t.
+struct Launcher {
+    virtual ~Launcher() {}
+    virtual int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) = 0;
+};
+
+// --------------------------------------------------------------------------------------
+// projection epilogues
+// --------------------------------------------------------------------------------------
+enum EpiMode : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_F32 = 3 };
+
+struct EpiArgs {
+    int mode;
+    int n_out;          // valid output features (per group)
+    int ld;             // row stride (elements) of the output / residual rows
+    // EPI_QKV: q [rows][q_width]; caches [seq][nkv][cap][d]
+    bf16* q;
+    int q_width;
+    bf16* kc;
+    bf16* vc;
+    const int* kv_len;
+    int nkv, cap, d;
+    // EPI_RESID: out = resid + acc (bf16); EPI_SWIGLU: out = silu(gate) * up (bf16)
+    const bf16* resid;
+    bf16* out;
+    // EPI_F32
+    float* out_f32;
+};
+
+// Skinny GEMM  D[out_feature][token] = sum_k W[out_feature][k] * X[token][k]  on tcgen05.
+// Work unit = (group, 128-row tile, K segment); the K split is fixed by the shape so the
+// fp32 summation order never depends on the grid or on the token count.
+struct GemmProblem {
+    CUtensorMap tmA;        // weights, 2-D [groups * rows_per_group][K], box {64, 64}, SW128
+    CUtensorMap tmB;        // activations, 2-D [rows][K], box {64, 16}, SW128
+    int K, kb_total, ksplit;
+    int m_tiles;            // 128-row tiles per group
+    int n_groups;
+    int rows_per_group;     // weight rows of one group
+    int a_tile_stride;      // first weight row of tile mt = mt * a_tile_stride (128 or 64)
+    int a_second_off;       // second 64-row half starts a_second_off rows later (64 or inter)
+    const int* group_offsets;  // device [n_groups + 1] token-row ranges, or NULL (dense)
+    int row0, nrows;        // dense: token rows [row0, row0 + nrows)
+    int R;                  // rows of the partial-sum buffer
+    int n_cap;              // tokens per pass (multiple of 16, <= 256)
+    int stages;             // shared-memory pipeline depth
+    int serpentine;         // visit groups in reverse order
+    float* partial;         // [ksplit][R][m_tiles][128] fp32
+    uint32_t* tile_cnt;     // [n_groups * m_tiles], zero between launches
+    EpiArgs epi;
+};
+
+// Same contraction on CUDA cores (small token counts).
+struct GemvProblem {
+    const bf16* W;          // [groups * rows_per_group][K]
+    int K, rows_per_group, n_groups, n_out, swiglu, up_off;
+    const bf16* X;          // activations [rows][K]
+    const int* group_offsets;
+    int row0, nrows;
+    EpiArgs epi;
+};
+
+struct AttnProblem {
+    CUtensorMap tmK, tmV;   // caches as 2-D [seq * nkv * cap][64], box {64, 32}, SW128
+    const bf16* q;          // [T][nq * 64]
+    const int* kv_len;      // [T]
+    bf16* o;                // [T][nq * 64]
+    float* part_ml;         // [nrows * nkv][S_max][16][2]
+    float* part_acc;        // [nrows * nkv][S_max][16][64]
+    uint32_t* cnt;          // [nrows * nkv]
+    int row0, nrows, nq, nkv, G, cap, window, chunk, S_max;
+    float scale_log2;       // log2(e) / sqrt(d)
+};
+
+struct NormProblem {
+    const bf16* x;
+    const bf16* g;
+    bf16* y;
+    int row0, nrows, H;
+    float eps;
+};
+
+struct RouterProblem {
+    const bf16* h;          // [T][H] batch-wide
+    const bf16* g;          // [H]
+    bf16* u;                // [T][H] batch-wide
+    const bf16* Wr;         // [E][H]
+    const float* bias;      // [E] or NULL
+    float* logits;          // [nrows][E]
+    int* idx;               // [nrows][k]
+    float* wts;             // [nrows][k]
+    int* user_idx;          // [T][k] batch-wide or NULL
+    float* user_w;
+    uint32_t* cnt;          // [ceil(nrows / 8)]
+    int row0, nrows, H, E, k;
+    float eps;
+};
+
+struct DispatchProblem {
+    const int* idx;         // [nrows][k]
+    const bf16* u;          // [T][H] batch-wide
+    bf16* xperm;            // [nrows * k][H]
+    int* offsets;           // [E_local + 1]
+    int* pair_pos;          // [nrows * k]
+    int row0, nrows, k, H, E, E_local, slot_map;
+};
+
+struct CombineProblem {
+    const bf16* h;          // [T][H] batch-wide
+    const float* Y;         // [nrows * k][H]
+    const float* wts;       // [nrows][k]
+    const int* pair_pos;    // [nrows * k]
+    bf16* out;              // [T][H] batch-wide
+    int row0, nrows, k, H;
+};
+
+// --------------------------------------------------------------------------------------
+// host enqueue functions (return cudaError_t as int)
+// --------------------------------------------------------------------------------------
+int enqueue_rmsnorm(Launcher& L, const NormProblem& p, const KCtx& c);
+int enqueue_router(Launcher& L, const RouterProblem& p, const KCtx& c);
+int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c);
+int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c);
+int enqueue_attention(Launcher& L, const AttnProblem& p, const KCtx& c);
+int enqueue_gemm_tc(Launcher& L, const GemmProblem& p, const KCtx& c);
+int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c);
+
+// shared-memory bytes a tcgen05 GEMM launch needs for (n_cap, stages)
+size_t gemm_tc_smem_bytes(int n_cap, int stages);
+// attention chunk length (positions per split-KV work item); fixed, never SM-dependent
+constexpr int kAttnChunk = 512;
+
+}  // namespace sgp

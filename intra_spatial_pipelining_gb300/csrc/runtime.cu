@@ -1,0 +1,1282 @@
+// Host runtime of libsgp: argument validation, workspace layout, the per-op launch
+// planning shared by temporal and pipelined execution, SM pools (green contexts), the
+// augmented task DAG of the pipeline as an explicit CUDA graph, stage timing and the
+// two-stage balancer.
+//
+// The execution model follows "SubGPU Pipelining: Intra-GPU Fine-Grained Spatial
+// Parallelism for LLM Inference": Section 3.1 (contiguous segments bound to stages with
+// disjoint SM pools, Eq. 1-3), Section 3.2 (tasks (layer, microbatch, segment) with data
+// edges and per-stage FIFO edges in a fixed global dispatch order), Section 5.3 (green
+// contexts for the SM pools, CUDA graphs for submission, events/graph edges for the
+// producer/consumer dependencies).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <unordered_set>
+#include <vector>
+
+#include "kernels.h"
+#include "sgp.h"
+
+using namespace sgp;
+
+// =======================================================================================
+// errors
+// =======================================================================================
+namespace {
+
+thread_local std::string g_err;
+
+int fail_cuda(cudaError_t e, const char* what) {
+    g_err = std::string(what) + ": " + cudaGetErrorString(e);
+    return SGP_ERR_CUDA;
+}
+int fail_drv(CUresult r, const char* what) {
+    g_err = std::string(what) + ": CUresult " + std::to_string((int)r);
+    return SGP_ERR_CUDA;
+}
+int fail_arg(const char* what) {
+    g_err = std::string("invalid argument: ") + what;
+    return SGP_ERR_INVALID_ARG;
+}
+
+#define CK(x)                                          \
+    do {                                               \
+        cudaError_t e_ = (x);                          \
+        if (e_ != cudaSuccess) return fail_cuda(e_, #x); \
+    } while (0)
+#define CKD(x)                                          \
+    do {                                                \
+        CUresult r_ = (x);                              \
+        if (r_ != CUDA_SUCCESS) return fail_drv(r_, #x); \
+    } while (0)
+
+// =======================================================================================
+// driver entry points (fetched at run time: the library links no libcuda)
+// =======================================================================================
+struct Driver {
+    PFN_cuTensorMapEncodeTiled_v12000 encodeTiled = nullptr;
+    PFN_cuGraphAddNode_v12030 graphAddNode = nullptr;
+    PFN_cuKernelSetAttribute_v12000 kernelSetAttribute = nullptr;
+    PFN_cuDeviceGetDevResource_v12040 devGetResource = nullptr;
+    PFN_cuDevSmResourceSplitByCount_v12040 smSplit = nullptr;
+    PFN_cuDevResourceGenerateDesc_v12040 genDesc = nullptr;
+    PFN_cuGreenCtxCreate_v12040 greenCreate = nullptr;
+    PFN_cuGreenCtxDestroy_v12040 greenDestroy = nullptr;
+    PFN_cuCtxFromGreenCtx_v12040 ctxFromGreen = nullptr;
+    PFN_cuGreenCtxGetDevResource_v12040 greenGetResource = nullptr;
+    bool core = false;   // tensor maps, graph nodes, kernel attributes
+    bool green = false;  // green-context API
+};
+
+template <typename F>
+bool get_entry(const char* name, F& fn, unsigned ver) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, ver, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+        return false;
+    fn = reinterpret_cast<F>(p);
+    return true;
+}
+
+Driver& drv() {
+    static Driver d;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        d.core = get_entry("cuTensorMapEncodeTiled", d.encodeTiled, 12000) &&
+                 get_entry("cuGraphAddNode", d.graphAddNode, 12030) &&
+                 get_entry("cuKernelSetAttribute", d.kernelSetAttribute, 12000);
+        d.green = get_entry("cuDeviceGetDevResource", d.devGetResource, 12040) &&
+                  get_entry("cuDevSmResourceSplitByCount", d.smSplit, 12040) &&
+                  get_entry("cuDevResourceGenerateDesc", d.genDesc, 12040) &&
+                  get_entry("cuGreenCtxCreate", d.greenCreate, 12040) &&
+                  get_entry("cuGreenCtxDestroy", d.greenDestroy, 12040) &&
+                  get_entry("cuCtxFromGreenCtx", d.ctxFromGreen, 12040) &&
+                  get_entry("cuGreenCtxGetDevResource", d.greenGetResource, 12040);
+    });
+    return d;
+}
+
+// Opt every kernel that asks for more than 48 KB of dynamic shared memory into the full
+// 227 KB, for the runtime's launches and (through its CUkernel) for every context.
+int ensure_smem_attr(const void* func, size_t smem) {
+    if (smem <= 48 * 1024) return 0;
+    static std::mutex mu;
+    static std::unordered_set<const void*> done;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count(func)) return 0;
+    const int max_smem = 227 * 1024;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return (int)e;
+    Driver& d = drv();
+    if (d.core) {
+        cudaKernel_t k;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaGetKernel(&k, func) == cudaSuccess)
+            d.kernelSetAttribute(CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, max_smem,
+                                 (CUkernel)k, (CUdevice)dev);
+    }
+    done.insert(func);
+    return 0;
+}
+
+// =======================================================================================
+// launchers
+// =======================================================================================
+struct StreamLauncher : Launcher {
+    cudaStream_t s;
+    explicit StreamLauncher(cudaStream_t st) : s(st) {}
+    int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) override {
+        int e = ensure_smem_attr(func, smem);
+        if (e) return e;
+        return (int)cudaLaunchKernel(func, grid, block, args, smem, s);
+    }
+};
+
+// Appends kernel nodes to a CUDA graph as a chain, bound to one (green) context.
+struct GraphLauncher : Launcher {
+    CUgraph g;
+    CUcontext ctx;
+    std::vector<CUgraphNode> deps;
+    GraphLauncher(CUgraph graph, CUcontext c) : g(graph), ctx(c) {}
+    int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) override {
+        int e = ensure_smem_attr(func, smem);
+        if (e) return e;
+        cudaKernel_t k;
+        cudaError_t ce = cudaGetKernel(&k, func);
+        if (ce != cudaSuccess) return (int)ce;
+        CUgraphNodeParams np;
+        memset(&np, 0, sizeof(np));
+        np.type = CU_GRAPH_NODE_TYPE_KERNEL;
+        np.kernel.func = nullptr;
+        np.kernel.kern = (CUkernel)k;
+        np.kernel.ctx = ctx;
+        np.kernel.gridDimX = grid.x;
+        np.kernel.gridDimY = grid.y;
+        np.kernel.gridDimZ = grid.z;
+        np.kernel.blockDimX = block.x;
+        np.kernel.blockDimY = block.y;
+        np.kernel.blockDimZ = block.z;
+        np.kernel.sharedMemBytes = (unsigned)smem;
+        np.kernel.kernelParams = args;
+        CUgraphNode n;
+        CUresult r = drv().graphAddNode(&n, g, deps.empty() ? nullptr : deps.data(), nullptr,
+                                        deps.size(), &np);
+        if (r != CUDA_SUCCESS) {
+            g_err = "cuGraphAddNode: CUresult " + std::to_string((int)r);
+            return (int)cudaErrorUnknown;
+        }
+        deps.assign(1, n);
+        return 0;
+    }
+};
+
+// =======================================================================================
+// validation and launch planning
+// =======================================================================================
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_dims(const sgp_dims* d) {
+    if (!d) return fail_arg("dims is NULL");
+    if (d->head_dim != 64) return fail_arg("head_dim must be 64");
+    if (d->hidden <= 0 || d->hidden % 64) return fail_arg("hidden must be a positive multiple of 64");
+    if (d->inter <= 0 || d->inter % 64) return fail_arg("inter must be a positive multiple of 64");
+    if (d->n_kv_heads <= 0 || d->n_q_heads <= 0 || d->n_q_heads % d->n_kv_heads)
+        return fail_arg("n_q_heads must be a positive multiple of n_kv_heads");
+    if (d->n_q_heads / d->n_kv_heads > 16) return fail_arg("more than 16 query heads per KV head");
+    if (d->top_k < 1 || d->top_k > 8) return fail_arg("top_k must be in [1, 8]");
+    if (d->n_experts < d->top_k || d->n_experts > 1024) return fail_arg("n_experts out of range");
+    if (d->n_local_experts < 1 || d->n_local_experts > d->n_experts)
+        return fail_arg("n_local_experts out of range");
+    if (d->slot_map != 0 && d->slot_map != 1) return fail_arg("slot_map must be 0 or 1");
+    if (d->path < 0 || d->path > 2) return fail_arg("path must be SGP_PATH_*");
+    if (!(d->rms_eps > 0.f)) return fail_arg("rms_eps must be positive");
+    if (d->hidden > 8192) return fail_arg("hidden above 8192 is not supported");
+    return SGP_OK;
+}
+
+int qkv_rows(const sgp_dims& d) { return (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim; }
+int q_width(const sgp_dims& d) { return d.n_q_heads * d.head_dim; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// fixed K split of a projection: ~160 units in total, >= 4 k-blocks per segment
+int choose_ksplit(int tiles, int kb_total) {
+    int ks = (int)std::lround(160.0 / tiles);
+    ks = std::max(1, std::min(ks, kb_total / 4));
+    return std::max(1, ks);
+}
+
+struct GemmShape {
+    int K, rows_per_group, n_groups, m_tiles, a_tile_stride, a_second_off, ksplit;
+};
+GemmShape gemm_shape(const sgp_dims& d, int op) {
+    GemmShape g{};
+    switch (op) {
+        case SGP_OP_QKV:
+            g = {d.hidden, qkv_rows(d), 1, cdiv(qkv_rows(d), 128), 128, 64, 1};
+            break;
+        case SGP_OP_OPROJ:
+            g = {q_width(d), d.hidden, 1, cdiv(d.hidden, 128), 128, 64, 1};
+            break;
+        case SGP_OP_EXPERT_UP:
+            g = {d.hidden, 2 * d.inter, d.n_local_experts, d.inter / 64, 64, d.inter, 1};
+            break;
+        default:  // SGP_OP_EXPERT_DOWN
+            g = {d.inter, d.hidden, d.n_local_experts, cdiv(d.hidden, 128), 128, 64, 1};
+            break;
+    }
+    g.ksplit = choose_ksplit(g.n_groups * g.m_tiles, g.K / 64);
+    return g;
+}
+
+bool use_tc_dense(const sgp_dims& d, int T) {
+    if (d.path == SGP_PATH_GEMV) return false;
+    if (d.path == SGP_PATH_TC) return true;
+    return T >= std::max(1, d.gemv_max_tokens);
+}
+bool use_tc_expert(const sgp_dims& d, int T) {
+    if (d.path == SGP_PATH_GEMV) return false;
+    if (d.path == SGP_PATH_TC) return true;
+    return (long)T * d.top_k >= (long)std::max(1, d.gemv_max_tokens) * d.n_local_experts;
+}
+
+int attn_smax(int max_kv) { return std::max(1, cdiv(max_kv, kAttnChunk)); }
+
+// ---------------------------------------------------------------------------------------
+// workspace layout: status | zeroed region (counters, flags) | batch-wide activations |
+// per-microbatch scratch.  All offsets 256-byte aligned.
+// ---------------------------------------------------------------------------------------
+struct Layout {
+    int T = 0, m = 1, b = 0, S_max = 1, n_flags = 0;
+    size_t status = 0, zero_beg = 0, zero_end = 0;
+    size_t tile_cnt = 0, attn_cnt = 0, router_cnt = 0, flags = 0, flag_cnt = 0;
+    size_t a = 0, q = 0, o = 0, h = 0, u = 0;
+    size_t per_mu = 0;  // bytes of one microbatch's scratch block
+    size_t mu_base = 0;
+    // offsets inside a microbatch block
+    size_t part_ml = 0, part_acc = 0, logits = 0, idx = 0, wts = 0, offsets = 0, pair_pos = 0,
+           xperm = 0, zbuf = 0, ybuf = 0, gemm_part = 0;
+    int max_tiles = 0;
+    size_t total = 0;
+};
+
+size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags) {
+    Layout L;
+    L.T = T;
+    L.m = m;
+    L.b = T / m;
+    L.S_max = attn_smax(max_kv);
+    L.n_flags = n_flags;
+    const int b = L.b, H = d.hidden, qw = q_width(d), k = d.top_k, R = b * k;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = al256(off + bytes);
+        return o;
+    };
+    L.status = take(64);
+    L.zero_beg = off;
+    int max_tiles = 0;
+    for (int op : {SGP_OP_QKV, SGP_OP_OPROJ, SGP_OP_EXPERT_UP, SGP_OP_EXPERT_DOWN}) {
+        GemmShape g = gemm_shape(d, op);
+        max_tiles = std::max(max_tiles, g.n_groups * g.m_tiles);
+    }
+    L.max_tiles = max_tiles;
+    L.tile_cnt = take((size_t)m * max_tiles * 4);
+    L.attn_cnt = take((size_t)m * b * d.n_kv_heads * 4);
+    L.router_cnt = take((size_t)m * cdiv(b, 8) * 4);
+    L.flags = take((size_t)std::max(1, n_flags) * 4);
+    L.flag_cnt = take((size_t)std::max(1, n_flags) * 4);
+    L.zero_end = off;
+    L.a = take((size_t)T * H * 2);
+    L.q = take((size_t)T * qw * 2);
+    L.o = take((size_t)T * qw * 2);
+    L.h = take((size_t)T * H * 2);
+    L.u = take((size_t)T * H * 2);
+    // per-microbatch block
+    size_t mo = 0;
+    auto mtake = [&](size_t bytes) {
+        size_t o = mo;
+        mo = al256(mo + bytes);
+        return o;
+    };
+    L.part_ml = mtake((size_t)b * d.n_kv_heads * L.S_max * 32 * 4);
+    L.part_acc = mtake((size_t)b * d.n_kv_heads * L.S_max * 16 * 64 * 4);
+    L.logits = mtake((size_t)b * d.n_experts * 4);
+    L.idx = mtake((size_t)R * 4);
+    L.wts = mtake((size_t)R * 4);
+    L.offsets = mtake((size_t)(d.n_local_experts + 1) * 4);
+    L.pair_pos = mtake((size_t)R * 4);
+    L.xperm = mtake((size_t)R * H * 2);
+    L.zbuf = mtake((size_t)R * d.inter * 2);
+    L.ybuf = mtake((size_t)R * H * 4);
+    size_t gp = 0;
+    for (int op : {SGP_OP_QKV, SGP_OP_OPROJ, SGP_OP_EXPERT_UP, SGP_OP_EXPERT_DOWN}) {
+        GemmShape g = gemm_shape(d, op);
+        const int rows = (op == SGP_OP_QKV || op == SGP_OP_OPROJ) ? b : R;
+        gp = std::max(gp, (size_t)g.ksplit * rows * g.m_tiles * 128 * 4);
+    }
+    L.gemm_part = mtake(gp);
+    L.per_mu = al256(mo);
+    L.mu_base = off;
+    L.total = L.mu_base + (size_t)m * L.per_mu;
+    return L;
+}
+
+// pointers into one workspace
+struct Ws {
+    uint8_t* base;
+    const Layout* L;
+    uint32_t* status() const { return reinterpret_cast<uint32_t*>(base + L->status); }
+    template <typename T>
+    T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
+    template <typename T>
+    T* mu(int m, size_t off) const {
+        return reinterpret_cast<T*>(base + L->mu_base + (size_t)m * L->per_mu + off);
+    }
+};
+
+// ---------------------------------------------------------------------------------------
+// tensor maps
+// ---------------------------------------------------------------------------------------
+int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+              uint32_t box_inner, uint32_t box_rows) {
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = drv().encodeTiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                   const_cast<void*>(base), dims, strides, box, es,
+                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail_drv(r, "cuTensorMapEncodeTiled");
+    return SGP_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// one op of one layer for one microbatch
+// ---------------------------------------------------------------------------------------
+struct RunEnv {
+    const sgp_dims* d;
+    const sgp_layer* layer;
+    const int32_t* kv_len;
+    const bf16* x_cur;  // residual input of this layer (batch-wide)
+    bf16* x_out;        // residual output (batch-wide)
+    int T;
+    Ws ws;
+    int32_t* topk_idx;  // this layer's user outputs (batch-wide) or NULL
+    float* topk_w;
+    bool tc_dense, tc_expert;
+    int serpentine;
+};
+
+int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
+    const sgp_dims& d = *e.d;
+    const int b = e.ws.L->b, row0 = mu * b, R = b * d.top_k;
+    GemmShape gs = gemm_shape(d, op);
+    const bool grouped = (op == SGP_OP_EXPERT_UP || op == SGP_OP_EXPERT_DOWN);
+    const bool tc = grouped ? e.tc_expert : e.tc_dense;
+    const bf16* W = nullptr;
+    const bf16* X = nullptr;  // activation matrix base (dense: batch-wide; grouped: per mu)
+    int xrows = 0;
+    EpiArgs epi;
+    memset(&epi, 0, sizeof(epi));
+    switch (op) {
+        case SGP_OP_QKV:
+            W = (const bf16*)e.layer->w_qkv;
+            X = e.ws.at<bf16>(e.ws.L->a);
+            epi.mode = EPI_QKV;
+            epi.n_out = qkv_rows(d);
+            epi.q = e.ws.at<bf16>(e.ws.L->q);
+            epi.q_width = q_width(d);
+            epi.kc = (bf16*)e.layer->k_cache;
+            epi.vc = (bf16*)e.layer->v_cache;
+            epi.kv_len = e.kv_len;
+            epi.nkv = d.n_kv_heads;
+            epi.cap = e.layer->kv_cap;
+            epi.d = d.head_dim;
+            break;
+        case SGP_OP_OPROJ:
+            W = (const bf16*)e.layer->w_o;
+            X = e.ws.at<bf16>(e.ws.L->o);
+            epi.mode = EPI_RESID;
+            epi.n_out = d.hidden;
+            epi.ld = d.hidden;
+            epi.resid = e.x_cur;
+            epi.out = e.ws.at<bf16>(e.ws.L->h);
+            break;
+        case SGP_OP_EXPERT_UP:
+            W = (const bf16*)e.layer->w_gate_up;
+            X = e.ws.mu<bf16>(mu, e.ws.L->xperm);
+            xrows = R;
+            epi.mode = EPI_SWIGLU;
+            epi.n_out = d.inter;
+            epi.ld = d.inter;
+            epi.out = e.ws.mu<bf16>(mu, e.ws.L->zbuf);
+            break;
+        default:
+            W = (const bf16*)e.layer->w_down;
+            X = e.ws.mu<bf16>(mu, e.ws.L->zbuf);
+            xrows = R;
+            epi.mode = EPI_F32;
+            epi.n_out = d.hidden;
+            epi.ld = d.hidden;
+            epi.out_f32 = e.ws.mu<float>(mu, e.ws.L->ybuf);
+            break;
+    }
+    const int* goff = grouped ? e.ws.mu<int>(mu, e.ws.L->offsets) : nullptr;
+    if (!tc) {
+        GemvProblem p;
+        memset(&p, 0, sizeof(p));
+        p.W = W;
+        p.K = gs.K;
+        p.rows_per_group = gs.rows_per_group;
+        p.n_groups = gs.n_groups;
+        p.n_out = (op == SGP_OP_EXPERT_UP) ? d.inter : gs.rows_per_group;
+        p.swiglu = (op == SGP_OP_EXPERT_UP);
+        p.up_off = d.inter;
+        p.X = X;
+        p.group_offsets = goff;
+        p.row0 = grouped ? 0 : row0;
+        p.nrows = grouped ? 0 : b;
+        p.epi = epi;
+        return enqueue_gemv(L, p, c);
+    }
+    GemmProblem p;
+    memset(&p, 0, sizeof(p));
+    int r;
+    const uint64_t total_rows = (uint64_t)gs.n_groups * gs.rows_per_group;
+    if ((r = make_tmap(&p.tmA, W, gs.K, total_rows, 64, 64)) != SGP_OK) return r;
+    if (grouped) {
+        if ((r = make_tmap(&p.tmB, X, gs.K, (uint64_t)xrows, 64, 16)) != SGP_OK) return r;
+    } else {
+        // only this microbatch's rows are visible to the loads (the rest is OOB = zero)
+        if ((r = make_tmap(&p.tmB, X + (size_t)row0 * gs.K, gs.K, (uint64_t)b, 64, 16)) != SGP_OK)
+            return r;
+    }
+    p.K = gs.K;
+    p.kb_total = gs.K / 64;
+    p.ksplit = gs.ksplit;
+    p.m_tiles = gs.m_tiles;
+    p.n_groups = gs.n_groups;
+    p.rows_per_group = gs.rows_per_group;
+    p.a_tile_stride = gs.a_tile_stride;
+    p.a_second_off = gs.a_second_off;
+    p.group_offsets = goff;
+    p.row0 = row0;
+    p.nrows = b;
+    p.R = grouped ? R : b;
+    int expect = grouped ? std::max(16, 2 * cdiv(R, gs.n_groups)) : b;
+    p.n_cap = std::min(256, std::max(16, (expect + 15) & ~15));
+    const int stage_bytes = 16384 + p.n_cap * 128;
+    p.stages = std::max(2, std::min(8, (110 * 1024 - 1280) / stage_bytes));
+    p.serpentine = grouped && e.serpentine && (mu & 1);
+    p.partial = e.ws.mu<float>(mu, e.ws.L->gemm_part);
+    p.tile_cnt = e.ws.at<uint32_t>(e.ws.L->tile_cnt) + (size_t)mu * e.ws.L->max_tiles;
+    p.epi = epi;
+    return enqueue_gemm_tc(L, p, c);
+}
+
+int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
+    const sgp_dims& d = *e.d;
+    const Layout& Lay = *e.ws.L;
+    const int b = Lay.b, row0 = mu * b;
+    int r = 0;
+    switch (op) {
+        case SGP_OP_RMSNORM_ATTN: {
+            NormProblem p{e.x_cur, (const bf16*)e.layer->g_attn, e.ws.at<bf16>(Lay.a), row0, b,
+                          d.hidden, d.rms_eps};
+            return enqueue_rmsnorm(L, p, c);
+        }
+        case SGP_OP_QKV:
+        case SGP_OP_OPROJ:
+        case SGP_OP_EXPERT_UP:
+        case SGP_OP_EXPERT_DOWN:
+            return gemm_op(L, e, op, mu, c);
+        case SGP_OP_ATTENTION: {
+            AttnProblem p;
+            memset(&p, 0, sizeof(p));
+            const uint64_t rows = (uint64_t)e.T * d.n_kv_heads * e.layer->kv_cap;
+            if ((r = make_tmap(&p.tmK, e.layer->k_cache, 64, rows, 64, 32)) != SGP_OK) return r;
+            if ((r = make_tmap(&p.tmV, e.layer->v_cache, 64, rows, 64, 32)) != SGP_OK) return r;
+            p.q = e.ws.at<bf16>(Lay.q);
+            p.kv_len = e.kv_len;
+            p.o = e.ws.at<bf16>(Lay.o);
+            p.part_ml = e.ws.mu<float>(mu, Lay.part_ml);
+            p.part_acc = e.ws.mu<float>(mu, Lay.part_acc);
+            p.cnt = e.ws.at<uint32_t>(Lay.attn_cnt) + (size_t)mu * b * d.n_kv_heads;
+            p.row0 = row0;
+            p.nrows = b;
+            p.nq = d.n_q_heads;
+            p.nkv = d.n_kv_heads;
+            p.G = d.n_q_heads / d.n_kv_heads;
+            p.cap = e.layer->kv_cap;
+            p.window = e.layer->window;
+            p.chunk = kAttnChunk;
+            const int span = e.layer->window > 0 ? std::min(e.layer->window, e.layer->kv_cap)
+                                                 : e.layer->kv_cap;
+            p.S_max = attn_smax(span);
+            if (p.S_max > Lay.S_max) return fail_arg("kv_cap exceeds the workspace's max_kv_len");
+            p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
+            return enqueue_attention(L, p, c);
+        }
+        case SGP_OP_ROUTER: {
+            RouterProblem p;
+            memset(&p, 0, sizeof(p));
+            p.h = e.ws.at<bf16>(Lay.h);
+            p.g = (const bf16*)e.layer->g_mlp;
+            p.u = e.ws.at<bf16>(Lay.u);
+            p.Wr = (const bf16*)e.layer->w_router;
+            p.bias = e.layer->router_bias;
+            p.logits = e.ws.mu<float>(mu, Lay.logits);
+            p.idx = e.ws.mu<int>(mu, Lay.idx);
+            p.wts = e.ws.mu<float>(mu, Lay.wts);
+            p.user_idx = e.topk_idx;
+            p.user_w = e.topk_w;
+            p.cnt = e.ws.at<uint32_t>(Lay.router_cnt) + (size_t)mu * cdiv(b, 8);
+            p.row0 = row0;
+            p.nrows = b;
+            p.H = d.hidden;
+            p.E = d.n_experts;
+            p.k = d.top_k;
+            p.eps = d.rms_eps;
+            return enqueue_router(L, p, c);
+        }
+        case SGP_OP_DISPATCH: {
+            DispatchProblem p{e.ws.mu<int>(mu, Lay.idx), e.ws.at<bf16>(Lay.u),
+                              e.ws.mu<bf16>(mu, Lay.xperm), e.ws.mu<int>(mu, Lay.offsets),
+                              e.ws.mu<int>(mu, Lay.pair_pos), row0, b, d.top_k, d.hidden,
+                              d.n_experts, d.n_local_experts, d.slot_map};
+            return enqueue_dispatch(L, p, c);
+        }
+        case SGP_OP_COMBINE: {
+            CombineProblem p{e.ws.at<bf16>(Lay.h), e.ws.mu<float>(mu, Lay.ybuf),
+                             e.ws.mu<float>(mu, Lay.wts), e.ws.mu<int>(mu, Lay.pair_pos),
+                             e.x_out, row0, b, d.top_k, d.hidden};
+            return enqueue_combine(L, p, c);
+        }
+        default:
+            return fail_arg("op index");
+    }
+}
+
+int check_layer(const sgp_dims& d, const sgp_layer* l, int T) {
+    if (!l) return fail_arg("layer is NULL");
+    const void* ptrs[] = {l->g_attn, l->w_qkv, l->w_o, l->g_mlp, l->w_router,
+                          l->w_gate_up, l->w_down, l->k_cache, l->v_cache};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return fail_arg("layer pointer NULL or not 16-byte aligned");
+    if (l->kv_cap < 1) return fail_arg("kv_cap must be positive");
+    if (l->window < 0) return fail_arg("window must be >= 0");
+    if ((uint64_t)T * d.n_kv_heads * l->kv_cap >= (1ull << 31))
+        return fail_arg("KV cache rows exceed 2^31");
+    return SGP_OK;
+}
+
+int status_to_code(uint32_t s) {
+    if (s & ST_TIMEOUT) return SGP_ERR_TIMEOUT;
+    if (s & ST_HANDOFF) return SGP_ERR_HANDOFF;
+    if (s & ST_BOUNDS) return SGP_ERR_DEVICE_BOUNDS;
+    return SGP_OK;
+}
+
+KCtx plain_ctx(uint32_t* status, uint64_t timeout, uint32_t tag) {
+    KCtx c;
+    memset(&c, 0, sizeof(c));
+    c.status = status;
+    c.timeout_ns = timeout;
+    c.tag = tag;
+    return c;
+}
+
+constexpr uint64_t kDefaultTimeout = 2000000000ull;
+
+int run_layer_stream(const sgp_dims& d, const sgp_layer* layer, int li, const int32_t* kv_len,
+                     const bf16* x_cur, bf16* x_out, int T, int32_t* tki, float* tkw, Ws ws,
+                     cudaStream_t s) {
+    StreamLauncher L(s);
+    RunEnv e{&d, layer, kv_len, x_cur, x_out, T, ws, tki, tkw, use_tc_dense(d, T),
+             use_tc_expert(d, T), 0};
+    for (int op = 0; op < SGP_N_OPS; ++op) {
+        KCtx c = plain_ctx(ws.status(), kDefaultTimeout, ((uint32_t)op << 24) | ((uint32_t)li << 12));
+        int r = enqueue_op(L, e, op, 0, c);
+        if (r == SGP_ERR_INVALID_ARG || r == SGP_ERR_CUDA) return r;
+        if (r != 0) return fail_cuda((cudaError_t)r, "kernel launch");
+    }
+    return SGP_OK;
+}
+
+}  // namespace
+
+// =======================================================================================
+// C ABI: info
+// =======================================================================================
+extern "C" const char* sgp_status_string(int s) {
+    switch (s) {
+        case SGP_OK: return "ok";
+        case SGP_ERR_INVALID_ARG: return "invalid argument";
+        case SGP_ERR_UNSUPPORTED: return "unsupported device or feature";
+        case SGP_ERR_CUDA: return "CUDA error";
+        case SGP_ERR_TIMEOUT: return "device wait timed out";
+        case SGP_ERR_OOM: return "out of memory";
+        case SGP_ERR_HANDOFF: return "stage handoff check failed";
+        case SGP_ERR_DEVICE_BOUNDS: return "device index out of range (skipped)";
+        default: return "unknown status";
+    }
+}
+
+extern "C" const char* sgp_last_error(void) { return g_err.c_str(); }
+
+extern "C" int sgp_device_info_get(sgp_device_info* info) {
+    if (!info) return fail_arg("info is NULL");
+    memset(info, 0, sizeof(*info));
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&info->sm_count, cudaDevAttrMultiProcessorCount, dev));
+    CK(cudaDeviceGetAttribute(&info->cc_major, cudaDevAttrComputeCapabilityMajor, dev));
+    CK(cudaDeviceGetAttribute(&info->cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
+    int l2 = 0;
+    CK(cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev));
+    info->l2_bytes = (size_t)l2;
+    Driver& d = drv();
+    if (d.green) {
+        CK(cudaFree(0));
+        CUdevResource res;
+        memset(&res, 0, sizeof(res));
+        if (d.devGetResource((CUdevice)dev, &res, CU_DEV_RESOURCE_TYPE_SM) == CUDA_SUCCESS) {
+            info->green_ctx_supported = 1;
+            info->sm_min_partition = (int)res.sm.minSmPartitionSize;
+            info->sm_alignment = (int)res.sm.smCoscheduledAlignment;
+        }
+    }
+    return SGP_OK;
+}
+
+// =======================================================================================
+// C ABI: temporal execution
+// =======================================================================================
+extern "C" size_t sgp_workspace_bytes(const sgp_dims* d, int n_tokens, int max_kv_len) {
+    if (check_dims(d) != SGP_OK || n_tokens < 1 || max_kv_len < 1) return 0;
+    return make_layout(*d, n_tokens, 1, max_kv_len, 0).total;
+}
+
+static int temporal_common(const sgp_dims* d, const sgp_layer* layers, int n_layers,
+                           const int32_t* kv_len, const void* x_in, void* x_out, int T,
+                           int32_t* tki, float* tkw, void* ws, size_t ws_bytes,
+                           const sgp_layer_dump* dump, cudaStream_t s) {
+    int r;
+    if ((r = check_dims(d)) != SGP_OK) return r;
+    if (T < 1) return fail_arg("n_tokens must be positive");
+    if (n_layers < 1 || !layers) return fail_arg("no layers");
+    if (!kv_len || !x_in || !x_out || !ws) return fail_arg("NULL pointer");
+    if (!aligned16(x_in) || !aligned16(x_out) || (reinterpret_cast<uintptr_t>(ws) & 255))
+        return fail_arg("x must be 16-byte and workspace 256-byte aligned");
+    int max_cap = 1;
+    for (int l = 0; l < n_layers; ++l) {
+        if ((r = check_layer(*d, &layers[l], T)) != SGP_OK) return r;
+        max_cap = std::max(max_cap, layers[l].kv_cap);
+    }
+    Layout Lay = make_layout(*d, T, 1, max_cap, 0);
+    if (ws_bytes < Lay.total) return fail_arg("workspace too small");
+    if (!drv().core) {
+        g_err = "CUDA driver entry points unavailable";
+        return SGP_ERR_UNSUPPORTED;
+    }
+    Ws w{(uint8_t*)ws, &Lay};
+    CK(cudaMemsetAsync(w.base + Lay.zero_beg, 0, Lay.zero_end - Lay.zero_beg, s));
+    for (int l = 0; l < n_layers; ++l) {
+        const bf16* xc = (const bf16*)(l == 0 ? x_in : x_out);
+        int32_t* ti = tki ? tki + (size_t)l * T * d->top_k : nullptr;
+        float* tw = tkw ? tkw + (size_t)l * T * d->top_k : nullptr;
+        if ((r = run_layer_stream(*d, &layers[l], l, kv_len, xc, (bf16*)x_out, T, ti, tw, w, s)) !=
+            SGP_OK)
+            return r;
+    }
+    if (dump) {
+        const size_t H = d->hidden, qw = q_width(*d), R = (size_t)T * d->top_k;
+        auto cp = [&](void* dst, const void* src, size_t bytes) -> int {
+            if (dst) CK(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s));
+            return SGP_OK;
+        };
+        if ((r = cp(dump->a, w.base + Lay.a, T * H * 2))) return r;
+        if ((r = cp(dump->q, w.base + Lay.q, T * qw * 2))) return r;
+        if ((r = cp(dump->o, w.base + Lay.o, T * qw * 2))) return r;
+        if ((r = cp(dump->h, w.base + Lay.h, T * H * 2))) return r;
+        if ((r = cp(dump->u, w.base + Lay.u, T * H * 2))) return r;
+        if ((r = cp(dump->logits, w.mu<float>(0, Lay.logits), (size_t)T * d->n_experts * 4))) return r;
+        if ((r = cp(dump->slot_offsets, w.mu<int>(0, Lay.offsets), (d->n_local_experts + 1) * 4)))
+            return r;
+        if ((r = cp(dump->pair_pos, w.mu<int>(0, Lay.pair_pos), R * 4))) return r;
+        if ((r = cp(dump->z, w.mu<bf16>(0, Lay.zbuf), R * d->inter * 2))) return r;
+        if ((r = cp(dump->y, w.mu<float>(0, Lay.ybuf), R * H * 4))) return r;
+    }
+    return SGP_OK;
+}
+
+extern "C" int sgp_layer_temporal(const sgp_dims* d, const sgp_layer* layer, const int32_t* kv_len,
+                                  const void* x_in, void* x_out, int n_tokens, int32_t* topk_idx,
+                                  float* topk_w, void* ws, size_t ws_bytes,
+                                  const sgp_layer_dump* dump, sgp_stream_t stream) {
+    return temporal_common(d, layer, 1, kv_len, x_in, x_out, n_tokens, topk_idx, topk_w, ws,
+                           ws_bytes, dump, (cudaStream_t)stream);
+}
+
+extern "C" int sgp_stack_temporal(const sgp_dims* d, const sgp_layer* layers, int n_layers,
+                                  const int32_t* kv_len, const void* x_in, void* x_out,
+                                  int n_tokens, int32_t* topk_idx, float* topk_w, void* ws,
+                                  size_t ws_bytes, sgp_stream_t stream) {
+    return temporal_common(d, layers, n_layers, kv_len, x_in, x_out, n_tokens, topk_idx, topk_w,
+                           ws, ws_bytes, nullptr, (cudaStream_t)stream);
+}
+
+extern "C" int sgp_status_from_workspace(const void* ws, sgp_stream_t stream) {
+    if (!ws) return fail_arg("workspace is NULL");
+    uint32_t st[4] = {0, 0, 0, 0};
+    CK(cudaStreamSynchronize((cudaStream_t)stream));
+    CK(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
+    CK(cudaMemset(const_cast<void*>(ws), 0, sizeof(st)));
+    if (st[0]) {
+        char buf[96];
+        snprintf(buf, sizeof(buf), "device status 0x%x at op %u layer %u micro %u (detail %u)",
+                 st[0], st[1] >> 24, (st[1] >> 12) & 0xFFF, st[1] & 0xFFF, st[2]);
+        g_err = buf;
+    }
+    return status_to_code(st[0]);
+}
+
+// =======================================================================================
+// C ABI: pipeline
+// =======================================================================================
+struct PTask {
+    int stage, mu;
+    int l0, op0, l1, op1;      // first and last (layer, op), inclusive, along the chain
+    int pred_data, pred_stage;
+};
+
+struct sgp_pipeline {
+    sgp_dims dims;
+    int n_stages = 1, micro = 1, max_tokens = 0, max_kv = 0;
+    sgp_pipeline_opts opts;
+    int stage_of_op[2][SGP_N_OPS];
+    int split[3] = {0, 0, 0};
+    int dev = 0;
+    CUgreenCtx gctx[4] = {nullptr, nullptr, nullptr, nullptr};
+    CUcontext sctx[3] = {nullptr, nullptr, nullptr};
+    int n_gctx = 0;
+    uint8_t* ws = nullptr;
+    size_t ws_bytes = 0;
+    int ws_T = 0, ws_nflags = 0;
+    Layout lay;
+    // graph cache
+    cudaGraphExec_t exec = nullptr;
+    std::vector<uint8_t> key;
+    std::vector<PTask> tasks;
+    cudaStream_t last_stream = nullptr;
+};
+
+namespace {
+
+std::vector<PTask> build_tasks(const sgp_pipeline& p, const sgp_layer* layers, int n_layers, int m) {
+    std::vector<PTask> per;
+    std::vector<std::vector<int>> chain(m);
+    // tasks of each microbatch along its chain
+    std::vector<PTask> all;
+    std::vector<long> first_pos;
+    for (int mu = 0; mu < m; ++mu) {
+        int cur = -1;
+        for (int l = 0; l < n_layers; ++l) {
+            const int sl = layers[l].window > 0 ? 1 : 0;
+            for (int op = 0; op < SGP_N_OPS; ++op) {
+                const int st = p.stage_of_op[sl][op];
+                if (cur >= 0 && all[cur].stage == st) {
+                    all[cur].l1 = l;
+                    all[cur].op1 = op;
+                } else {
+                    PTask t{st, mu, l, op, l, op, cur, -1};
+                    all.push_back(t);
+                    first_pos.push_back((long)l * SGP_N_OPS + op);
+                    cur = (int)all.size() - 1;
+                }
+            }
+        }
+    }
+    // global dispatch order: by chain position of the first op, then microbatch
+    std::vector<int> order(all.size());
+    for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+        if (first_pos[a] != first_pos[b]) return first_pos[a] < first_pos[b];
+        return all[a].mu < all[b].mu;
+    });
+    std::vector<int> newidx(all.size());
+    for (size_t i = 0; i < order.size(); ++i) newidx[order[i]] = (int)i;
+    std::vector<PTask> out(all.size());
+    int last_on_stage[4] = {-1, -1, -1, -1};
+    for (size_t i = 0; i < order.size(); ++i) {
+        PTask t = all[order[i]];
+        t.pred_data = t.pred_data >= 0 ? newidx[t.pred_data] : -1;
+        t.pred_stage = last_on_stage[t.stage];
+        last_on_stage[t.stage] = (int)i;
+        out[i] = t;
+    }
+    return out;
+}
+
+int ensure_ws(sgp_pipeline* p, int T, int nflags) {
+    if (p->ws && p->ws_T == T && p->ws_nflags >= nflags) return SGP_OK;
+    if (p->ws) {
+        cudaFree(p->ws);
+        p->ws = nullptr;
+    }
+    Layout L = make_layout(p->dims, T, T / p->micro, p->max_kv, nflags);
+    cudaError_t e = cudaMalloc(&p->ws, L.total);
+    if (e != cudaSuccess) {
+        g_err = std::string("cudaMalloc: ") + cudaGetErrorString(e);
+        return SGP_ERR_OOM;
+    }
+    CK(cudaMemset(p->ws, 0, L.total));
+    p->lay = L;
+    p->ws_bytes = L.total;
+    p->ws_T = T;
+    p->ws_nflags = nflags;
+    return SGP_OK;
+}
+
+// Builds the graph of the given tasks.  stage_only >= 0 keeps only that stage's tasks and
+// drops their cross-stage data edges (used for timing one stage alone).
+int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_layer* layers,
+                const int32_t* kv_len, const void* x_in, void* x_out, int T, int32_t* tki,
+                float* tkw, int stage_only, cudaGraph_t* out_graph) {
+    const sgp_dims& d = p->dims;
+    cudaGraph_t g;
+    CK(cudaGraphCreate(&g, 0));
+    Ws w{p->ws, &p->lay};
+    cudaGraphNode_t zero;
+    cudaMemsetParams ms;
+    memset(&ms, 0, sizeof(ms));
+    ms.dst = p->ws + p->lay.zero_beg;
+    ms.value = 0;
+    ms.elementSize = 1;
+    ms.width = p->lay.zero_end - p->lay.zero_beg;
+    ms.height = 1;
+    ms.pitch = 0;
+    cudaError_t ce = cudaGraphAddMemsetNode(&zero, g, nullptr, 0, &ms);
+    if (ce != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return fail_cuda(ce, "cudaGraphAddMemsetNode");
+    }
+    std::vector<CUgraphNode> last(tasks.size(), nullptr);
+    const bool tcd = use_tc_dense(d, T), tce = use_tc_expert(d, T);
+    const uint64_t timeout = p->opts.wait_timeout_ns ? p->opts.wait_timeout_ns : kDefaultTimeout;
+    uint32_t* flags = w.at<uint32_t>(p->lay.flags);
+    uint32_t* fcnt = w.at<uint32_t>(p->lay.flag_cnt);
+    for (size_t i = 0; i < tasks.size(); ++i) {
+        const PTask& t = tasks[i];
+        if (stage_only >= 0 && t.stage != stage_only) continue;
+        GraphLauncher L((CUgraph)g, p->sctx[t.stage]);
+        const bool keep_data = stage_only < 0;
+        if (keep_data && t.pred_data >= 0) L.deps.push_back(last[t.pred_data]);
+        if (t.pred_stage >= 0 && last[t.pred_stage]) L.deps.push_back(last[t.pred_stage]);
+        if (L.deps.empty()) L.deps.push_back((CUgraphNode)zero);
+        int l = t.l0, op = t.op0;
+        bool first = true;
+        while (true) {
+            const bool lastop = (l == t.l1 && op == t.op1);
+            KCtx c = plain_ctx(w.status(), timeout,
+                               ((uint32_t)op << 24) | ((uint32_t)l << 12) | (uint32_t)t.mu);
+            if (first && keep_data && t.pred_data >= 0) c.wait_flag = flags + t.pred_data;
+            if (lastop) {
+                c.post_flag = flags + i;
+                c.post_cnt = fcnt + i;
+                if ((p->opts.fault_inject & 1u) && (int)i == p->opts.fault_task)
+                    c.fault |= FAULT_SKIP_PUBLISH;
+            }
+            if ((p->opts.fault_inject & 2u) && i == 0 && first) c.fault |= FAULT_DROP_TMA;
+            RunEnv e{&d, &layers[l], kv_len, (const bf16*)(l == 0 ? x_in : x_out), (bf16*)x_out, T,
+                     w, tki ? tki + (size_t)l * T * d.top_k : nullptr,
+                     tkw ? tkw + (size_t)l * T * d.top_k : nullptr, tcd, tce,
+                     p->opts.serpentine_experts};
+            int r = enqueue_op(L, e, op, t.mu, c);
+            if (r != 0) {
+                cudaGraphDestroy(g);
+                if (r == SGP_ERR_INVALID_ARG || r == SGP_ERR_CUDA) return r;
+                return fail_cuda((cudaError_t)r, "graph kernel node");
+            }
+            first = false;
+            if (lastop) break;
+            if (++op == SGP_N_OPS) {
+                op = 0;
+                ++l;
+            }
+        }
+        last[i] = L.deps[0];
+    }
+    *out_graph = g;
+    return SGP_OK;
+}
+
+int setup_green(sgp_pipeline* p) {
+    Driver& d = drv();
+    if (!d.green) {
+        g_err = "green-context driver API unavailable";
+        return SGP_ERR_UNSUPPORTED;
+    }
+    CK(cudaFree(0));
+    CUdevResource cur;
+    memset(&cur, 0, sizeof(cur));
+    CKD(d.devGetResource((CUdevice)p->dev, &cur, CU_DEV_RESOURCE_TYPE_SM));
+    for (int s = 0; s < p->n_stages; ++s) {
+        const bool lastst = (s == p->n_stages - 1);
+        CUdevResource grp, rest;
+        memset(&grp, 0, sizeof(grp));
+        memset(&rest, 0, sizeof(rest));
+        if (lastst && (int)cur.sm.smCount == p->split[s]) {
+            grp = cur;
+        } else {
+            unsigned nb = 1;
+            CKD(d.smSplit(&grp, &nb, &cur, &rest, (unsigned)p->opts.green_ctx_flags,
+                          (unsigned)p->split[s]));
+            if (nb != 1 || (int)grp.sm.smCount != p->split[s]) {
+                g_err = "SM split of " + std::to_string(p->split[s]) + " gave " +
+                        std::to_string(grp.sm.smCount) + " SMs";
+                return SGP_ERR_INVALID_ARG;
+            }
+        }
+        CUdevResourceDesc desc;
+        CKD(d.genDesc(&desc, &grp, 1));
+        CKD(d.greenCreate(&p->gctx[p->n_gctx], desc, (CUdevice)p->dev, CU_GREEN_CTX_DEFAULT_STREAM));
+        CKD(d.ctxFromGreen(&p->sctx[s], p->gctx[p->n_gctx]));
+        p->n_gctx++;
+        if (!lastst) {
+            // the remainder must become a green context before it can be split again
+            CUdevResourceDesc rdesc;
+            CKD(d.genDesc(&rdesc, &rest, 1));
+            CKD(d.greenCreate(&p->gctx[p->n_gctx], rdesc, (CUdevice)p->dev,
+                              CU_GREEN_CTX_DEFAULT_STREAM));
+            memset(&cur, 0, sizeof(cur));
+            CKD(d.greenGetResource(p->gctx[p->n_gctx], &cur, CU_DEV_RESOURCE_TYPE_SM));
+            p->n_gctx++;
+        }
+    }
+    return SGP_OK;
+}
+
+}  // namespace
+
+extern "C" int sgp_enumerate_splits(int n_sm, int quantum, int p_min, int* out, int max_out) {
+    if (n_sm < 2 || quantum < 1 || p_min < 1) return fail_arg("n_sm, quantum, p_min");
+    int lo = ((p_min + quantum - 1) / quantum) * quantum;
+    int n = 0;
+    for (int pa = lo; pa <= n_sm - p_min; pa += quantum) {
+        if (out && n < max_out) out[n] = pa;
+        ++n;
+    }
+    return n;
+}
+
+extern "C" int sgp_pipeline_create(const sgp_dims* d, const int* sm_split, int n_stages,
+                                   int microbatch, int max_tokens, int max_kv_len,
+                                   const sgp_pipeline_opts* opts, sgp_pipeline** out) {
+    int r;
+    if (!out) return fail_arg("out is NULL");
+    *out = nullptr;
+    if ((r = check_dims(d)) != SGP_OK) return r;
+    if (n_stages < 1 || n_stages > 3) return fail_arg("n_stages must be 1, 2 or 3");
+    if (microbatch < 1 || max_tokens < 1 || max_tokens % microbatch)
+        return fail_arg("microbatch must divide max_tokens");
+    if (max_kv_len < 1) return fail_arg("max_kv_len");
+    if (!drv().core) {
+        g_err = "CUDA driver entry points unavailable";
+        return SGP_ERR_UNSUPPORTED;
+    }
+    sgp_pipeline* p = new (std::nothrow) sgp_pipeline();
+    if (!p) return SGP_ERR_OOM;
+    p->dims = *d;
+    p->n_stages = n_stages;
+    p->micro = microbatch;
+    p->max_tokens = max_tokens;
+    p->max_kv = max_kv_len;
+    if (opts)
+        p->opts = *opts;
+    else
+        memset(&p->opts, 0, sizeof(p->opts));
+    if (p->opts.custom_cut) {
+        for (int s = 0; s < 2; ++s)
+            for (int op = 0; op < SGP_N_OPS; ++op) {
+                const int st = p->opts.stage_of_op[s][op];
+                if (st < 0 || st >= n_stages) {
+                    delete p;
+                    return fail_arg("stage_of_op out of range");
+                }
+                p->stage_of_op[s][op] = st;
+            }
+    } else {
+        for (int s = 0; s < 2; ++s)
+            for (int op = 0; op < SGP_N_OPS; ++op) {
+                int st = 0;
+                if (n_stages == 2) st = op <= SGP_OP_ATTENTION ? 0 : 1;
+                if (n_stages == 3)
+                    st = op <= SGP_OP_ATTENTION ? 0 : (op <= SGP_OP_ROUTER ? 1 : 2);
+                p->stage_of_op[s][op] = st;
+            }
+    }
+    CK(cudaGetDevice(&p->dev));
+    const bool green = n_stages >= 2 && p->opts.use_green_contexts >= 0;
+    if (green) {
+        if (!sm_split) {
+            delete p;
+            return fail_arg("sm_split is NULL");
+        }
+        int nsm = 0;
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, p->dev);
+        int sum = 0;
+        for (int s = 0; s < n_stages; ++s) {
+            if (sm_split[s] < 1) {
+                delete p;
+                return fail_arg("sm_split entries must be positive");
+            }
+            p->split[s] = sm_split[s];
+            sum += sm_split[s];
+        }
+        if (sum > nsm) {
+            delete p;
+            return fail_arg("sm_split sums to more than the SM count");
+        }
+        if ((r = setup_green(p)) != SGP_OK) {
+            sgp_pipeline_destroy(p);
+            return r;
+        }
+    }
+    if ((r = ensure_ws(p, max_tokens, 1)) != SGP_OK) {
+        sgp_pipeline_destroy(p);
+        return r;
+    }
+    *out = p;
+    return SGP_OK;
+}
+
+static int read_status(sgp_pipeline* p) {
+    uint32_t st[4] = {0, 0, 0, 0};
+    CK(cudaMemcpy(st, p->ws + p->lay.status, sizeof(st), cudaMemcpyDeviceToHost));
+    if (st[0]) {
+        CK(cudaMemset(p->ws + p->lay.status, 0, sizeof(st)));
+        char buf[96];
+        snprintf(buf, sizeof(buf), "device status 0x%x at op %u layer %u micro %u (detail %u)",
+                 st[0], st[1] >> 24, (st[1] >> 12) & 0xFFF, st[1] & 0xFFF, st[2]);
+        g_err = buf;
+    }
+    return status_to_code(st[0]);
+}
+
+static int pipeline_prepare(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
+                            const int32_t* kv_len, const void* x_in, void* x_out, int T) {
+    int r;
+    if (!p) return fail_arg("pipeline is NULL");
+    if (!layers || n_layers < 1) return fail_arg("no layers");
+    if (T < 1 || T > p->max_tokens || T % p->micro) return fail_arg("n_tokens vs microbatch");
+    if (!kv_len || !x_in || !x_out || !aligned16(x_in) || !aligned16(x_out))
+        return fail_arg("NULL or unaligned pointer");
+    for (int l = 0; l < n_layers; ++l) {
+        if ((r = check_layer(p->dims, &layers[l], T)) != SGP_OK) return r;
+        if (layers[l].kv_cap > p->max_kv && layers[l].window == 0)
+            return fail_arg("kv_cap above the pipeline's max_kv_len");
+    }
+    return SGP_OK;
+}
+
+extern "C" int sgp_pipeline_run(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
+                                const int32_t* kv_len, const void* x_in, void* x_out,
+                                int n_tokens, int32_t* topk_idx, float* topk_w,
+                                sgp_stream_t stream) {
+    int r;
+    if ((r = pipeline_prepare(p, layers, n_layers, kv_len, x_in, x_out, n_tokens)) != SGP_OK)
+        return r;
+    cudaStream_t s = (cudaStream_t)stream;
+    // report a device error of an earlier, never-synchronised run
+    if (p->last_stream != nullptr || p->exec != nullptr) {
+        uint32_t st0 = 0;
+        CK(cudaMemcpyAsync(&st0, p->ws + p->lay.status, 4, cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        if (st0) return read_status(p);
+    }
+    std::vector<uint8_t> key;
+    auto add = [&](const void* v, size_t n) {
+        const uint8_t* b = (const uint8_t*)v;
+        key.insert(key.end(), b, b + n);
+    };
+    add(layers, sizeof(sgp_layer) * n_layers);
+    add(&kv_len, sizeof(kv_len));
+    add(&x_in, sizeof(x_in));
+    add(&x_out, sizeof(x_out));
+    add(&n_tokens, sizeof(n_tokens));
+    add(&topk_idx, sizeof(topk_idx));
+    add(&topk_w, sizeof(topk_w));
+    if (!p->exec || key != p->key) {
+        const int m = n_tokens / p->micro;
+        std::vector<PTask> tasks = build_tasks(*p, layers, n_layers, m);
+        if ((r = ensure_ws(p, n_tokens, (int)tasks.size())) != SGP_OK) return r;
+        // ensure_ws recomputed the layout for this token count
+        if (p->lay.m != m) {
+            cudaFree(p->ws);
+            p->ws = nullptr;
+            if ((r = ensure_ws(p, n_tokens, (int)tasks.size())) != SGP_OK) return r;
+        }
+        cudaGraph_t g;
+        if ((r = build_graph(p, tasks, layers, kv_len, x_in, x_out, n_tokens, topk_idx, topk_w, -1,
+                             &g)) != SGP_OK)
+            return r;
+        if (p->exec) {
+            cudaGraphExecDestroy(p->exec);
+            p->exec = nullptr;
+        }
+        cudaError_t e = cudaGraphInstantiate(&p->exec, g, 0);
+        cudaGraphDestroy(g);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaGraphInstantiate");
+        p->key = key;
+        p->tasks = tasks;
+    }
+    CK(cudaGraphLaunch(p->exec, s));
+    p->last_stream = s;
+    return SGP_OK;
+}
+
+extern "C" int sgp_pipeline_sync(sgp_pipeline* p) {
+    if (!p) return fail_arg("pipeline is NULL");
+    if (p->last_stream) CK(cudaStreamSynchronize(p->last_stream));
+    CK(cudaDeviceSynchronize());
+    return read_status(p);
+}
+
+extern "C" int sgp_pipeline_stage_times(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
+                                        const int32_t* kv_len, const void* x_in, void* x_out,
+                                        int n_tokens, int reps, float* t_us) {
+    int r;
+    if ((r = pipeline_prepare(p, layers, n_layers, kv_len, x_in, x_out, n_tokens)) != SGP_OK)
+        return r;
+    if (!t_us || reps < 1) return fail_arg("t_us / reps");
+    const int m = n_tokens / p->micro;
+    std::vector<PTask> tasks = build_tasks(*p, layers, n_layers, m);
+    if ((r = ensure_ws(p, n_tokens, (int)tasks.size())) != SGP_OK) return r;
+    if (p->lay.m != m) {
+        cudaFree(p->ws);
+        p->ws = nullptr;
+        if (p->exec) {
+            cudaGraphExecDestroy(p->exec);
+            p->exec = nullptr;
+        }
+        if ((r = ensure_ws(p, n_tokens, (int)tasks.size())) != SGP_OK) return r;
+    }
+    cudaStream_t s;
+    CK(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
+    cudaEvent_t e0, e1;
+    CK(cudaEventCreate(&e0));
+    CK(cudaEventCreate(&e1));
+    for (int st = 0; st < p->n_stages; ++st) {
+        cudaGraph_t g;
+        if ((r = build_graph(p, tasks, layers, kv_len, x_in, x_out, n_tokens, nullptr, nullptr, st,
+                             &g)) != SGP_OK)
+            return r;
+        cudaGraphExec_t ex;
+        cudaError_t ce = cudaGraphInstantiate(&ex, g, 0);
+        cudaGraphDestroy(g);
+        if (ce != cudaSuccess) return fail_cuda(ce, "cudaGraphInstantiate");
+        std::vector<float> ts;
+        for (int i = 0; i < reps + 1; ++i) {
+            CK(cudaEventRecord(e0, s));
+            CK(cudaGraphLaunch(ex, s));
+            CK(cudaEventRecord(e1, s));
+            CK(cudaEventSynchronize(e1));
+            float ms = 0.f;
+            CK(cudaEventElapsedTime(&ms, e0, e1));
+            if (i > 0) ts.push_back(ms * 1000.f);
+        }
+        cudaGraphExecDestroy(ex);
+        std::sort(ts.begin(), ts.end());
+        t_us[st] = ts[ts.size() / 2];
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaStreamDestroy(s);
+    return read_status(p);
+}
+
+extern "C" int sgp_pipeline_tasks(sgp_pipeline* p, int* n_tasks, int32_t* rows, int max_rows) {
+    if (!p || !n_tasks) return fail_arg("NULL");
+    *n_tasks = (int)p->tasks.size();
+    if (rows)
+        for (int i = 0; i < (int)p->tasks.size() && i < max_rows; ++i) {
+            const PTask& t = p->tasks[i];
+            rows[5 * i + 0] = t.stage;
+            rows[5 * i + 1] = t.l0;
+            rows[5 * i + 2] = t.mu;
+            rows[5 * i + 3] = t.pred_data;
+            rows[5 * i + 4] = t.pred_stage;
+        }
+    return SGP_OK;
+}
+
+extern "C" void sgp_pipeline_destroy(sgp_pipeline* p) {
+    if (!p) return;
+    if (p->last_stream) cudaStreamSynchronize(p->last_stream);
+    if (p->exec) cudaGraphExecDestroy(p->exec);
+    if (p->ws) cudaFree(p->ws);
+    Driver& d = drv();
+    for (int i = p->n_gctx - 1; i >= 0; --i)
+        if (p->gctx[i] && d.greenDestroy) d.greenDestroy(p->gctx[i]);
+    delete p;
+}
+
+extern "C" int sgp_pipeline_balance(const sgp_dims* d, const sgp_layer* layers, int n_layers,
+                                    const int32_t* kv_len, const void* x_in, void* x_out,
+                                    int n_tokens, int microbatch, int max_kv_len, int quantum,
+                                    int reps, const sgp_pipeline_opts* opts, int* best_split_out,
+                                    int* splits, float* t_us, int max_out, int* n_out) {
+    int r;
+    if (!best_split_out || !n_out) return fail_arg("NULL output");
+    sgp_device_info info;
+    if ((r = sgp_device_info_get(&info)) != SGP_OK) return r;
+    if (!info.green_ctx_supported) return SGP_ERR_UNSUPPORTED;
+    const int q = std::max(quantum, std::max(1, info.sm_alignment));
+    const int pmin = std::max(q, info.sm_min_partition);
+    std::vector<int> cand(sgp_enumerate_splits(info.sm_count, q, pmin, nullptr, 0));
+    sgp_enumerate_splits(info.sm_count, q, pmin, cand.data(), (int)cand.size());
+    float best = INFINITY;
+    *best_split_out = -1;
+    int n = 0;
+    for (int pa : cand) {
+        int split[2] = {pa, info.sm_count - pa};
+        sgp_pipeline* p = nullptr;
+        if ((r = sgp_pipeline_create(d, split, 2, microbatch, n_tokens, max_kv_len, opts, &p)) !=
+            SGP_OK)
+            continue;  // a split the device cannot form is skipped
+        float t[2] = {0.f, 0.f};
+        r = sgp_pipeline_stage_times(p, layers, n_layers, kv_len, x_in, x_out, n_tokens, reps, t);
+        sgp_pipeline_destroy(p);
+        if (r != SGP_OK) return r;
+        if (n < max_out) {
+            if (splits) splits[n] = pa;
+            if (t_us) {
+                t_us[2 * n] = t[0];
+                t_us[2 * n + 1] = t[1];
+            }
+        }
+        ++n;
+        const float mx = std::max(t[0], t[1]);
+        if (mx < best) {
+            best = mx;
+            *best_split_out = pa;
+        }
+    }
+    *n_out = n;
+    return *best_split_out >= 0 ? SGP_OK : SGP_ERR_UNSUPPORTED;
+}

@@ -1,0 +1,144 @@
+"""GPU parity of one decode layer (temporal execution) against the fp64 oracle,
+through the C ABI.  Tolerance: max|err| <= 2e-2 * max|ref| per bf16 tensor;
+routing sets bit-exact (inputs keep a top-k logit margin >= 1e-3)."""
+import numpy as np
+import pytest
+import torch
+
+from intra_spatial_pipelining_gb300 import sgp, synth
+from oracle import layer as O
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+def test_generator_identical_on_cpu_and_gpu():
+    a = synth.normal(5, "k_cache", 3, (3, 5000), 0.02, "cpu")
+    b = synth.normal(5, "k_cache", 3, (3, 5000), 0.02, "cuda").cpu()
+    assert torch.equal(a, b)
+    g1 = synth.normal(5, "g_attn", 1, (2880,), 0.02, "cpu", mean_one=True)
+    g2 = synth.normal(5, "g_attn", 1, (2880,), 0.02, "cuda", mean_one=True).cpu()
+    assert torch.equal(g1, g2)
+    assert torch.equal(synth.kv_len(synth.sweep_workload(64, 1), 3, "cpu"),
+                       synth.kv_len(synth.sweep_workload(64, 1), 3, "cuda").cpu())
+
+
+def test_device_info():
+    info = sgp.sgp_device_info_get()
+    print(f"sm_count={info.sm_count} cc={info.cc_major}.{info.cc_minor} "
+          f"green={info.green_ctx_supported} min_part={info.sm_min_partition} "
+          f"align={info.sm_alignment} l2={info.l2_bytes}")
+    assert info.sm_count > 0 and info.cc_major == 10
+
+
+def _check_layer(inp, ref, res, T):
+    s = inp.shape
+    assert res["status"] == sgp.SGP_OK, sgp.sgp_status_string(res["status"])
+    dmp = res["dump"]
+    errs = {}
+    for name in ("a", "q", "o", "h", "u"):
+        errs[name] = H.assert_close(name, dmp[name], ref[name])
+    errs["logits"] = H.assert_close("logits", dmp["logits"], ref["logits"], tol=1e-3)
+    assert H.routing_sets(res["idx"]) == H.routing_sets(ref["idx"])
+    # weights matched by expert index
+    gi, gw = res["idx"].cpu().numpy(), res["w"].cpu().numpy()
+    for t in range(T):
+        g = dict(zip(gi[t].tolist(), gw[t].tolist()))
+        for e, wv in zip(ref["idx"][t].tolist(), ref["w"][t].tolist()):
+            assert abs(g[e] - wv) <= 1e-4, (t, e, g[e], wv)
+    assert abs(float(gw.sum(axis=1).max()) - 1.0) < 1e-5
+    # routed rows: slot order, pair positions
+    off = dmp["slot_offsets"].cpu().numpy()
+    pos = dmp["pair_pos"].cpu().numpy().reshape(T, s.top_k)
+    slots = np.array([[O.slot_of(int(e), s.n_experts, s.n_local_experts, s.slot_map)
+                       for e in row] for row in gi])
+    for t in range(T):
+        for j in range(s.top_k):
+            assert off[slots[t, j]] <= pos[t, j] < off[slots[t, j] + 1]
+    # SwiGLU rows and expert-down rows vs the oracle's per-pick values (matched by expert)
+    zr = np.zeros((T * s.top_k, s.inter))
+    yr = np.zeros((T * s.top_k, s.hidden))
+    ri = ref["idx"]
+    for t in range(T):
+        for j in range(s.top_k):
+            jr = list(ri[t]).index(gi[t, j])
+            zr[pos[t, j]] = ref["z"][t][jr]
+            yr[pos[t, j]] = ref["y"][t][jr]
+    errs["z"] = H.assert_close("z", dmp["z"], zr)
+    errs["y"] = H.assert_close("y", dmp["y"], yr)
+    errs["x_next"] = H.assert_close("x_next", res["x_next"], ref["x_next"])
+    return errs
+
+
+@pytest.mark.parametrize("path", [sgp.PATH_GEMV, sgp.PATH_TC])
+def test_tiny_layer_vs_oracle(path):
+    wl = synth.WORKLOADS["tiny"]
+    inp, ref = H.make_inputs_with_margin(wl, 1)
+    res = H.run_temporal_layer(inp, H.dims(wl.shape, path))
+    errs = _check_layer(inp, ref, res, wl.n_tokens)
+    print("tiny", path, {k: f"{v:.2e}" for k, v in errs.items()})
+    # the appended cache row equals the projection output
+    k, v = inp.caches[0]
+    L = inp.kv_len.cpu().numpy()
+    kn = np.array([k[t, :, L[t] - 1].float().cpu().numpy().reshape(-1) for t in range(wl.n_tokens)])
+    H.assert_close("k_new", kn, ref["k_new"].reshape(wl.n_tokens, -1))
+
+
+def test_gptoss_layer_vs_oracle():
+    wl = synth.WORKLOADS["gptoss_layer"]
+    inp, ref = H.make_inputs_with_margin(wl, 2)
+    res = H.run_temporal_layer(inp, H.dims(wl.shape))
+    errs = _check_layer(inp, ref, res, wl.n_tokens)
+    print("gptoss_layer", {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("window", [0, 16, 200])
+def test_ragged_lengths_and_windows(window):
+    """Sequence lengths at tile and chunk edges (1, 31, 32, 33, 511, 512, 513, 1100)."""
+    wl = synth.WORKLOADS["tiny"].with_(n_tokens=8, kv_len=1200, kv_cap=1200)
+    for a in range(20):
+        inp = H.make_inputs(wl, 3, [a])
+        inp.kv_len.copy_(torch.tensor([1, 31, 32, 33, 511, 512, 513, 1100], dtype=torch.int32))
+        # override the layer's window
+        lay = inp.sgp_layers()[0]
+        lay.window = window
+        w = {n: (v.cpu() if v is not None else None) for n, v in inp.weights[0].items()}
+        k, v = synth.kv_cache(wl, 0, inp.seed, "cpu")
+        ref = O.layer(wl.shape, w, O.f64(inp.x), inp.kv_len.cpu().numpy(), O.f64(k), O.f64(v),
+                      window)
+        if min(O.topk_margin(z, wl.shape.top_k) for z in ref["logits"]) >= H.MARGIN:
+            break
+    d = H.dims(wl.shape, sgp.PATH_TC)
+    ws = H.workspace(d, wl.n_tokens, wl.cap)
+    out = torch.empty_like(inp.x)
+    bufs, st = H.dump_buffers(wl.shape, wl.n_tokens)
+    sgp.sgp_layer_temporal(d, lay, inp.kv_len, inp.x, out, wl.n_tokens, None, None, ws, st)
+    assert sgp.sgp_status_from_workspace(ws) == sgp.SGP_OK
+    H.assert_close("o", bufs["o"], ref["o"])
+    H.assert_close("x_next", out, ref["x_next"])
+
+
+def test_invalid_arguments_are_rejected():
+    wl = synth.WORKLOADS["tiny"]
+    inp = H.make_inputs(wl, 4)
+    d = H.dims(wl.shape)
+    ws = H.workspace(d, wl.n_tokens, wl.cap)
+    out = torch.empty_like(inp.x)
+    lay = inp.sgp_layers()[0]
+    bad = H.dims(wl.shape)
+    bad.head_dim = 32
+    with pytest.raises(sgp.SgpError) as e:
+        sgp.sgp_layer_temporal(bad, lay, inp.kv_len, inp.x, out, wl.n_tokens, None, None, ws)
+    assert e.value.code == sgp.SGP_ERR_INVALID_ARG
+    small = ws[: ws.numel() // 2]
+    with pytest.raises(sgp.SgpError) as e:
+        sgp.sgp_layer_temporal(d, lay, inp.kv_len, inp.x, out, wl.n_tokens, None, None, small)
+    assert e.value.code == sgp.SGP_ERR_INVALID_ARG
+
+
+def test_out_of_range_kv_len_is_reported_not_faulted():
+    wl = synth.WORKLOADS["tiny"]
+    inp = H.make_inputs(wl, 5)
+    inp.kv_len[3] = wl.cap + 7          # beyond the cache: kernels must skip and report
+    res = H.run_temporal_layer(inp, H.dims(wl.shape), dump=False)
+    assert res["status"] == sgp.SGP_ERR_DEVICE_BOUNDS

@@ -1,0 +1,158 @@
+"""GPU tests of the spatial pipeline through the C ABI: pipelined output bit-identical
+to temporal output for several microbatch counts, stage counts and cuts; the task DAG
+equal to the schedule model's; device-side failures reported as status codes."""
+import numpy as np
+import pytest
+import torch
+
+from intra_spatial_pipelining_gb300 import sgp, synth
+from oracle import schedule as S
+from tests import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+def _splits(n_stages):
+    info = sgp.sgp_device_info_get()
+    a = max(1, info.sm_alignment)
+    N = info.sm_count
+    if n_stages == 1:
+        return [N]
+    if n_stages == 2:
+        pa = max(a, (N // 2 // a) * a)
+        return [pa, ((N - pa) // a) * a]
+    p = max(a, (N // 3 // a) * a)
+    return [p, p, ((N - 2 * p) // a) * a]
+
+
+def _stack_inputs(n_layers, kv_len, seed, n_tokens=64):
+    wl = synth.WORKLOADS["gptoss_36l"].with_(n_layers=n_layers, kv_len=kv_len, n_tokens=n_tokens)
+    return wl, H.make_inputs(wl, seed)
+
+
+def _temporal(inp, d):
+    wl = inp.wl
+    T = wl.n_tokens
+    inp.reset_caches()
+    ws = H.workspace(d, T, wl.cap)
+    out = torch.empty_like(inp.x)
+    tki = torch.zeros(wl.n_layers, T, wl.shape.top_k, dtype=torch.int32, device="cuda")
+    tkw = torch.zeros(wl.n_layers, T, wl.shape.top_k, dtype=torch.float32, device="cuda")
+    sgp.sgp_stack_temporal(d, inp.sgp_layers(), inp.kv_len, inp.x, out, T, tki, tkw, ws)
+    assert sgp.sgp_status_from_workspace(ws) == sgp.SGP_OK
+    caches = [(k.clone(), v.clone()) for k, v in inp.caches]
+    return out, tki, tkw, caches
+
+
+def _pipelined(inp, d, n_stages, micro, opts=None, reps=2):
+    wl = inp.wl
+    T = wl.n_tokens
+    p = sgp.sgp_pipeline_create(d, _splits(n_stages), n_stages, micro, T, wl.cap, opts)
+    try:
+        out = torch.empty_like(inp.x)
+        tki = torch.zeros(wl.n_layers, T, wl.shape.top_k, dtype=torch.int32, device="cuda")
+        tkw = torch.zeros(wl.n_layers, T, wl.shape.top_k, dtype=torch.float32, device="cuda")
+        for _ in range(reps):       # replays of the same graph give the same result
+            inp.reset_caches()
+            sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, T, tki, tkw)
+            st = sgp.sgp_pipeline_sync(p)
+            assert st == sgp.SGP_OK, sgp.sgp_status_string(st)
+        tasks = sgp.sgp_pipeline_tasks(p)
+    finally:
+        sgp.sgp_pipeline_destroy(p)
+    return out, tki, tkw, tasks
+
+
+def test_tiny_pipeline_bit_identical():
+    wl = synth.WORKLOADS["tiny"].with_(n_layers=2, layer_pattern="alternate", window=64)
+    inp = H.make_inputs(wl, 7)
+    d = H.dims(wl.shape)
+    ref = _temporal(inp, d)
+    got = _pipelined(inp, d, 2, 4)
+    assert torch.equal(got[0], ref[0])
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+
+
+@pytest.mark.parametrize("n_stages,micro", [(1, 64), (2, 32), (2, 16), (3, 16)])
+def test_gptoss_stack_pipeline_bit_identical(n_stages, micro):
+    wl, inp = _stack_inputs(4, 1024, 8)
+    d = H.dims(wl.shape)
+    ref = _temporal(inp, d)
+    got = _pipelined(inp, d, n_stages, micro)
+    assert torch.equal(got[0], ref[0]), "x_out differs"
+    assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2]), "routing differs"
+    for (k0, v0), (k1, v1) in zip(ref[3], inp.caches):
+        assert torch.equal(k0, k1) and torch.equal(v0, v1), "KV append differs"
+
+
+def test_task_dag_matches_schedule_model():
+    wl, inp = _stack_inputs(3, 256, 9, n_tokens=32)
+    d = H.dims(wl.shape)
+    _, _, _, tasks = _pipelined(inp, d, 2, 8, reps=1)
+    model = S.build_tasks(3, 4, 2)
+    assert len(tasks) == len(model)
+    for got, m in zip(tasks, model):
+        assert got[0] == m["stage"] - 1 and got[1] == m["layer"] and got[2] == m["micro"]
+        assert got[3] == (m["data"][0] if m["data"] else -1)
+        assert got[4] == (m["stage_pred"] if m["stage_pred"] is not None else -1)
+
+
+def test_macro_cut_bit_identical():
+    """Full-attention FMHA alone on stage 0, everything else (including sliding-window
+    attention) on stage 1: tasks span layer boundaries."""
+    wl, inp = _stack_inputs(4, 1024, 10)
+    d = H.dims(wl.shape)
+    full = [1] * sgp.N_OPS
+    full[2] = 0
+    cut = [full, [1] * sgp.N_OPS]
+    ref = _temporal(inp, d)
+    got = _pipelined(inp, d, 2, 32, sgp.make_opts(stage_of_op=cut))
+    assert torch.equal(got[0], ref[0])
+
+
+def test_handoff_check_reports_missing_publish():
+    wl, inp = _stack_inputs(2, 256, 11, n_tokens=16)
+    d = H.dims(wl.shape)
+    p = sgp.sgp_pipeline_create(d, _splits(2), 2, 8, 16, wl.cap,
+                                sgp.make_opts(fault_inject=1, fault_task=0))
+    try:
+        out = torch.empty_like(inp.x)
+        sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, 16)
+        assert sgp.sgp_pipeline_sync(p) == sgp.SGP_ERR_HANDOFF
+        assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK     # status cleared after reading
+    finally:
+        sgp.sgp_pipeline_destroy(p)
+
+
+def test_bounded_wait_times_out_and_reports():
+    wl, inp = _stack_inputs(1, 256, 12, n_tokens=16)
+    d = H.dims(wl.shape, sgp.PATH_TC)
+    p = sgp.sgp_pipeline_create(d, _splits(2), 2, 8, 16, wl.cap,
+                                sgp.make_opts(fault_inject=2, wait_timeout_ns=20_000_000))
+    try:
+        out = torch.empty_like(inp.x)
+        sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, 16)
+        assert sgp.sgp_pipeline_sync(p) == sgp.SGP_ERR_TIMEOUT
+        # the context stays usable: a clean pipeline runs afterwards
+        q = sgp.sgp_pipeline_create(d, _splits(2), 2, 8, 16, wl.cap)
+        sgp.sgp_pipeline_run(q, inp.sgp_layers(), inp.kv_len, inp.x, out, 16)
+        assert sgp.sgp_pipeline_sync(q) == sgp.SGP_OK
+        sgp.sgp_pipeline_destroy(q)
+    finally:
+        sgp.sgp_pipeline_destroy(p)
+
+
+def test_stage_times_and_balancer_pick_a_legal_split():
+    wl, inp = _stack_inputs(2, 1024, 13)
+    d = H.dims(wl.shape)
+    info = sgp.sgp_device_info_get()
+    out = torch.empty_like(inp.x)
+    best, rows = sgp.sgp_pipeline_balance(d, inp.sgp_layers(), inp.kv_len, inp.x, out,
+                                          wl.n_tokens, 32, wl.cap, quantum=32, reps=2)
+    q = max(32, info.sm_alignment)
+    legal = sgp.sgp_enumerate_splits(info.sm_count, q, max(q, info.sm_min_partition))
+    assert best in legal and [r[0] for r in rows] == legal
+    assert all(r[1] > 0 and r[2] > 0 for r in rows)
+    i = [r[0] for r in rows].index(best)
+    assert max(rows[i][1:]) == min(max(r[1:]) for r in rows)
+    print("balance", best, rows)
