@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Benchmark of the 36-layer GPT-OSS-120B-shaped decode iteration on GB300.
+
+One step = one decode iteration: 64 sequences (one new token each) through 36
+layers that alternate sliding-window-128 and full attention over a KV cache of
+8,192 positions, run as the two-stage intra-GPU spatial pipeline (stage A:
+RMSNorm + QKV + attention; stage B: o-proj + router + SwiGLU experts +
+combine) through the C ABI.  The same work run temporally (every kernel on all
+SMs) is reported beside it.  Inputs are seeded synthetic tensors (random
+weights of the per-GPU slice shape; no trained checkpoint) resident in HBM; the
+working set (about 48 GB) is far larger than L2, so no flush is needed between
+steps.
+
+`python bench.py [--gpus N] [--steps K] [--warmup W]` prints one JSON line.
+Under torchrun every rank runs an independent replica (the path has no
+cross-GPU exchange) and rank 0 prints the aggregate.
+`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "36-layer decode iteration µs, tokens/s/GPU; DRAM GB/s as % of HBM peak"
+UNIT = "tokens/s"
+ATTN_SRC = os.path.join(ROOT, "intra_spatial_pipelining_gb300", "csrc", "k_attention.cu")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_decode_kernel_gptoss_36l.md")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="sgp", choices=["sgp", "reference"])
+    ap.add_argument("--workload", default="gptoss_36l")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--kv-len", type=int, default=None, help="override the KV length")
+    ap.add_argument("--stages", type=int, default=2)
+    ap.add_argument("--micro", type=int, default=None, help="sequences per microbatch")
+    ap.add_argument("--split", default="auto", help="'auto' (balancer) or comma list of SMs")
+    ap.add_argument("--cut", default="layer", choices=["layer", "macro"])
+    ap.add_argument("--no-temporal", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------
+def workload(args):
+    from intra_spatial_pipelining_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    kw = {}
+    if args.layers:
+        kw["n_layers"] = args.layers
+    if args.kv_len:
+        kw["kv_len"] = args.kv_len
+    return wl.with_(**kw) if kw else wl
+
+
+def describe(wl, extra):
+    s = wl.shape
+    cfg = {"workload": (f"{wl.name}: {wl.n_layers} layers "
+                        f"({'alternating sliding-' + str(wl.window) + '/full' if wl.layer_pattern == 'alternate' else 'full'}"
+                        f" attention), {wl.n_tokens} sequences, KV {wl.kv_len}, hidden {s.hidden}, "
+                        f"{s.n_q_heads}q/{s.n_kv_heads}kv heads x {s.head_dim}, {s.n_experts} experts "
+                        f"top-{s.top_k}, {s.n_local_experts} local experts, SwiGLU {s.inter}"),
+           "layers": wl.n_layers, "n_tokens": wl.n_tokens, "kv_len": wl.kv_len,
+           "l2": "inputs larger than L2 (no flush)"}
+    cfg.update(extra)
+    return cfg
+
+
+def algorithmic_bytes(wl):
+    """Unique bytes of one iteration: every weight and KV element read once, the KV append,
+    and the per-layer activations (x in/out, a, q, o, h, u, routed rows)."""
+    s = wl.shape
+    per_layer_w = 2 * (s.qkv_rows * s.hidden + s.hidden * s.q_width + s.n_experts * s.hidden
+                       + s.n_local_experts * 3 * s.hidden * s.inter + 2 * s.hidden)
+    T = wl.n_tokens
+    act = 2 * T * (6 * s.hidden + 2 * s.q_width) + T * s.top_k * (2 * s.hidden + 2 * s.inter + 4 * s.hidden)
+    tot = 0
+    for l in range(wl.n_layers):
+        w = wl.layer_window(l)
+        span = min(w, wl.kv_len) if w else wl.kv_len
+        kv = T * s.n_kv_heads * span * s.head_dim * 2 * 2
+        tot += per_layer_w + kv + T * s.n_kv_heads * s.head_dim * 2 * 2 + act
+    return tot
+
+
+def attn_bytes(wl, layer):
+    s = wl.shape
+    w = wl.layer_window(layer)
+    span = min(w, wl.kv_len) if w else wl.kv_len
+    T = wl.n_tokens
+    return T * s.n_kv_heads * span * s.head_dim * 4 + T * s.q_width * 4
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def read_traffic():
+    """ncu DRAM bytes per launch of the attention kernel from the committed summary, or None
+    when the summary is missing or was taken from a different kernel source."""
+    try:
+        txt = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None
+    src_hash = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
+    h = t = None
+    for line in txt.splitlines():
+        if line.startswith("kernel_source_sha256_16:"):
+            h = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_full_layer_launch:"):
+            t = float(line.split(":", 1)[1].strip())
+    return t if (h == src_hash and t) else None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle (bounded sample)
+# ------------------------------------------------------------------------------------------
+class OracleSample:
+    """The fp64 oracle on a bounded sample: n_tok sequences through one sliding and one full
+    layer.  Inputs are drawn once; run() times only the oracle and scales to the metric:
+    tokens/s = 1 / (time per token through all layers)."""
+
+    def __init__(self, wl, seed, n_tok=1, layer_pair=(0, 1)):
+        import numpy as np
+
+        from intra_spatial_pipelining_gb300 import synth
+        from oracle import layer as O
+        self.O, self.wl, self.n_tok, self.layer_pair = O, wl, n_tok, layer_pair
+        self.x = O.f64(synth.x_in(wl, seed))[:n_tok]
+        self.kvl = synth.kv_len(wl, seed).numpy()[:n_tok]
+        self.layers = []
+        for l in layer_pair:
+            w = synth.layer_weights(wl, l, seed)
+            caches = [synth.kv_cache_rows(wl, l, seed, b) for b in range(n_tok)]
+            kc = np.stack([O.f64(k) for k, _ in caches])
+            vc = np.stack([O.f64(v) for _, v in caches])
+            self.layers.append((l, w, kc, vc))
+        self.threads = os.cpu_count()
+
+    def run(self):
+        x = self.x
+        t0 = time.perf_counter()
+        for l, w, kc, vc in self.layers:
+            r = self.O.layer(self.wl.shape, w, x, self.kvl, kc.copy(), vc.copy(),
+                             self.wl.layer_window(l))
+            x = r["x_next"]
+        secs = time.perf_counter() - t0
+        per_token_all = secs / self.n_tok * self.wl.n_layers / len(self.layer_pair)
+        return 1.0 / per_token_all, secs
+
+    def describe(self, secs):
+        return (f"{self.n_tok} sequence(s) through 1 sliding + 1 full layer per step "
+                f"({secs:.1f} s, fp64 numpy, BLAS default threads), scaled to "
+                f"{self.wl.n_layers} layers")
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = workload(args)
+    smp = OracleSample(wl, args.seed)
+    for _ in range(args.warmup):
+        smp.run()
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        v, t = smp.run()
+        vals.append(v)
+        secs += t
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": describe(wl, {"arm": "fp64 CPU oracle"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
+                             "sample": smp.describe(secs / args.steps)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------
+def run_sgp(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from intra_spatial_pipelining_gb300 import sgp, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    sgp.lib()
+    wl = workload(args)
+    s = wl.shape
+    T = wl.n_tokens
+    seed = args.seed + 1000 * rank
+
+    # ---- inputs (resident in HBM) ----
+    synth._CHUNK = 1 << 28
+    x = synth.x_in(wl, seed, dev)
+    kv_len = synth.kv_len(wl, seed, dev)
+    weights = [synth.layer_weights(wl, l, seed, dev) for l in range(wl.n_layers)]
+    caches = [synth.kv_cache(wl, l, seed, dev) for l in range(wl.n_layers)]
+    layers = sgp.layer_array([sgp.make_layer(w, k, v, wl.layer_window(l))
+                              for l, (w, (k, v)) in enumerate(zip(weights, caches))])
+    d = sgp.make_dims(s)
+    out = x.clone()
+    info = sgp.sgp_device_info_get()
+    N = info.sm_count
+    stream = torch.cuda.current_stream()
+
+    # ---- pipeline configuration ----
+    n_stages = args.stages
+    micro = args.micro or (T // max(1, wl.microbatches))
+    opts = None
+    if args.cut == "macro":
+        full = [1] * sgp.N_OPS
+        full[sgp.OPS.index("attention")] = 0
+        opts = sgp.make_opts(stage_of_op=[full, [1] * sgp.N_OPS])
+    balance_rows = None
+    if n_stages == 1:
+        split = [N]
+    elif args.split == "auto" and n_stages == 2:
+        best, balance_rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro,
+                                                      wl.cap, quantum=8, reps=3, opts=opts)
+        # check the model's pick against full pipelined runs of the best few candidates
+        ranked = sorted(balance_rows, key=lambda r: max(r[1], r[2]))[:4]
+        best_t = None
+        for pa, _, _ in ranked:
+            p = sgp.sgp_pipeline_create(d, [pa, N - pa], 2, micro, T, wl.cap, opts)
+            sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
+            sgp.check(sgp.sgp_pipeline_sync(p), "pipeline")
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(3):
+                sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
+            t1.record(stream)
+            t1.synchronize()
+            sgp.check(sgp.sgp_pipeline_sync(p), "pipeline")
+            sgp.sgp_pipeline_destroy(p)
+            ms = t0.elapsed_time(t1) / 3
+            if best_t is None or ms < best_t:
+                best_t, best = ms, pa
+        split = [best, N - best]
+    elif args.split == "auto":
+        a = max(1, info.sm_alignment)
+        p0 = max(a, (N // 3 // a) * a)
+        split = [p0, p0, N - 2 * p0]
+    else:
+        split = [int(v) for v in args.split.split(",")]
+
+    def make(nst, spl, mb, o):
+        return sgp.sgp_pipeline_create(d, spl, nst, mb, T, wl.cap, o)
+
+    def time_runs(p, steps, warmup):
+        for _ in range(warmup):
+            sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
+        sgp.check(sgp.sgp_pipeline_sync(p), "warmup")
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        sgp.check(sgp.sgp_pipeline_sync(p), "timed runs")
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+            dist.barrier()
+        return ms / steps
+
+    pipe = make(n_stages, split, micro, opts)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ms_pipe = time_runs(pipe, args.steps, args.warmup)
+    clk = clocks.stop()
+
+    ms_temp = None
+    temporal = None
+    if not args.no_temporal:
+        tp = make(1, [N], T, None)
+        ms_temp = time_runs(tp, args.steps, args.warmup)
+        sgp.sgp_pipeline_destroy(tp)
+
+    # ---- e2e through the public API: pinned H2D of the step's input, D2H of its result ----
+    e2e = None
+    if not args.no_e2e:
+        hx = x.cpu().pin_memory()
+        hout = torch.empty_like(hx).pin_memory()
+        x_dev = torch.empty_like(x)
+        for _ in range(args.warmup):
+            x_dev.copy_(hx, non_blocking=True)
+            sgp.sgp_pipeline_run(pipe, layers, kv_len, x_dev, out, T)
+            hout.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            x_dev.copy_(hx, non_blocking=True)
+            sgp.sgp_pipeline_run(pipe, layers, kv_len, x_dev, out, T)
+            hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        sgp.check(sgp.sgp_pipeline_sync(pipe), "e2e runs")
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": world * T / (ms_e2e * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": hx.numel() * hx.element_size(),
+               "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+               "ms_per_step": ms_e2e}
+    n_tasks = len(sgp.sgp_pipeline_tasks(pipe))
+    sgp.sgp_pipeline_destroy(pipe)
+
+    # ---- roofline of the dominant kernel (full-attention decode), timed alone ----
+    full_layer = next((l for l in range(wl.n_layers) if wl.layer_window(l) == 0), 0)
+    lay = layers[full_layer]
+    nbytes = sgp.sgp_workspace_bytes(d, T, wl.cap)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    sgp.sgp_layer_temporal(d, lay, kv_len, x, out, T, None, None, ws, None, stream)
+    reps = max(5, args.steps)
+    for _ in range(3):
+        sgp.sgp_layer_op(d, lay, sgp.OPS.index("attention"), kv_len, x, out, T, ws, stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        sgp.sgp_layer_op(d, lay, sgp.OPS.index("attention"), kv_len, x, out, T, ws, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sgp.check(sgp.sgp_status_from_workspace(ws), "attention launches")
+    attn_ms = e0.elapsed_time(e1) / reps
+    peak, peak_kind = read_peaks()
+    ab = attn_bytes(wl, full_layer)
+    achieved = ab / (attn_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": read_traffic(),
+                "kernel": "attn_decode_kernel (full-attention layer)",
+                "algorithmic_bytes_per_launch": ab, "launch_us": attn_ms * 1e3,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs copy bandwidth)"}
+
+    if rank != 0:
+        return
+    total_bytes = algorithmic_bytes(wl)
+    value = world * T / (ms_pipe * 1e-3)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        smp = OracleSample(wl, args.seed)
+        v, secs = smp.run()
+        cpu = {"value": v, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
+               "sample": smp.describe(secs)}
+    iter_us = ms_pipe * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_pipe, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": describe(wl, {"mode": f"spatial pipeline, {n_stages} stages",
+                                "cut": args.cut, "sm_split": split,
+                                "microbatches": T // micro, "microbatch": micro,
+                                "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+        "iteration_us": iter_us,
+        "tokens_per_s_per_user": 1e6 / iter_us,
+        "dram_algorithmic_gbs": total_bytes / (ms_pipe * 1e-3) / 1e9,
+        "dram_pct_of_peak": 100.0 * total_bytes / (ms_pipe * 1e-3) / 1e9 / peak,
+        "temporal": None if ms_temp is None else {
+            "iteration_us": ms_temp * 1e3, "tokens_per_s": world * T / (ms_temp * 1e-3),
+            "dram_pct_of_peak": 100.0 * total_bytes / (ms_temp * 1e-3) / 1e9 / peak,
+            "pipeline_speedup": ms_temp / ms_pipe},
+        "balance": None if balance_rows is None else [
+            {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in balance_rows],
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * n_tasks_kernels(wl, T // micro),
+        "clocks": clk,
+        "algorithmic_bytes_per_step": total_bytes,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def n_tasks_kernels(wl, m):
+    """Kernels one iteration launches: 9 ops per layer and microbatch, plus the finishing
+    kernel of each of the 4 projections that run on tensor cores."""
+    from intra_spatial_pipelining_gb300 import sgp
+    return wl.n_layers * (sgp.N_OPS + 4) * m
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_sgp(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

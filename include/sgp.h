@@ -186,6 +186,16 @@ int sgp_stack_temporal(const sgp_dims* dims, const sgp_layer* layers, int n_laye
                        int32_t* topk_idx, float* topk_w, void* workspace, size_t ws_bytes,
                        sgp_stream_t stream);
 
+/* Launches op `op` (SGP_OP_*) of one temporal layer alone, on `stream`.  Its inputs are what
+ * `workspace` holds from an earlier sgp_layer_temporal with the same arguments (for example
+ * the normalised activations of op 0), so a sequence of ops 0..8 equals one
+ * sgp_layer_temporal call.  Used to time and profile single kernels.  The zeroed counters
+ * of the workspace must hold zero, as every kernel leaves them.  Arguments and returns as
+ * sgp_layer_temporal. */
+int sgp_layer_op(const sgp_dims* dims, const sgp_layer* layer, int op, const int32_t* kv_len,
+                 const void* x_in, void* x_out, int n_tokens, void* workspace, size_t ws_bytes,
+                 sgp_stream_t stream);
+
 /* Synchronises `stream`, returns the device status recorded in `workspace` since the last
  * read (SGP_OK, SGP_ERR_TIMEOUT, SGP_ERR_HANDOFF, SGP_ERR_DEVICE_BOUNDS) and clears it.
  * Returns SGP_ERR_CUDA if the copy fails. */

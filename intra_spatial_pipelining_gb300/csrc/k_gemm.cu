@@ -3,11 +3,17 @@
 //
 // Decode gives few tokens per weight matrix (64 per layer, 16-64 per expert slot), so the
 // contraction is "swap-AB": the weight tile is the MMA's M = 128 operand and the tokens are
-// its N (16..256) operand.  Weights stream from HBM through a TMA -> shared-memory ring
-// (128-byte swizzle, L2 evict-first), one elected thread issues tcgen05.mma into a TMEM
-// accumulator, and the epilogue reads TMEM with tcgen05.ld.  Each (group, 128-row tile,
-// K segment) is one CTA; K segments are summed in a fixed order by the last CTA of the
-// tile, so results are independent of the grid size and of the number of tokens.
+// its N (16..256) operand.  Two kernels per projection:
+//   gemm_tc_kernel   one CTA per (group, 128-row weight tile, K segment): weights stream
+//                    HBM -> shared memory through a TMA ring (128-byte swizzle, L2
+//                    evict-first), one elected thread issues tcgen05.mma into a TMEM
+//                    accumulator, and the fp32 tile leaves with one TMA bulk store per pass
+//                    into a partial-sum buffer.  Nothing else: no scalar stores, no
+//                    cross-CTA protocol.
+//   gemm_finish_kernel  every thread owns 8 consecutive outputs of one token: it sums the
+//                    K segments in segment order (fixed, so results never depend on the
+//                    grid or the token count) and applies the fused epilogue with 16-byte
+//                    loads and stores.
 #include <algorithm>
 
 #include "kernels.h"
@@ -21,49 +27,6 @@ constexpr int kStageA = 128 * 128;  // A tile: 128 rows x 64 bf16
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-// Stores one finished output (feature f of the group, output row trow).
-__device__ __forceinline__ void epi_store(const EpiArgs& e, const KCtx& c, int f, int trow,
-                                          float v) {
-    if (f >= e.n_out) return;
-    switch (e.mode) {
-        case EPI_QKV: {
-            if (f < e.q_width) {
-                e.q[(size_t)trow * e.q_width + f] = __float2bfloat16_rn(v);
-            } else {
-                int r = f - e.q_width;
-                int which = r / (e.nkv * e.d);  // 0 = k, 1 = v
-                int kh = (r / e.d) % e.nkv;
-                int dd = r % e.d;
-                int pos = e.kv_len[trow] - 1;
-                if (pos < 0 || pos >= e.cap) {
-                    report(c, ST_BOUNDS, (uint32_t)pos);
-                    return;
-                }
-                bf16* cache = which == 0 ? e.kc : e.vc;
-                cache[(((size_t)trow * e.nkv + kh) * e.cap + pos) * e.d + dd] =
-                    __float2bfloat16_rn(v);
-            }
-            break;
-        }
-        case EPI_RESID: {
-            size_t o = (size_t)trow * e.ld + f;
-            e.out[o] = __float2bfloat16_rn(__bfloat162float(e.resid[o]) + v);
-            break;
-        }
-        case EPI_F32:
-            e.out_f32[(size_t)trow * e.ld + f] = v;
-            break;
-        default:
-            break;
-    }
-}
-
-__device__ __forceinline__ void epi_swiglu(const EpiArgs& e, int i, int trow, float gate,
-                                           float up) {
-    if (i >= e.n_out) return;
-    e.out[(size_t)trow * e.ld + i] = __float2bfloat16_rn(silu_f(gate) * up);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ GemmProblem P, const KCtx ctx) {
     extern __shared__ uint8_t smem_raw[];
@@ -71,11 +34,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = P.stages;
     const int stage_bytes = kStageA + P.n_cap * 128;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P.ring_bytes);
     uint64_t* empty = full + S;
     uint64_t* accbar = empty + S;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accbar + 1);
-    int* sh_flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] error, [1] last-CTA
+    int* sh_err = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     task_begin(ctx);
@@ -88,18 +51,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (P.serpentine) g = P.n_groups - 1 - g;
     const int kb0 = (ks * P.kb_total) / P.ksplit;
     const int kb1 = ((ks + 1) * P.kb_total) / P.ksplit;
-    // tma_r0: first activation row in the B tensor map; out_r0: first output row of the
-    // epilogue; lr0: first row of the partial-sum buffer.  Dense: the map starts at this
-    // microbatch's first token row.  Grouped: rows of the slot-sorted matrix.
-    int tma_r0, out_r0, n, lr0;
+    // tma_r0: first activation row in the B tensor map (dense: the map starts at this
+    // microbatch's first token; grouped: rows of the slot-sorted matrix); lr0: first row of
+    // the partial-sum buffer.
+    int tma_r0, n, lr0;
     if (P.group_offsets != nullptr) {
         tma_r0 = P.group_offsets[g];
         n = P.group_offsets[g + 1] - tma_r0;
-        out_r0 = tma_r0;
         lr0 = tma_r0;
     } else {
         tma_r0 = 0;
-        out_r0 = P.row0;
         n = P.nrows;
         lr0 = 0;
     }
@@ -125,8 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(accbar, 1);
-        sh_flags[0] = 0;
-        sh_flags[1] = 0;
+        *sh_err = 0;
         fence_barrier_init();
         prefetch_tensormap(&P.tmA);
         prefetch_tensormap(&P.tmB);
@@ -154,13 +114,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- TMA producer ----
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            for (int i = 0; i < nk && !*(volatile int*)&sh_flags[0]; ++i) {
+            for (int i = 0; i < nk && !*(volatile int*)sh_err; ++i) {
                 const uint32_t it = it0 + i;
                 const int s = it % S;
                 const uint32_t j = it / S;
                 if (j > 0 && !mbar_wait(&empty[s], (j - 1) & 1, ctx.timeout_ns)) {
                     report(ctx, ST_TIMEOUT, 1);
-                    atomicExch(&sh_flags[0], 1);
+                    atomicExch(sh_err, 1);
                     break;
                 }
                 if ((ctx.fault & FAULT_DROP_TMA) && blockIdx.x == 0 && pass == 0 && i == 0)
@@ -186,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t j = it / S;
                 if (!mbar_wait(&full[s], j & 1, ctx.timeout_ns)) {
                     report(ctx, ST_TIMEOUT, 2);
-                    atomicExch(&sh_flags[0], 1);
+                    atomicExch(sh_err, 1);
                     okk = false;
                     break;
                 }
@@ -203,13 +163,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
 
-        // ---- epilogue: TMEM -> fp32 partial sums ----
+        // ---- TMEM -> shared memory [token][128 rows] fp32 -> one bulk store ----
         bool ok = mbar_wait(accbar, (uint32_t)pass & 1u, ctx.timeout_ns);
         if (!ok) {
             if (lane == 0) report(ctx, ST_TIMEOUT, 3);
-            atomicExch(&sh_flags[0], 1);
+            atomicExch(sh_err, 1);
         }
         ok = __all_sync(0xffffffffu, ok);
+        float* Ts = reinterpret_cast<float*>(smem);  // the ring is idle: all MMAs completed
         if (ok) {
             tc_fence_after();
             const int row = warp * 32 + lane;
@@ -219,23 +180,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_x16(tbase + (uint32_t)cc, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int tok = c0 + cc + q;
-                    if (tok < n) {
-                        const size_t lr = (size_t)(lr0 + tok);
-                        P.partial[(((size_t)ks * P.R + lr) * P.m_tiles + mt) * 128 + row] =
-                            __uint_as_float(v[q]);
-                    }
-                }
+                for (int q = 0; q < 16; ++q) Ts[(cc + q) * 128 + row] = __uint_as_float(v[q]);
             }
         }
         tc_fence_before();
+        fence_proxy_async();
         __syncthreads();
-        if (sh_flags[0]) break;
+        if (*sh_err) break;
+        const int nv = min(np, n - c0);  // valid tokens of this pass
+        if (tid == 0) {
+            bulk_store(P.partial + (((size_t)mt * P.ksplit + ks) * P.R + lr0 + c0) * 128, Ts,
+                       (uint32_t)nv * 512u);
+            bulk_commit();
+            bulk_wait_all();  // shared memory is reused by the next pass; results complete
+        }
+        __syncthreads();
     }
 
     // ---- teardown ----
-    if (sh_flags[0] && warp == 0 && lane == 0) {
+    if (*sh_err && warp == 0 && lane == 0) {
         // drain TMA loads still in flight into this CTA's shared memory (bounded)
         for (int s = 0; s < S; ++s)
             if (issued_mask & (1u << s))
@@ -243,48 +206,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, ncols);
-    if (sh_flags[0]) {
-        task_end(ctx);
-        return;
-    }
+    task_end(ctx);
+}
 
-    // ---- K-segment reduction (fixed order) by the last CTA of the tile ----
-    __threadfence();
-    __syncthreads();
-    uint32_t* cnt = &P.tile_cnt[g * P.m_tiles + mt];
-    if (tid == 0) {
-        const uint32_t prev = atomicAdd(cnt, 1u);
-        sh_flags[1] = (prev == (uint32_t)P.ksplit - 1) ? 1 : 0;
-        if (sh_flags[1]) *cnt = 0;
-    }
-    __syncthreads();
-    if (sh_flags[1]) {
-        __threadfence();
-        const EpiArgs& e = P.epi;
-        const size_t rstride = (size_t)P.R * P.m_tiles * 128;
-        if (e.mode == EPI_SWIGLU) {
-            const int half = tid >> 6, r = tid & 63;
-            for (int t2 = 0; t2 < n; t2 += 2) {
-                const int tok = t2 + half;
-                if (tok < n) {
-                    const float* base =
-                        P.partial + ((size_t)(lr0 + tok) * P.m_tiles + mt) * 128;
-                    float gsum = 0.f, usum = 0.f;
-                    for (int s2 = 0; s2 < P.ksplit; ++s2) {
-                        gsum += __ldcg(base + s2 * rstride + r);
-                        usum += __ldcg(base + s2 * rstride + 64 + r);
-                    }
-                    epi_swiglu(e, mt * 64 + r, out_r0 + tok, gsum, usum);
-                }
+// ---------------------------------------------------------------------------------------
+// K-segment reduction + fused epilogue: one thread = 8 consecutive outputs of one token.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gemm_finish_kernel(const FinishProblem P, const KCtx ctx) {
+    task_begin(ctx);
+    const EpiArgs& e = P.epi;
+    const bool swiglu = e.mode == EPI_SWIGLU;
+    const int per_tok = swiglu ? 8 : 16;          // 8-output groups per (tile, token)
+    const int total = P.m_tiles * P.rows * per_tok;
+    for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += gridDim.x * blockDim.x) {
+        const int q8 = u % per_tok;
+        const int lr = (u / per_tok) % P.rows;
+        const int mt = u / (per_tok * P.rows);
+        const size_t base = ((size_t)mt * P.ksplit * P.R + lr) * 128;  // (mt, s = 0, lr)
+        const size_t sstride = (size_t)P.R * 128;                     // next K segment
+        const int trow = P.out_row0 + lr;
+        if (swiglu) {
+            const int i0 = mt * 64 + 8 * q8;
+            if (i0 >= e.n_out) continue;
+            float gsum[8], usum[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) gsum[i] = usum[i] = 0.f;
+            for (int s = 0; s < P.ksplit; ++s) {
+                const float4* pg =
+                    reinterpret_cast<const float4*>(P.partial + base + s * sstride + 8 * q8);
+                const float4* pu =
+                    reinterpret_cast<const float4*>(P.partial + base + s * sstride + 64 + 8 * q8);
+                const float4 g0 = __ldcg(pg), g1 = __ldcg(pg + 1), u0 = __ldcg(pu),
+                             u1 = __ldcg(pu + 1);
+                gsum[0] += g0.x; gsum[1] += g0.y; gsum[2] += g0.z; gsum[3] += g0.w;
+                gsum[4] += g1.x; gsum[5] += g1.y; gsum[6] += g1.z; gsum[7] += g1.w;
+                usum[0] += u0.x; usum[1] += u0.y; usum[2] += u0.z; usum[3] += u0.w;
+                usum[4] += u1.x; usum[5] += u1.y; usum[6] += u1.z; usum[7] += u1.w;
             }
-        } else {
-            for (int tok = 0; tok < n; ++tok) {
-                const float* base = P.partial + ((size_t)(lr0 + tok) * P.m_tiles + mt) * 128;
-                float sum = 0.f;
-                for (int s2 = 0; s2 < P.ksplit; ++s2) sum += __ldcg(base + s2 * rstride + tid);
-                epi_store(e, ctx, mt * P.a_tile_stride + tid, out_r0 + tok, sum);
-            }
+            uint4 o;
+            o.x = pack_bf16x2(silu_f(gsum[0]) * usum[0], silu_f(gsum[1]) * usum[1]);
+            o.y = pack_bf16x2(silu_f(gsum[2]) * usum[2], silu_f(gsum[3]) * usum[3]);
+            o.z = pack_bf16x2(silu_f(gsum[4]) * usum[4], silu_f(gsum[5]) * usum[5]);
+            o.w = pack_bf16x2(silu_f(gsum[6]) * usum[6], silu_f(gsum[7]) * usum[7]);
+            *reinterpret_cast<uint4*>(e.out + (size_t)trow * e.ld + i0) = o;
+            continue;
         }
+        const int f0 = mt * 128 + 8 * q8;  // first of the 8 output features
+        if (f0 >= e.n_out) continue;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        for (int s = 0; s < P.ksplit; ++s) {
+            const float4* pp =
+                reinterpret_cast<const float4*>(P.partial + base + s * sstride + 8 * q8);
+            const float4 a = __ldcg(pp), b = __ldcg(pp + 1);
+            v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+            v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+        }
+        if (e.mode == EPI_F32) {
+            float4* o = reinterpret_cast<float4*>(e.out_f32 + (size_t)trow * e.ld + f0);
+            o[0] = make_float4(v[0], v[1], v[2], v[3]);
+            o[1] = make_float4(v[4], v[5], v[6], v[7]);
+            continue;
+        }
+        if (e.mode == EPI_RESID) {
+            float r[8];
+            unpack8(*reinterpret_cast<const uint4*>(e.resid + (size_t)trow * e.ld + f0), r);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] += r[i];
+        }
+        uint4 o;
+        o.x = pack_bf16x2(v[0], v[1]);
+        o.y = pack_bf16x2(v[2], v[3]);
+        o.z = pack_bf16x2(v[4], v[5]);
+        o.w = pack_bf16x2(v[6], v[7]);
+        bf16* dst;
+        if (e.mode == EPI_RESID) {
+            dst = e.out + (size_t)trow * e.ld + f0;
+        } else if (f0 < e.q_width) {  // EPI_QKV: query heads
+            dst = e.q + (size_t)trow * e.q_width + f0;
+        } else {                      // EPI_QKV: append k / v at slot kv_len - 1
+            const int r = f0 - e.q_width;
+            const int which = r / (e.nkv * e.d);
+            const int kh = (r / e.d) % e.nkv;
+            const int pos = e.kv_len[trow] - 1;
+            if (pos < 0 || pos >= e.cap) {
+                report(ctx, ST_BOUNDS, (uint32_t)pos);
+                continue;
+            }
+            bf16* cache = which == 0 ? e.kc : e.vc;
+            dst = cache + (((size_t)trow * e.nkv + kh) * e.cap + pos) * e.d + (r % e.d);
+        }
+        *reinterpret_cast<uint4*>(dst) = o;
     }
     task_end(ctx);
 }
@@ -292,6 +305,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------------
 // CUDA-core GEMV path: one warp per output feature, 8 tokens per pass, 16-byte loads.
 // ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void gemv_store(const EpiArgs& e, const KCtx& c, int f, int trow,
+                                           float v) {
+    if (f >= e.n_out) return;
+    switch (e.mode) {
+        case EPI_QKV: {
+            if (f < e.q_width) {
+                e.q[(size_t)trow * e.q_width + f] = __float2bfloat16_rn(v);
+            } else {
+                const int r = f - e.q_width;
+                const int which = r / (e.nkv * e.d);
+                const int kh = (r / e.d) % e.nkv;
+                const int pos = e.kv_len[trow] - 1;
+                if (pos < 0 || pos >= e.cap) {
+                    report(c, ST_BOUNDS, (uint32_t)pos);
+                    return;
+                }
+                bf16* cache = which == 0 ? e.kc : e.vc;
+                cache[(((size_t)trow * e.nkv + kh) * e.cap + pos) * e.d + (r % e.d)] =
+                    __float2bfloat16_rn(v);
+            }
+            break;
+        }
+        case EPI_RESID: {
+            const size_t o = (size_t)trow * e.ld + f;
+            e.out[o] = __float2bfloat16_rn(__bfloat162float(e.resid[o]) + v);
+            break;
+        }
+        case EPI_F32:
+            e.out_f32[(size_t)trow * e.ld + f] = v;
+            break;
+        default:
+            break;
+    }
+}
+
 __global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KCtx ctx) {
     task_begin(ctx);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -343,10 +391,14 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KC
             }
             if (lane == 0) {
                 for (int i = 0; i < nt; ++i) {
-                    if (P.swiglu)
-                        epi_swiglu(P.epi, f, r0 + t0 + i, a1[i], a2[i]);
-                    else
-                        epi_store(P.epi, ctx, f, r0 + t0 + i, a1[i]);
+                    const int trow = r0 + t0 + i;
+                    if (P.swiglu) {
+                        if (f < P.epi.n_out)
+                            P.epi.out[(size_t)trow * P.epi.ld + f] =
+                                __float2bfloat16_rn(silu_f(a1[i]) * a2[i]);
+                    } else {
+                        gemv_store(P.epi, ctx, f, trow, a1[i]);
+                    }
                 }
             }
         }
@@ -356,15 +408,32 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KC
 
 }  // namespace
 
+size_t gemm_tc_ring_bytes(int n_cap, int stages) {
+    size_t ring = (size_t)stages * (kStageA + n_cap * 128);
+    size_t ts = (size_t)n_cap * 512;  // the accumulator staged as [token][128] fp32
+    return ring > ts ? ring : ts;
+}
+
 size_t gemm_tc_smem_bytes(int n_cap, int stages) {
-    return (size_t)stages * (kStageA + n_cap * 128) + 1024 + 256;
+    return gemm_tc_ring_bytes(n_cap, stages) + 1024 + 256;
 }
 
 int enqueue_gemm_tc(Launcher& L, const GemmProblem& p, const KCtx& c) {
     dim3 grid(p.n_groups * p.m_tiles * p.ksplit), block(kThreads);
+    if ((size_t)p.ring_bytes != gemm_tc_ring_bytes(p.n_cap, p.stages))
+        return (int)cudaErrorInvalidValue;
     void* args[] = {(void*)&p, (void*)&c};
     return L.launch((const void*)gemm_tc_kernel, grid, block,
                     gemm_tc_smem_bytes(p.n_cap, p.stages), args);
+}
+
+int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c) {
+    const int per_tok = p.epi.mode == EPI_SWIGLU ? 8 : 16;
+    const long total = (long)p.m_tiles * p.rows * per_tok;
+    const int blocks = (int)std::min<long>((total + 255) / 256, 4096);
+    void* args[] = {(void*)&p, (void*)&c};
+    return L.launch((const void*)gemm_finish_kernel, dim3(std::max(1, blocks)), dim3(256), 0,
+                    args);
 }
 
 int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c) {

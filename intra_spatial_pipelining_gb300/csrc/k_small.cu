@@ -65,53 +65,92 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterProblem P, cons
     const int nv = P.H >> 3;
     const int ntok = min(kRouterTok, P.nrows - tg * kRouterTok);
 
-    // (1) RMSNorm of this group's tokens, warp w -> token w
+    // Router weight row of this warp's expert: issue its loads first (registers), so they
+    // overlap the normalisation below.  H <= kMaxVec * 256.
+    constexpr int kMaxVec = 4;  // 16-byte vectors per lane per block of 32 * kMaxVec
+    const int e = blockIdx.y * 8 + warp;
+    const bool has_e = e < P.E;
+    const uint4* wrow = reinterpret_cast<const uint4*>(P.Wr + (size_t)(has_e ? e : 0) * P.H);
+
+    // (1) RMSNorm of this group's tokens, warp w -> token w (row kept in registers)
     if (warp < ntok) {
         const int row = P.row0 + tg * kRouterTok + warp;
         const uint4* h = reinterpret_cast<const uint4*>(P.h + (size_t)row * P.H);
         const uint4* g = reinterpret_cast<const uint4*>(P.g);
+        uint4* uo = reinterpret_cast<uint4*>(P.u + (size_t)row * P.H);
         float ss = 0.f;
-        for (int v = lane; v < nv; v += 32) {
-            float f[8];
-            unpack8(h[v], f);
+        for (int v0 = 0; v0 < nv; v0 += 32 * kMaxVec) {
+            uint4 hv[kMaxVec];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+            for (int i = 0; i < kMaxVec; ++i) {
+                const int v = v0 + i * 32 + lane;
+                hv[i] = v < nv ? h[v] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxVec; ++i) {
+                float f[8];
+                unpack8(hv[i], f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
+            }
         }
         ss = warp_sum(ss);
         const float inv = rsqrtf(ss / (float)P.H + P.eps);
-        uint4* uo = reinterpret_cast<uint4*>(P.u + (size_t)row * P.H);
-        for (int v = lane; v < nv; v += 32) {
-            float f[8], gg[8];
-            unpack8(h[v], f);
-            unpack8(g[v], gg);
-            uint4 o;
-            o.x = pack_bf16x2(f[0] * inv * gg[0], f[1] * inv * gg[1]);
-            o.y = pack_bf16x2(f[2] * inv * gg[2], f[3] * inv * gg[3]);
-            o.z = pack_bf16x2(f[4] * inv * gg[4], f[5] * inv * gg[5]);
-            o.w = pack_bf16x2(f[6] * inv * gg[6], f[7] * inv * gg[7]);
-            us[warp * nv + v] = o;
-            if (blockIdx.y == 0) uo[v] = o;
+        for (int v0 = 0; v0 < nv; v0 += 32 * kMaxVec) {
+            uint4 hv[kMaxVec], gv[kMaxVec];
+#pragma unroll
+            for (int i = 0; i < kMaxVec; ++i) {
+                const int v = v0 + i * 32 + lane;
+                hv[i] = v < nv ? h[v] : make_uint4(0, 0, 0, 0);
+                gv[i] = v < nv ? g[v] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxVec; ++i) {
+                const int v = v0 + i * 32 + lane;
+                if (v < nv) {
+                    float f[8], gg[8];
+                    unpack8(hv[i], f);
+                    unpack8(gv[i], gg);
+                    uint4 o;
+                    o.x = pack_bf16x2(f[0] * inv * gg[0], f[1] * inv * gg[1]);
+                    o.y = pack_bf16x2(f[2] * inv * gg[2], f[3] * inv * gg[3]);
+                    o.z = pack_bf16x2(f[4] * inv * gg[4], f[5] * inv * gg[5]);
+                    o.w = pack_bf16x2(f[6] * inv * gg[6], f[7] * inv * gg[7]);
+                    us[warp * nv + v] = o;
+                    if (blockIdx.y == 0) uo[v] = o;
+                }
+            }
         }
     }
     __syncthreads();
 
     // (2) logits, warp w -> expert e
-    const int e = blockIdx.y * 8 + warp;
-    if (e < P.E) {
-        const uint4* w = reinterpret_cast<const uint4*>(P.Wr + (size_t)e * P.H);
+    if (has_e) {
         float acc[kRouterTok];
 #pragma unroll
         for (int i = 0; i < kRouterTok; ++i) acc[i] = 0.f;
-        for (int v = lane; v < nv; v += 32) {
-            float wf[8];
-            unpack8(__ldg(w + v), wf);
+        for (int v0 = 0; v0 < nv; v0 += 32 * kMaxVec) {
+            uint4 wv[kMaxVec];
 #pragma unroll
-            for (int i = 0; i < kRouterTok; ++i) {
-                if (i < ntok) {
-                    float uf[8];
-                    unpack8(us[i * nv + v], uf);
+            for (int i = 0; i < kMaxVec; ++i) {
+                const int v = v0 + i * 32 + lane;
+                wv[i] = v < nv ? __ldg(wrow + v) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[i] = fmaf(wf[q], uf[q], acc[i]);
+            for (int i = 0; i < kMaxVec; ++i) {
+                const int v = v0 + i * 32 + lane;
+                if (v < nv) {
+                    float wf[8];
+                    unpack8(wv[i], wf);
+#pragma unroll
+                    for (int t = 0; t < kRouterTok; ++t) {
+                        if (t < ntok) {
+                            float uf[8];
+                            unpack8(us[t * nv + v], uf);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) acc[t] = fmaf(wf[q], uf[q], acc[t]);
+                        }
+                    }
                 }
             }
         }
@@ -143,7 +182,8 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterProblem P, cons
 #pragma unroll
         for (int i = 0; i < kMaxPer; ++i) {
             const int ee = i * 32 + lane;
-            zv[i] = (i < per && ee < P.E) ? __ldcg(z + ee) : -INFINITY;
+            float v = (i < per && ee < P.E) ? __ldcg(z + ee) : -INFINITY;
+            zv[i] = isnan(v) ? -INFINITY : v;  // a NaN logit ranks below every number
         }
         uint32_t taken = 0;
         float selz[8];
@@ -155,7 +195,7 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterProblem P, cons
             for (int i = 0; i < kMaxPer; ++i) {
                 const int ee = i * 32 + lane;
                 if (i < per && ee < P.E && !(taken & (1u << i)) &&
-                    (zv[i] > bv || (zv[i] == bv && ee < bi))) {
+                    (zv[i] > bv || (zv[i] == bv && ee < bi) || bi == 0x7fffffff)) {
                     bv = zv[i];
                     bi = ee;
                 }
@@ -245,12 +285,27 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const DispatchProblem P, 
     __syncthreads();
     const int nv = P.H >> 3;
     const int rbeg = blockIdx.x * kDispRows;
-    const int rend = min(R, rbeg + kDispRows);
-    for (int r = rbeg; r < rend; ++r) {
-        const int t = row_pair[r] / P.k;
-        const uint4* src = reinterpret_cast<const uint4*>(P.u + (size_t)(P.row0 + t) * P.H);
-        uint4* dst = reinterpret_cast<uint4*>(P.xperm + (size_t)r * P.H);
-        for (int v = threadIdx.x; v < nv; v += 256) dst[v] = src[v];
+    const int total = (min(R, rbeg + kDispRows) - rbeg) * nv;
+    constexpr int kU = 4;  // loads in flight per thread
+    for (int i0 = threadIdx.x; i0 < total; i0 += 256 * kU) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + u * 256;
+            if (i < total) {
+                const int r = rbeg + i / nv, c = i % nv;
+                const int t = row_pair[r] / P.k;
+                v[u] = reinterpret_cast<const uint4*>(P.u + (size_t)(P.row0 + t) * P.H)[c];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + u * 256;
+            if (i < total) {
+                const int r = rbeg + i / nv, c = i % nv;
+                reinterpret_cast<uint4*>(P.xperm + (size_t)r * P.H)[c] = v[u];
+            }
+        }
     }
     task_end(ctx);
 }

@@ -60,9 +60,17 @@ struct GemmProblem {
     int R;                  // rows of the partial-sum buffer
     int n_cap;              // tokens per pass (multiple of 16, <= 256)
     int stages;             // shared-memory pipeline depth
+    int ring_bytes;         // bytes of the stage ring (also holds the staged accumulator)
     int serpentine;         // visit groups in reverse order
-    float* partial;         // [ksplit][R][m_tiles][128] fp32
-    uint32_t* tile_cnt;     // [n_groups * m_tiles], zero between launches
+    float* partial;         // [m_tiles][ksplit][R][128] fp32 tiles (token-major rows)
+};
+
+// Sum of the K segments of every partial tile + fused epilogue.
+struct FinishProblem {
+    const float* partial;   // as GemmProblem::partial
+    int ksplit, m_tiles, R;
+    int rows;               // partial rows to finish: [0, rows)
+    int out_row0;           // output row of partial row 0
     EpiArgs epi;
 };
 
@@ -139,9 +147,11 @@ int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c);
 int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c);
 int enqueue_attention(Launcher& L, const AttnProblem& p, const KCtx& c);
 int enqueue_gemm_tc(Launcher& L, const GemmProblem& p, const KCtx& c);
+int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c);
 int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c);
 
 // shared-memory bytes a tcgen05 GEMM launch needs for (n_cap, stages)
+size_t gemm_tc_ring_bytes(int n_cap, int stages);
 size_t gemm_tc_smem_bytes(int n_cap, int stages);
 // attention chunk length (positions per split-KV work item); fixed, never SM-dependent
 constexpr int kAttnChunk = 512;

@@ -257,7 +257,7 @@ int attn_smax(int max_kv) { return std::max(1, cdiv(max_kv, kAttnChunk)); }
 struct Layout {
     int T = 0, m = 1, b = 0, S_max = 1, n_flags = 0;
     size_t status = 0, zero_beg = 0, zero_end = 0;
-    size_t tile_cnt = 0, attn_cnt = 0, router_cnt = 0, flags = 0, flag_cnt = 0;
+    size_t attn_cnt = 0, router_cnt = 0, flags = 0, flag_cnt = 0;
     size_t a = 0, q = 0, o = 0, h = 0, u = 0;
     size_t per_mu = 0;  // bytes of one microbatch's scratch block
     size_t mu_base = 0;
@@ -292,7 +292,6 @@ Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags) {
         max_tiles = std::max(max_tiles, g.n_groups * g.m_tiles);
     }
     L.max_tiles = max_tiles;
-    L.tile_cnt = take((size_t)m * max_tiles * 4);
     L.attn_cnt = take((size_t)m * b * d.n_kv_heads * 4);
     L.router_cnt = take((size_t)m * cdiv(b, 8) * 4);
     L.flags = take((size_t)std::max(1, n_flags) * 4);
@@ -480,12 +479,28 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     int expect = grouped ? std::max(16, 2 * cdiv(R, gs.n_groups)) : b;
     p.n_cap = std::min(256, std::max(16, (expect + 15) & ~15));
     const int stage_bytes = 16384 + p.n_cap * 128;
-    p.stages = std::max(2, std::min(8, (110 * 1024 - 1280) / stage_bytes));
+    // two CTAs per SM: ring + barriers within ~112 KB
+    p.stages = std::max(2, std::min(8, (110 * 1024) / stage_bytes));
+    p.ring_bytes = (int)gemm_tc_ring_bytes(p.n_cap, p.stages);
     p.serpentine = grouped && e.serpentine && (mu & 1);
     p.partial = e.ws.mu<float>(mu, e.ws.L->gemm_part);
-    p.tile_cnt = e.ws.at<uint32_t>(e.ws.L->tile_cnt) + (size_t)mu * e.ws.L->max_tiles;
-    p.epi = epi;
-    return enqueue_gemm_tc(L, p, c);
+    // the flag check belongs to the first launch, the publish to the last
+    KCtx c1 = c, c2 = c;
+    c1.post_flag = nullptr;
+    c1.post_cnt = nullptr;
+    c2.wait_flag = nullptr;
+    c2.fault = 0;
+    if ((r = enqueue_gemm_tc(L, p, c1)) != 0) return r;
+    FinishProblem f;
+    memset(&f, 0, sizeof(f));
+    f.partial = p.partial;
+    f.ksplit = p.ksplit;
+    f.m_tiles = p.m_tiles;
+    f.R = p.R;
+    f.rows = p.R;
+    f.out_row0 = grouped ? 0 : row0;
+    f.epi = epi;
+    return enqueue_gemm_finish(L, f, c2);
 }
 
 int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
@@ -677,7 +692,7 @@ static int temporal_common(const sgp_dims* d, const sgp_layer* layers, int n_lay
                            const sgp_layer_dump* dump, cudaStream_t s) {
     int r;
     if ((r = check_dims(d)) != SGP_OK) return r;
-    if (T < 1) return fail_arg("n_tokens must be positive");
+    if (T < 1 || T > 256) return fail_arg("n_tokens must be in [1, 256]");
     if (n_layers < 1 || !layers) return fail_arg("no layers");
     if (!kv_len || !x_in || !x_out || !ws) return fail_arg("NULL pointer");
     if (!aligned16(x_in) || !aligned16(x_out) || (reinterpret_cast<uintptr_t>(ws) & 255))
@@ -738,6 +753,31 @@ extern "C" int sgp_stack_temporal(const sgp_dims* d, const sgp_layer* layers, in
                                   size_t ws_bytes, sgp_stream_t stream) {
     return temporal_common(d, layers, n_layers, kv_len, x_in, x_out, n_tokens, topk_idx, topk_w,
                            ws, ws_bytes, nullptr, (cudaStream_t)stream);
+}
+
+extern "C" int sgp_layer_op(const sgp_dims* d, const sgp_layer* layer, int op,
+                            const int32_t* kv_len, const void* x_in, void* x_out, int n_tokens,
+                            void* ws, size_t ws_bytes, sgp_stream_t stream) {
+    int r;
+    if ((r = check_dims(d)) != SGP_OK) return r;
+    if (op < 0 || op >= SGP_N_OPS) return fail_arg("op index");
+    if (n_tokens < 1 || n_tokens > 256) return fail_arg("n_tokens must be in [1, 256]");
+    if (!kv_len || !x_in || !x_out || !ws) return fail_arg("NULL pointer");
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) || !aligned16(x_in) || !aligned16(x_out))
+        return fail_arg("alignment");
+    if ((r = check_layer(*d, layer, n_tokens)) != SGP_OK) return r;
+    Layout Lay = make_layout(*d, n_tokens, 1, layer->kv_cap, 0);
+    if (ws_bytes < Lay.total) return fail_arg("workspace too small");
+    if (!drv().core) return SGP_ERR_UNSUPPORTED;
+    Ws w{(uint8_t*)ws, &Lay};
+    StreamLauncher L((cudaStream_t)stream);
+    RunEnv e{d, layer, kv_len, (const bf16*)x_in, (bf16*)x_out, n_tokens, w, nullptr, nullptr,
+             use_tc_dense(*d, n_tokens), use_tc_expert(*d, n_tokens), 0};
+    KCtx c = plain_ctx(w.status(), kDefaultTimeout, (uint32_t)op << 24);
+    r = enqueue_op(L, e, op, 0, c);
+    if (r == SGP_ERR_INVALID_ARG || r == SGP_ERR_CUDA) return r;
+    if (r != 0) return fail_cuda((cudaError_t)r, "kernel launch");
+    return SGP_OK;
 }
 
 extern "C" int sgp_status_from_workspace(const void* ws, sgp_stream_t stream) {
@@ -901,7 +941,7 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
                 if ((p->opts.fault_inject & 1u) && (int)i == p->opts.fault_task)
                     c.fault |= FAULT_SKIP_PUBLISH;
             }
-            if ((p->opts.fault_inject & 2u) && i == 0 && first) c.fault |= FAULT_DROP_TMA;
+            if ((p->opts.fault_inject & 2u) && i == 0 && op == SGP_OP_QKV) c.fault |= FAULT_DROP_TMA;
             RunEnv e{&d, &layers[l], kv_len, (const bf16*)(l == 0 ? x_in : x_out), (bf16*)x_out, T,
                      w, tki ? tki + (size_t)l * T * d.top_k : nullptr,
                      tkw ? tkw + (size_t)l * T * d.top_k : nullptr, tcd, tce,
@@ -994,6 +1034,7 @@ extern "C" int sgp_pipeline_create(const sgp_dims* d, const int* sm_split, int n
     if (n_stages < 1 || n_stages > 3) return fail_arg("n_stages must be 1, 2 or 3");
     if (microbatch < 1 || max_tokens < 1 || max_tokens % microbatch)
         return fail_arg("microbatch must divide max_tokens");
+    if (microbatch > 256) return fail_arg("microbatch above 256 sequences");
     if (max_kv_len < 1) return fail_arg("max_kv_len");
     if (!drv().core) {
         g_err = "CUDA driver entry points unavailable";

@@ -75,6 +75,9 @@ _SIGS = {
     "sgp_stack_temporal": (C.c_int, [C.POINTER(sgp_dims), C.POINTER(sgp_layer), C.c_int,
                                      C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
                                      C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "sgp_layer_op": (C.c_int, [C.POINTER(sgp_dims), C.POINTER(sgp_layer), C.c_int, C.c_void_p,
+                               C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_size_t,
+                               C.c_void_p]),
     "sgp_status_from_workspace": (C.c_int, [C.c_void_p, C.c_void_p]),
     "sgp_pipeline_create": (C.c_int, [C.POINTER(sgp_dims), C.POINTER(C.c_int), C.c_int, C.c_int,
                                       C.c_int, C.c_int, C.POINTER(sgp_pipeline_opts),
@@ -215,6 +218,14 @@ def sgp_stack_temporal(dims, layers, kv_len, x_in, x_out, n_tokens: int, topk_id
         C.byref(dims), arr, len(layers), _p(kv_len), _p(x_in), _p(x_out), n_tokens,
         _p(topk_idx), _p(topk_w), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)), "sgp_stack_temporal")
+
+
+def sgp_layer_op(dims, layer: sgp_layer, op: int, kv_len, x_in, x_out, n_tokens: int,
+                 workspace, stream=None) -> int:
+    return check(lib().sgp_layer_op(C.byref(dims), C.byref(layer), op, _p(kv_len), _p(x_in),
+                                    _p(x_out), n_tokens, _p(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream)), "sgp_layer_op")
 
 
 def sgp_status_from_workspace(workspace, stream=None) -> int:

@@ -86,15 +86,22 @@ def test_gptoss_stack_pipeline_bit_identical(n_stages, micro):
 
 
 def test_task_dag_matches_schedule_model():
+    """Same tasks, data edges and per-stage FIFO edges as the schedule model (task ids
+    may differ: any topological dispatch order is allowed; compare by task key)."""
     wl, inp = _stack_inputs(3, 256, 9, n_tokens=32)
     d = H.dims(wl.shape)
     _, _, _, tasks = _pipelined(inp, d, 2, 8, reps=1)
     model = S.build_tasks(3, 4, 2)
     assert len(tasks) == len(model)
-    for got, m in zip(tasks, model):
-        assert got[0] == m["stage"] - 1 and got[1] == m["layer"] and got[2] == m["micro"]
-        assert got[3] == (m["data"][0] if m["data"] else -1)
-        assert got[4] == (m["stage_pred"] if m["stage_pred"] is not None else -1)
+    gkey = [(t[0], t[1], t[2]) for t in tasks]
+    mkey = [(m["stage"] - 1, m["layer"], m["micro"]) for m in model]
+    assert sorted(gkey) == sorted(mkey)
+    gk = lambda i: gkey[i] if i >= 0 else None
+    mk = lambda i: mkey[i] if i is not None else None
+    g = {gkey[i]: (gk(t[3]), gk(t[4])) for i, t in enumerate(tasks)}
+    m = {mkey[i]: (mk(x["data"][0] if x["data"] else None), mk(x["stage_pred"]))
+         for i, x in enumerate(model)}
+    assert g == m
 
 
 def test_macro_cut_bit_identical():
