@@ -201,6 +201,34 @@ int sgp_layer_op(const sgp_dims* dims, const sgp_layer* layer, int op, const int
  * Returns SGP_ERR_CUDA if the copy fails. */
 int sgp_status_from_workspace(const void* workspace, sgp_stream_t stream);
 
+/* ---- router without device allocation ----------------------------------------------
+ * Some callers cannot call cudaMalloc at all: code that runs while a CUDA graph is being
+ * captured, or inside an engine whose memory pool owns every byte of the device, or a
+ * plugin that is handed only its inputs and outputs.  This entry point serves them: it is
+ * the router of op SGP_OP_ROUTER (RMSNorm of h, fp32 logits, top-k, softmax over the k
+ * selected logits) for one layer, and it allocates nothing.  The paper has no counterpart;
+ * it is an interface convenience.
+ *
+ * Its scratch (fp32 logits, arrival counters, a status word) is a fixed array inside the
+ * library: at most 262,144 logits, i.e. n_tokens * n_experts <= 262144 (for example 256
+ * tokens x 1024 experts), about 1 MiB, which every GPU that loads the library keeps until
+ * the process exits.  The first call on a device looks up that array's device address (with
+ * the device current) and caches it; make that first call before any stream capture.
+ * Every call shares the array: the counters are cleared on `stream` at the start of each
+ * call, the logits keep the last call's values, and calls that overlap on the GPU (two
+ * streams, or two host threads) race -- serialise them.
+ *
+ *   h          device bf16 [n_tokens][H]   residual stream after the attention block
+ *   g_mlp      device bf16 [H];  w_router device bf16 [E][H];  router_bias device fp32 [E] or NULL
+ *   u_out      device bf16 [n_tokens][H]   RMSNorm(h; g_mlp), as the layer computes it
+ *   topk_idx   device int32 [n_tokens][k]; topk_w device fp32 [n_tokens][k]
+ * Results equal those sgp_layer_temporal produces for the same h.  Returns SGP_OK,
+ * SGP_ERR_INVALID_ARG (NULL or unaligned pointer, unsupported dims, or a size beyond the
+ * fixed scratch; nothing is launched) or SGP_ERR_CUDA. */
+int sgp_router_topk_noalloc(const sgp_dims* dims, const void* h, const void* g_mlp,
+                            const void* w_router, const float* router_bias, int n_tokens,
+                            void* u_out, int32_t* topk_idx, float* topk_w, sgp_stream_t stream);
+
 /* ---- spatial pipeline (Section 3: cut, binding, SM allocation, microbatches) -------- */
 typedef struct sgp_pipeline sgp_pipeline;
 

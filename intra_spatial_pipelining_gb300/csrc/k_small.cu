@@ -2,7 +2,11 @@
 // dispatch (stable counting sort of the routed pairs by expert slot + row gather) and the
 // weighted combine with the residual.  All loads and stores are 16-byte vectors, every
 // reduction has a fixed order, and each token's result depends only on that token.
+#include <cstring>
+#include <mutex>
+
 #include "kernels.h"
+#include "sgp.h"
 
 namespace sgp {
 
@@ -353,6 +357,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, co
 
 }  // namespace
 
+// ---------------------------------------------------------------------------------------
+// Router without device allocation (see sgp_router_topk_noalloc in sgp.h).  The scratch the
+// router needs -- fp32 logits, per-token-group arrival counters and a status word -- lives
+// in this fixed array; every GPU that loads the library holds it until the process exits.
+// ---------------------------------------------------------------------------------------
+constexpr size_t kNoallocLogits = 256 * 1024;                    // fp32 logits (1 MiB)
+constexpr size_t kNoallocCounters = 256;                         // u32 token-group counters
+constexpr size_t kNoallocBytes = kNoallocLogits * 4 + kNoallocCounters * 4 + 64;
+static __device__ __align__(256) unsigned char g_router_scratch[kNoallocBytes];
+
 int enqueue_rmsnorm(Launcher& L, const NormProblem& p, const KCtx& c) {
     void* args[] = {(void*)&p, (void*)&c};
     return L.launch((const void*)rmsnorm_kernel, dim3(p.nrows), dim3(256), 0, args);
@@ -379,3 +393,81 @@ int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c) {
 }
 
 }  // namespace sgp
+
+// Host side of the allocation-free router.  The device address of g_router_scratch is
+// fetched once per device (with that device current) and cached.
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[128];
+}  // namespace
+
+extern "C" int sgp_router_topk_noalloc(const sgp_dims* d, const void* h, const void* g_mlp,
+                                       const void* w_router, const float* router_bias,
+                                       int n_tokens, void* u_out, int32_t* topk_idx,
+                                       float* topk_w, sgp_stream_t stream) {
+    using namespace sgp;
+    if (!d || !h || !g_mlp || !w_router || !u_out || !topk_idx || !topk_w)
+        return SGP_ERR_INVALID_ARG;
+    if (d->hidden <= 0 || d->hidden % 64 || d->hidden > 8192 || d->top_k < 1 || d->top_k > 8 ||
+        d->n_experts < d->top_k || d->n_experts > 1024 || !(d->rms_eps > 0.f))
+        return SGP_ERR_INVALID_ARG;
+    const void* ptrs[] = {h, g_mlp, w_router, u_out};
+    for (const void* q : ptrs)
+        if (reinterpret_cast<uintptr_t>(q) & 15) return SGP_ERR_INVALID_ARG;
+    const int groups = (n_tokens + kRouterTok - 1) / kRouterTok;
+    // sizes beyond the fixed scratch are refused; nothing is launched
+    if (n_tokens < 1 || (size_t)n_tokens * d->n_experts > kNoallocLogits ||
+        (size_t)groups > kNoallocCounters)
+        return SGP_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return SGP_ERR_CUDA;
+    void* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (g_noalloc_ptr[dev] == nullptr) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_router_scratch) != cudaSuccess || p == nullptr)
+                return SGP_ERR_CUDA;
+            g_noalloc_ptr[dev] = p;
+        }
+        base = g_noalloc_ptr[dev];
+    }
+    float* logits = reinterpret_cast<float*>(base);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(logits + kNoallocLogits);
+    uint32_t* status = cnt + kNoallocCounters;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // counters (and the status word) must start at zero; the logits need no clearing
+    if (cudaMemsetAsync(cnt, 0, kNoallocCounters * 4 + 64, s) != cudaSuccess) return SGP_ERR_CUDA;
+    RouterProblem p;
+    memset(&p, 0, sizeof(p));
+    p.h = reinterpret_cast<const bf16*>(h);
+    p.g = reinterpret_cast<const bf16*>(g_mlp);
+    p.u = reinterpret_cast<bf16*>(u_out);
+    p.Wr = reinterpret_cast<const bf16*>(w_router);
+    p.bias = router_bias;
+    p.logits = logits;
+    p.idx = topk_idx;
+    p.wts = topk_w;
+    p.cnt = cnt;
+    p.row0 = 0;
+    p.nrows = n_tokens;
+    p.H = d->hidden;
+    p.E = d->n_experts;
+    p.k = d->top_k;
+    p.eps = d->rms_eps;
+    KCtx c;
+    memset(&c, 0, sizeof(c));
+    c.status = status;
+    c.timeout_ns = 2000000000ull;
+    const size_t smem = (size_t)kRouterTok * d->hidden * sizeof(bf16);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute((const void*)router_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return SGP_ERR_CUDA;
+    void* args[] = {(void*)&p, (void*)&c};
+    dim3 grid(groups, (d->n_experts + 7) / 8);
+    if (cudaLaunchKernel((const void*)router_kernel, grid, dim3(256), args, smem, s) !=
+        cudaSuccess)
+        return SGP_ERR_CUDA;
+    return SGP_OK;
+}

@@ -79,6 +79,9 @@ _SIGS = {
                                C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_size_t,
                                C.c_void_p]),
     "sgp_status_from_workspace": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "sgp_router_topk_noalloc": (C.c_int, [C.POINTER(sgp_dims), C.c_void_p, C.c_void_p,
+                                          C.c_void_p, C.c_void_p, C.c_int, C.c_void_p,
+                                          C.c_void_p, C.c_void_p, C.c_void_p]),
     "sgp_pipeline_create": (C.c_int, [C.POINTER(sgp_dims), C.POINTER(C.c_int), C.c_int, C.c_int,
                                       C.c_int, C.c_int, C.POINTER(sgp_pipeline_opts),
                                       C.POINTER(C.c_void_p)]),
@@ -226,6 +229,14 @@ def sgp_layer_op(dims, layer: sgp_layer, op: int, kv_len, x_in, x_out, n_tokens:
                                     _p(x_out), n_tokens, _p(workspace),
                                     workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "sgp_layer_op")
+
+
+def sgp_router_topk_noalloc(dims, h, g_mlp, w_router, router_bias, n_tokens: int, u_out,
+                            topk_idx, topk_w, stream=None) -> int:
+    return check(lib().sgp_router_topk_noalloc(C.byref(dims), _p(h), _p(g_mlp), _p(w_router),
+                                               _p(router_bias), n_tokens, _p(u_out),
+                                               _p(topk_idx), _p(topk_w), _stream(stream)),
+                 "sgp_router_topk_noalloc")
 
 
 def sgp_status_from_workspace(workspace, stream=None) -> int:
