@@ -22,264 +22,326 @@ namespace sgp {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kStageA = 128 * 128;  // A tile: 128 rows x 64 bf16
+constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kStageA = kGemmKps * 128 * 128;  // A: kGemmKps k-blocks of 128 rows x 64 bf16
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// named barrier of the 4 epilogue warps
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// same barrier, returning the OR of `v` over the 128 epilogue threads (uniform decision)
+__device__ __forceinline__ bool epi_bar_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+// One work unit = (group, 128-row weight tile, K segment) and its token range.
+struct Unit {
+    int g, mt, ks, kb0, nk, n, npass, tma_r0, lr0;
+};
+
+__device__ __forceinline__ Unit unit_info(const GemmProblem& P, int u, const KCtx& c) {
+    Unit x;
+    const int per_group = P.m_tiles * P.ksplit;
+    x.g = u / per_group;
+    const int rem = u % per_group;
+    x.mt = rem / P.ksplit;
+    x.ks = rem % P.ksplit;
+    if (P.serpentine) x.g = P.n_groups - 1 - x.g;
+    // K segment = stage blocks [sb0, sb1); k-blocks beyond K are zero-filled by the loads
+    const int sb0 = (x.ks * P.n_sb) / P.ksplit;
+    x.kb0 = sb0 * kGemmKps;
+    x.nk = ((x.ks + 1) * P.n_sb) / P.ksplit - sb0;  // stage blocks of this segment
+    if (P.group_offsets != nullptr) {
+        x.tma_r0 = P.group_offsets[x.g];
+        x.n = P.group_offsets[x.g + 1] - x.tma_r0;
+        x.lr0 = x.tma_r0;
+    } else {
+        x.tma_r0 = 0;
+        x.n = P.nrows;
+        x.lr0 = 0;
+    }
+    if (x.lr0 < 0 || x.n < 0 || x.lr0 + x.n > P.R) {
+        if (threadIdx.x == 0) report(c, ST_BOUNDS, (uint32_t)(x.lr0 + x.n));
+        x.n = 0;
+    }
+    if (x.nk <= 0) x.n = 0;
+    x.npass = (((x.n + 15) & ~15) + P.n_cap - 1) / P.n_cap;
+    return x;
+}
+
+// Persistent: CTA b processes units b, b + gridDim.x, ... in that order; every role walks the
+// same job sequence (unit, pass), so the ring and TMEM phases line up without messages.
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ GemmProblem P, const KCtx ctx) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = P.stages;
-    const int stage_bytes = kStageA + P.n_cap * 128;
+    const int stage_b = kGemmKps * P.n_cap * 128;  // B: kGemmKps k-blocks of n_cap rows
+    const int stage_bytes = kStageA + stage_b;
+    float* Ts = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);  // [n_cap][128]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + P.ring_bytes);
     uint64_t* empty = full + S;
-    uint64_t* accbar = empty + S;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accbar + 1);
+    uint64_t* tfull = empty + S;   // [2] accumulator ready
+    uint64_t* tempty = tfull + 2;  // [2] accumulator drained
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
     int* sh_err = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     task_begin(ctx);
-
-    // ---- work unit --------------------------------------------------------------------
-    const int per_group = P.m_tiles * P.ksplit;
-    int g = blockIdx.x / per_group;
-    const int rem = blockIdx.x % per_group;
-    const int mt = rem / P.ksplit, ks = rem % P.ksplit;
-    if (P.serpentine) g = P.n_groups - 1 - g;
-    const int kb0 = (ks * P.kb_total) / P.ksplit;
-    const int kb1 = ((ks + 1) * P.kb_total) / P.ksplit;
-    // tma_r0: first activation row in the B tensor map (dense: the map starts at this
-    // microbatch's first token; grouped: rows of the slot-sorted matrix); lr0: first row of
-    // the partial-sum buffer.
-    int tma_r0, n, lr0;
-    if (P.group_offsets != nullptr) {
-        tma_r0 = P.group_offsets[g];
-        n = P.group_offsets[g + 1] - tma_r0;
-        lr0 = tma_r0;
-    } else {
-        tma_r0 = 0;
-        n = P.nrows;
-        lr0 = 0;
-    }
-    if (lr0 < 0 || n < 0 || lr0 + n > P.R) {
-        if (tid == 0) report(ctx, ST_BOUNDS, (uint32_t)(lr0 + n));
-        n = 0;
-    }
-    if (n == 0 || kb1 <= kb0) {
-        task_end(ctx);
-        return;
-    }
-    const int n_pad = (n + 15) & ~15;
-    const int npass = (n_pad + P.n_cap - 1) / P.n_cap;
-    const int cols_needed = n_pad < P.n_cap ? n_pad : P.n_cap;
-    uint32_t ncols = 32;
-    while (ncols < (uint32_t)cols_needed) ncols <<= 1;
-    const int rowA1 = g * P.rows_per_group + mt * P.a_tile_stride;
-    const int rowA2 = rowA1 + P.a_second_off;
+    uint32_t acc_cols = 32;
+    while (acc_cols < (uint32_t)P.n_cap) acc_cols <<= 1;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accbar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
         *sh_err = 0;
         fence_barrier_init();
         prefetch_tensormap(&P.tmA);
         prefetch_tensormap(&P.tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, ncols);
+        tmem_alloc(tmem_slot, 2 * acc_cols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int nk = kb1 - kb0;
 
-    // per-stage parity of the last load issued (producer), for draining on error
-    uint32_t issued_mask = 0, issued_par = 0;
-
-    for (int pass = 0; pass < npass; ++pass) {
-        const int c0 = pass * P.n_cap;
-        const int np = min(P.n_cap, n_pad - c0);
-        const int nbox = np >> 4;
-        const uint32_t it0 = (uint32_t)pass * nk;
-
-        if (warp == 0 && lane == 0) {
-            // ---- TMA producer ----
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
-            for (int i = 0; i < nk && !*(volatile int*)sh_err; ++i) {
-                const uint32_t it = it0 + i;
-                const int s = it % S;
-                const uint32_t j = it / S;
-                if (j > 0 && !mbar_wait(&empty[s], (j - 1) & 1, ctx.timeout_ns)) {
-                    report(ctx, ST_TIMEOUT, 1);
-                    atomicExch(sh_err, 1);
-                    break;
+            uint32_t it = 0;
+            uint32_t issued_mask = 0, issued_par = 0;
+            bool dropped = false;
+            for (int u = blockIdx.x; u < P.n_units && !*(volatile int*)sh_err; u += gridDim.x) {
+                const Unit x = unit_info(P, u, ctx);
+                const int rowA1 = x.g * P.rows_per_group + x.mt * P.a_tile_stride;
+                for (int pass = 0; pass < x.npass; ++pass) {
+                    const int c0 = pass * P.n_cap;
+                    for (int i = 0; i < x.nk; ++i, ++it) {
+                        const int s = it % S;
+                        const uint32_t j = it / S;
+                        if (j > 0 && !mbar_wait(&empty[s], (j - 1) & 1, ctx.timeout_ns)) {
+                            report(ctx, ST_TIMEOUT, 1);
+                            atomicExch(sh_err, 1);
+                            break;
+                        }
+                        if ((ctx.fault & FAULT_DROP_TMA) && blockIdx.x == 0 && !dropped) {
+                            dropped = true;  // test-only: this stage never fills
+                            continue;
+                        }
+                        uint8_t* sa = smem + (size_t)s * stage_bytes;
+                        uint8_t* sb = sa + kStageA;
+                        const int kb = x.kb0 + i * kGemmKps;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(kStageA + stage_b));
+                        if (P.a_4d)
+                            tma_load_4d(sa, &P.tmA, &full[s], 0, rowA1, 0, kb, pol_w);
+                        else
+                            tma_load_3d(sa, &P.tmA, &full[s], 0, rowA1, kb, pol_w);
+                        tma_load_3d(sb, &P.tmB, &full[s], 0, x.tma_r0 + c0, kb, pol_x);
+                        issued_mask |= 1u << s;
+                        issued_par = (issued_par & ~(1u << s)) | ((j & 1u) << s);
+                    }
+                    if (*(volatile int*)sh_err) break;
                 }
-                if ((ctx.fault & FAULT_DROP_TMA) && blockIdx.x == 0 && pass == 0 && i == 0)
-                    continue;  // test-only: this stage never fills
-                uint8_t* sa = smem + (size_t)s * stage_bytes;
-                uint8_t* sb = sa + kStageA;
-                const int kx = (kb0 + i) * 64;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(kStageA + nbox * 2048));
-                tma_load_2d(sa, &P.tmA, &full[s], kx, rowA1, pol_w);
-                tma_load_2d(sa + kStageA / 2, &P.tmA, &full[s], kx, rowA2, pol_w);
-                for (int b = 0; b < nbox; ++b)
-                    tma_load_2d(sb + b * 2048, &P.tmB, &full[s], kx, tma_r0 + c0 + 16 * b, pol_x);
-                issued_mask |= 1u << s;
-                issued_par = (issued_par & ~(1u << s)) | ((j & 1u) << s);
             }
-        } else if (warp == 1 && lane == 0) {
-            // ---- MMA issuer ----
-            const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)np);
-            bool okk = true;
-            for (int i = 0; i < nk; ++i) {
-                const uint32_t it = it0 + i;
-                const int s = it % S;
-                const uint32_t j = it / S;
-                if (!mbar_wait(&full[s], j & 1, ctx.timeout_ns)) {
-                    report(ctx, ST_TIMEOUT, 2);
+            if (*(volatile int*)sh_err) {
+                // drain loads still in flight into this CTA's shared memory (bounded)
+                for (int s = 0; s < S; ++s)
+                    if (issued_mask & (1u << s))
+                        (void)mbar_wait(&full[s], (issued_par >> s) & 1u, 10000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            uint32_t it = 0, job = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < P.n_units && ok; u += gridDim.x) {
+                const Unit x = unit_info(P, u, ctx);
+                const int n_pad = (x.n + 15) & ~15;
+                for (int pass = 0; pass < x.npass && ok; ++pass, ++job) {
+                    const int np = min(P.n_cap, n_pad - pass * P.n_cap);
+                    const uint32_t b = job & 1u, jb = job >> 1;
+                    if (jb > 0 && !mbar_wait(&tempty[b], (jb - 1) & 1u, ctx.timeout_ns)) {
+                        report(ctx, ST_TIMEOUT, 5);
+                        atomicExch(sh_err, 1);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t acc = tmem + b * acc_cols;
+                    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)np);
+                    for (int i = 0; i < x.nk; ++i, ++it) {
+                        const int s = it % S;
+                        const uint32_t j = it / S;
+                        if (!mbar_wait(&full[s], j & 1, ctx.timeout_ns)) {
+                            report(ctx, ST_TIMEOUT, 2);
+                            atomicExch(sh_err, 1);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+                        const uint32_t sb = sa + kStageA;
+#pragma unroll
+                        for (int kk = 0; kk < kGemmKps; ++kk)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc_mma_bf16(acc, smem_desc_sw128(sa + kk * 16384 + 32 * k),
+                                            smem_desc_sw128(sb + kk * (P.n_cap * 128) + 32 * k),
+                                            idesc, (i > 0 || kk > 0 || k > 0) ? 1u : 0u);
+                        tc_commit(&empty[s]);
+                    }
+                    if (ok) tc_commit(&tfull[b]);
+                }
+            }
+        }
+    } else {
+        // ================= epilogue: TMEM -> shared -> one bulk store per job =================
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        const int row = q * 32 + lane;
+        const bool issuer = (warp == 2 && lane == 0);
+        uint32_t job = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < P.n_units && ok; u += gridDim.x) {
+            const Unit x = unit_info(P, u, ctx);
+            const int n_pad = (x.n + 15) & ~15;
+            for (int pass = 0; pass < x.npass; ++pass, ++job) {
+                const int c0 = pass * P.n_cap;
+                const int np = min(P.n_cap, n_pad - c0);
+                const uint32_t b = job & 1u, jb = job >> 1;
+                const bool w = mbar_wait(&tfull[b], jb & 1u, ctx.timeout_ns);
+                if (!w) {
+                    report(ctx, ST_TIMEOUT, 3);
                     atomicExch(sh_err, 1);
-                    okk = false;
+                }
+                // the previous job's bulk store must have finished reading Ts
+                if (issuer) bulk_wait_read();
+                // all four epilogue warps take the same decision
+                if (epi_bar_or(!w || *(volatile int*)sh_err)) {
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-                const uint32_t sb = sa + kStageA;
+                const uint32_t tbase = tmem + b * acc_cols + ((uint32_t)(q * 32) << 16);
+                for (int cc = 0; cc < np; cc += 16) {
+                    uint32_t v[16];
+                    tmem_ld_x16(tbase + (uint32_t)cc, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    tc_mma_bf16(tmem, smem_desc_sw128(sa + 32 * k), smem_desc_sw128(sb + 32 * k),
-                                idesc, (i > 0 || k > 0) ? 1u : 0u);
-                tc_commit(&empty[s]);
-            }
-            if (okk) tc_commit(accbar);
-        }
-        __syncwarp();
-
-        // ---- TMEM -> shared memory [token][128 rows] fp32 -> one bulk store ----
-        bool ok = mbar_wait(accbar, (uint32_t)pass & 1u, ctx.timeout_ns);
-        if (!ok) {
-            if (lane == 0) report(ctx, ST_TIMEOUT, 3);
-            atomicExch(sh_err, 1);
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        float* Ts = reinterpret_cast<float*>(smem);  // the ring is idle: all MMAs completed
-        if (ok) {
-            tc_fence_after();
-            const int row = warp * 32 + lane;
-            const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
-            for (int cc = 0; cc < np; cc += 16) {
-                uint32_t v[16];
-                tmem_ld_x16(tbase + (uint32_t)cc, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < 16; ++q) Ts[(cc + q) * 128 + row] = __uint_as_float(v[q]);
+                    for (int t = 0; t < 16; ++t) Ts[(cc + t) * 128 + row] = __uint_as_float(v[t]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);  // the accumulator may be reused
+                fence_proxy_async();
+                epi_bar();
+                if (issuer) {
+                    const int nv = min(np, x.n - c0);
+                    bulk_store(P.partial + (((size_t)x.mt * P.ksplit + x.ks) * P.R + x.lr0 + c0) * 128,
+                               Ts, (uint32_t)nv * 512u);
+                    bulk_commit();
+                }
             }
         }
-        tc_fence_before();
-        fence_proxy_async();
-        __syncthreads();
-        if (*sh_err) break;
-        const int nv = min(np, n - c0);  // valid tokens of this pass
-        if (tid == 0) {
-            bulk_store(P.partial + (((size_t)mt * P.ksplit + ks) * P.R + lr0 + c0) * 128, Ts,
-                       (uint32_t)nv * 512u);
-            bulk_commit();
-            bulk_wait_all();  // shared memory is reused by the next pass; results complete
-        }
-        __syncthreads();
-    }
-
-    // ---- teardown ----
-    if (*sh_err && warp == 0 && lane == 0) {
-        // drain TMA loads still in flight into this CTA's shared memory (bounded)
-        for (int s = 0; s < S; ++s)
-            if (issued_mask & (1u << s))
-                (void)mbar_wait(&full[s], (issued_par >> s) & 1u, 10000000ull);
+        if (issuer) bulk_wait_all();  // partial tiles complete before the CTA finishes
     }
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, ncols);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * acc_cols);
+    }
     task_end(ctx);
 }
 
 // ---------------------------------------------------------------------------------------
-// K-segment reduction + fused epilogue: one thread = 8 consecutive outputs of one token.
+// K-segment reduction + fused epilogue: one thread = 4 consecutive outputs of one token.  The
+// K-segment loads are issued before they are summed (in segment order).
 // ---------------------------------------------------------------------------------------
+constexpr int kFinUnroll = 8;
+
+__device__ __forceinline__ float4 sum_segments(const float* p, size_t sstride, int ks) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < ks; s0 += kFinUnroll) {
+        float4 v[kFinUnroll];
+#pragma unroll
+        for (int i = 0; i < kFinUnroll; ++i)
+            if (s0 + i < ks) v[i] = __ldcg(reinterpret_cast<const float4*>(p + (s0 + i) * sstride));
+#pragma unroll
+        for (int i = 0; i < kFinUnroll; ++i)
+            if (s0 + i < ks) {
+                acc.x += v[i].x;
+                acc.y += v[i].y;
+                acc.z += v[i].z;
+                acc.w += v[i].w;
+            }
+    }
+    return acc;
+}
+
 __global__ void __launch_bounds__(256) gemm_finish_kernel(const FinishProblem P, const KCtx ctx) {
     task_begin(ctx);
     const EpiArgs& e = P.epi;
     const bool swiglu = e.mode == EPI_SWIGLU;
-    const int per_tok = swiglu ? 8 : 16;          // 8-output groups per (tile, token)
+    const int per_tok = swiglu ? 16 : 32;         // 4-output groups per (tile, token)
     const int total = P.m_tiles * P.rows * per_tok;
+    const size_t sstride = (size_t)P.R * 128;     // next K segment
     for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += gridDim.x * blockDim.x) {
-        const int q8 = u % per_tok;
+        const int q4 = u % per_tok;
         const int lr = (u / per_tok) % P.rows;
         const int mt = u / (per_tok * P.rows);
-        const size_t base = ((size_t)mt * P.ksplit * P.R + lr) * 128;  // (mt, s = 0, lr)
-        const size_t sstride = (size_t)P.R * 128;                     // next K segment
+        const float* base = P.partial + ((size_t)mt * P.ksplit * P.R + lr) * 128;
         const int trow = P.out_row0 + lr;
         if (swiglu) {
-            const int i0 = mt * 64 + 8 * q8;
+            const int i0 = mt * 64 + 4 * q4;
             if (i0 >= e.n_out) continue;
-            float gsum[8], usum[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) gsum[i] = usum[i] = 0.f;
-            for (int s = 0; s < P.ksplit; ++s) {
-                const float4* pg =
-                    reinterpret_cast<const float4*>(P.partial + base + s * sstride + 8 * q8);
-                const float4* pu =
-                    reinterpret_cast<const float4*>(P.partial + base + s * sstride + 64 + 8 * q8);
-                const float4 g0 = __ldcg(pg), g1 = __ldcg(pg + 1), u0 = __ldcg(pu),
-                             u1 = __ldcg(pu + 1);
-                gsum[0] += g0.x; gsum[1] += g0.y; gsum[2] += g0.z; gsum[3] += g0.w;
-                gsum[4] += g1.x; gsum[5] += g1.y; gsum[6] += g1.z; gsum[7] += g1.w;
-                usum[0] += u0.x; usum[1] += u0.y; usum[2] += u0.z; usum[3] += u0.w;
-                usum[4] += u1.x; usum[5] += u1.y; usum[6] += u1.z; usum[7] += u1.w;
-            }
-            uint4 o;
-            o.x = pack_bf16x2(silu_f(gsum[0]) * usum[0], silu_f(gsum[1]) * usum[1]);
-            o.y = pack_bf16x2(silu_f(gsum[2]) * usum[2], silu_f(gsum[3]) * usum[3]);
-            o.z = pack_bf16x2(silu_f(gsum[4]) * usum[4], silu_f(gsum[5]) * usum[5]);
-            o.w = pack_bf16x2(silu_f(gsum[6]) * usum[6], silu_f(gsum[7]) * usum[7]);
-            *reinterpret_cast<uint4*>(e.out + (size_t)trow * e.ld + i0) = o;
+            const float4 g = sum_segments(base + 4 * q4, sstride, P.ksplit);
+            const float4 up = sum_segments(base + 64 + 4 * q4, sstride, P.ksplit);
+            uint2 o;
+            o.x = pack_bf16x2(silu_f(g.x) * up.x, silu_f(g.y) * up.y);
+            o.y = pack_bf16x2(silu_f(g.z) * up.z, silu_f(g.w) * up.w);
+            *reinterpret_cast<uint2*>(e.out + (size_t)trow * e.ld + i0) = o;
             continue;
         }
-        const int f0 = mt * 128 + 8 * q8;  // first of the 8 output features
+        const int f0 = mt * 128 + 4 * q4;  // first of the 4 output features
         if (f0 >= e.n_out) continue;
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
-        for (int s = 0; s < P.ksplit; ++s) {
-            const float4* pp =
-                reinterpret_cast<const float4*>(P.partial + base + s * sstride + 8 * q8);
-            const float4 a = __ldcg(pp), b = __ldcg(pp + 1);
-            v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
-            v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
-        }
+        float4 v = sum_segments(base + 4 * q4, sstride, P.ksplit);
         if (e.mode == EPI_F32) {
-            float4* o = reinterpret_cast<float4*>(e.out_f32 + (size_t)trow * e.ld + f0);
-            o[0] = make_float4(v[0], v[1], v[2], v[3]);
-            o[1] = make_float4(v[4], v[5], v[6], v[7]);
+            *reinterpret_cast<float4*>(e.out_f32 + (size_t)trow * e.ld + f0) = v;
             continue;
         }
         if (e.mode == EPI_RESID) {
-            float r[8];
-            unpack8(*reinterpret_cast<const uint4*>(e.resid + (size_t)trow * e.ld + f0), r);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] += r[i];
+            const uint2 rr = *reinterpret_cast<const uint2*>(e.resid + (size_t)trow * e.ld + f0);
+            const float2 r01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.x));
+            const float2 r23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.y));
+            v.x += r01.x;
+            v.y += r01.y;
+            v.z += r23.x;
+            v.w += r23.y;
         }
-        uint4 o;
-        o.x = pack_bf16x2(v[0], v[1]);
-        o.y = pack_bf16x2(v[2], v[3]);
-        o.z = pack_bf16x2(v[4], v[5]);
-        o.w = pack_bf16x2(v[6], v[7]);
+        uint2 o;
+        o.x = pack_bf16x2(v.x, v.y);
+        o.y = pack_bf16x2(v.z, v.w);
         bf16* dst;
         if (e.mode == EPI_RESID) {
             dst = e.out + (size_t)trow * e.ld + f0;
@@ -297,7 +359,7 @@ __global__ void __launch_bounds__(256) gemm_finish_kernel(const FinishProblem P,
             bf16* cache = which == 0 ? e.kc : e.vc;
             dst = cache + (((size_t)trow * e.nkv + kh) * e.cap + pos) * e.d + (r % e.d);
         }
-        *reinterpret_cast<uint4*>(dst) = o;
+        *reinterpret_cast<uint2*>(dst) = o;
     }
     task_end(ctx);
 }
@@ -409,9 +471,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KC
 }  // namespace
 
 size_t gemm_tc_ring_bytes(int n_cap, int stages) {
-    size_t ring = (size_t)stages * (kStageA + n_cap * 128);
-    size_t ts = (size_t)n_cap * 512;  // the accumulator staged as [token][128] fp32
-    return ring > ts ? ring : ts;
+    // stage ring, then the accumulator staging area [n_cap][128] fp32
+    return (size_t)stages * (kStageA + kGemmKps * n_cap * 128) + (size_t)n_cap * 512;
 }
 
 size_t gemm_tc_smem_bytes(int n_cap, int stages) {
@@ -419,7 +480,7 @@ size_t gemm_tc_smem_bytes(int n_cap, int stages) {
 }
 
 int enqueue_gemm_tc(Launcher& L, const GemmProblem& p, const KCtx& c) {
-    dim3 grid(p.n_groups * p.m_tiles * p.ksplit), block(kThreads);
+    dim3 grid(std::max(1, std::min(p.n_units, p.grid))), block(kThreads);
     if ((size_t)p.ring_bytes != gemm_tc_ring_bytes(p.n_cap, p.stages))
         return (int)cudaErrorInvalidValue;
     void* args[] = {(void*)&p, (void*)&c};
@@ -428,7 +489,7 @@ int enqueue_gemm_tc(Launcher& L, const GemmProblem& p, const KCtx& c) {
 }
 
 int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c) {
-    const int per_tok = p.epi.mode == EPI_SWIGLU ? 8 : 16;
+    const int per_tok = p.epi.mode == EPI_SWIGLU ? 16 : 32;
     const long total = (long)p.m_tiles * p.rows * per_tok;
     const int blocks = (int)std::min<long>((total + 255) / 256, 4096);
     void* args[] = {(void*)&p, (void*)&c};

@@ -46,10 +46,18 @@ struct EpiArgs {
 // Skinny GEMM  D[out_feature][token] = sum_k W[out_feature][k] * X[token][k]  on tcgen05.
 // Work unit = (group, 128-row tile, K segment); the K split is fixed by the shape so the
 // fp32 summation order never depends on the grid or on the token count.
+// Each pipeline stage holds kGemmKps consecutive 64-wide k-blocks: the 128-row weight tile
+// arrives in ONE TMA operation (32 KB) and the stage's activation rows in one more.
+constexpr int kGemmKps = 2;
+
 struct GemmProblem {
-    CUtensorMap tmA;        // weights, 2-D [groups * rows_per_group][K], box {64, 64}, SW128
-    CUtensorMap tmB;        // activations, 2-D [rows][K], box {64, 16}, SW128
+    // weights: plain  3-D {64, rows, k-blocks} box {64, 128, 2};
+    //          SwiGLU 4-D {64, rows, half, k-blocks} box {64, 64, 2, 2}, half = gate/up (I rows)
+    CUtensorMap tmA;
+    CUtensorMap tmB;        // activations, 3-D {64, rows, k-blocks}, box {64, n_cap, 2}, SW128
+    int a_4d;               // 1: SwiGLU (4-D weight map)
     int K, kb_total, ksplit;
+    int n_sb;               // stage blocks = ceil(kb_total / kGemmKps); K segments split these
     int m_tiles;            // 128-row tiles per group
     int n_groups;
     int rows_per_group;     // weight rows of one group
@@ -63,6 +71,8 @@ struct GemmProblem {
     int ring_bytes;         // bytes of the stage ring (also holds the staged accumulator)
     int serpentine;         // visit groups in reverse order
     float* partial;         // [m_tiles][ksplit][R][128] fp32 tiles (token-major rows)
+    int n_units;            // n_groups * m_tiles * ksplit
+    int grid;               // persistent CTAs (one per SM of the pool)
 };
 
 // Sum of the K segments of every partial tile + fused epilogue.
@@ -85,7 +95,7 @@ struct GemvProblem {
 };
 
 struct AttnProblem {
-    CUtensorMap tmK, tmV;   // caches as 2-D [seq * nkv * cap][64], box {64, 32}, SW128
+    CUtensorMap tmK, tmV;   // caches as 2-D [seq * nkv * cap][64], box {64, 128}, SW128
     const bf16* q;          // [T][nq * 64]
     const int* kv_len;      // [T]
     bf16* o;                // [T][nq * 64]

@@ -203,14 +203,26 @@ int check_dims(const sgp_dims* d) {
     return SGP_OK;
 }
 
-int qkv_rows(const sgp_dims& d) { return (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim; }
-int q_width(const sgp_dims& d) { return d.n_q_heads * d.head_dim; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// fixed K split of a projection: ~160 units in total, >= 4 k-blocks per segment
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return 1;
+    return n;
+}
+
+int qkv_rows(const sgp_dims& d) { return (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim; }
+int q_width(const sgp_dims& d) { return d.n_q_heads * d.head_dim; }
+
+// Fixed K split of a projection (a function of the shape only, so the fp32 summation order
+// never depends on the SM pool): ~456 work units for the persistent GEMM (3 per SM of a
+// 152-SM part), at least 4 k-blocks per segment.
 int choose_ksplit(int tiles, int kb_total) {
-    int ks = (int)std::lround(160.0 / tiles);
-    ks = std::max(1, std::min(ks, kb_total / 4));
+    const int n_sb = cdiv(kb_total, kGemmKps);  // K segments are made of whole stage blocks
+    int ks = (int)std::lround(456.0 / tiles);
+    ks = std::max(1, std::min(ks, n_sb / 2));
     return std::max(1, ks);
 }
 
@@ -348,6 +360,27 @@ struct Ws {
 // ---------------------------------------------------------------------------------------
 // tensor maps
 // ---------------------------------------------------------------------------------------
+// N-D bf16 tensor map with the 128-byte swizzle.  dims innermost first; strides in bytes
+// for dims 1..rank-1.
+int make_tmap_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides, const uint32_t* box) {
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    CUresult r = drv().encodeTiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                                   const_cast<void*>(base), d, st, b, es,
+                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail_drv(r, "cuTensorMapEncodeTiled");
+    return SGP_OK;
+}
+
 int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
               uint32_t box_inner, uint32_t box_rows) {
     cuuint64_t dims[2] = {inner, rows};
@@ -378,6 +411,7 @@ struct RunEnv {
     float* topk_w;
     bool tc_dense, tc_expert;
     int serpentine;
+    int pool_sms;       // SMs of the pool the kernels run on (persistent grid size)
 };
 
 int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
@@ -455,17 +489,40 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     GemmProblem p;
     memset(&p, 0, sizeof(p));
     int r;
+    // tokens per accumulator pass: the whole microbatch (dense) or the expected rows of a slot
+    // plus a quarter (grouped; a fuller slot takes a second pass)
+    int expect = grouped ? cdiv(R, gs.n_groups) : b;
+    if (grouped) expect += expect / 4;
+    p.n_cap = std::min(128, std::max(16, (expect + 15) & ~15));
+    const uint64_t kb_total = gs.K / 64, rowb = (uint64_t)gs.K * 2;
     const uint64_t total_rows = (uint64_t)gs.n_groups * gs.rows_per_group;
-    if ((r = make_tmap(&p.tmA, W, gs.K, total_rows, 64, 64)) != SGP_OK) return r;
-    if (grouped) {
-        if ((r = make_tmap(&p.tmB, X, gs.K, (uint64_t)xrows, 64, 16)) != SGP_OK) return r;
+    if (op == SGP_OP_EXPERT_UP) {
+        // {64, row, half, k-block}: the 64 gate rows and the 64 up rows of a tile land as one
+        // 128-row tile per k-block.  Rows are bounded so that row + half * I stays in range.
+        const uint64_t dims[4] = {64, total_rows - (uint64_t)d.inter, 2, kb_total};
+        const uint64_t str[3] = {rowb, (uint64_t)d.inter * rowb, 128};
+        const uint32_t box[4] = {64, 64, 2, (uint32_t)kGemmKps};
+        if ((r = make_tmap_nd(&p.tmA, W, 4, dims, str, box)) != SGP_OK) return r;
+        p.a_4d = 1;
     } else {
-        // only this microbatch's rows are visible to the loads (the rest is OOB = zero)
-        if ((r = make_tmap(&p.tmB, X + (size_t)row0 * gs.K, gs.K, (uint64_t)b, 64, 16)) != SGP_OK)
-            return r;
+        const uint64_t dims[3] = {64, total_rows, kb_total};
+        const uint64_t str[2] = {rowb, 128};
+        const uint32_t box[3] = {64, 128, (uint32_t)kGemmKps};
+        if ((r = make_tmap_nd(&p.tmA, W, 3, dims, str, box)) != SGP_OK) return r;
+        p.a_4d = 0;
+    }
+    {
+        // activations: grouped -> the slot-sorted matrix; dense -> only this microbatch's rows
+        // (the rest is out of bounds and reads as zero)
+        const bf16* xb = grouped ? X : X + (size_t)row0 * gs.K;
+        const uint64_t dims[3] = {64, (uint64_t)(grouped ? xrows : b), kb_total};
+        const uint64_t str[2] = {rowb, 128};
+        const uint32_t box[3] = {64, (uint32_t)p.n_cap, (uint32_t)kGemmKps};
+        if ((r = make_tmap_nd(&p.tmB, xb, 3, dims, str, box)) != SGP_OK) return r;
     }
     p.K = gs.K;
     p.kb_total = gs.K / 64;
+    p.n_sb = cdiv(p.kb_total, kGemmKps);
     p.ksplit = gs.ksplit;
     p.m_tiles = gs.m_tiles;
     p.n_groups = gs.n_groups;
@@ -476,12 +533,12 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     p.row0 = row0;
     p.nrows = b;
     p.R = grouped ? R : b;
-    int expect = grouped ? std::max(16, 2 * cdiv(R, gs.n_groups)) : b;
-    p.n_cap = std::min(256, std::max(16, (expect + 15) & ~15));
-    const int stage_bytes = 16384 + p.n_cap * 128;
-    // two CTAs per SM: ring + barriers within ~112 KB
-    p.stages = std::max(2, std::min(8, (110 * 1024) / stage_bytes));
+    const int stage_bytes = kGemmKps * (16384 + p.n_cap * 128);
+    // one persistent CTA per SM: ring + accumulator staging within the 227 KB limit
+    p.stages = std::max(2, std::min(8, (232448 - 1280 - p.n_cap * 512) / stage_bytes));
     p.ring_bytes = (int)gemm_tc_ring_bytes(p.n_cap, p.stages);
+    p.n_units = gs.n_groups * gs.m_tiles * gs.ksplit;
+    p.grid = e.pool_sms;
     p.serpentine = grouped && e.serpentine && (mu & 1);
     p.partial = e.ws.mu<float>(mu, e.ws.L->gemm_part);
     // the flag check belongs to the first launch, the publish to the last
@@ -523,8 +580,8 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
             AttnProblem p;
             memset(&p, 0, sizeof(p));
             const uint64_t rows = (uint64_t)e.T * d.n_kv_heads * e.layer->kv_cap;
-            if ((r = make_tmap(&p.tmK, e.layer->k_cache, 64, rows, 64, 32)) != SGP_OK) return r;
-            if ((r = make_tmap(&p.tmV, e.layer->v_cache, 64, rows, 64, 32)) != SGP_OK) return r;
+            if ((r = make_tmap(&p.tmK, e.layer->k_cache, 64, rows, 64, 128)) != SGP_OK) return r;
+            if ((r = make_tmap(&p.tmV, e.layer->v_cache, 64, rows, 64, 128)) != SGP_OK) return r;
             p.q = e.ws.at<bf16>(Lay.q);
             p.kv_len = e.kv_len;
             p.o = e.ws.at<bf16>(Lay.o);
@@ -622,7 +679,7 @@ int run_layer_stream(const sgp_dims& d, const sgp_layer* layer, int li, const in
                      cudaStream_t s) {
     StreamLauncher L(s);
     RunEnv e{&d, layer, kv_len, x_cur, x_out, T, ws, tki, tkw, use_tc_dense(d, T),
-             use_tc_expert(d, T), 0};
+             use_tc_expert(d, T), 0, device_sms()};
     for (int op = 0; op < SGP_N_OPS; ++op) {
         KCtx c = plain_ctx(ws.status(), kDefaultTimeout, ((uint32_t)op << 24) | ((uint32_t)li << 12));
         int r = enqueue_op(L, e, op, 0, c);
@@ -772,7 +829,7 @@ extern "C" int sgp_layer_op(const sgp_dims* d, const sgp_layer* layer, int op,
     Ws w{(uint8_t*)ws, &Lay};
     StreamLauncher L((cudaStream_t)stream);
     RunEnv e{d, layer, kv_len, (const bf16*)x_in, (bf16*)x_out, n_tokens, w, nullptr, nullptr,
-             use_tc_dense(*d, n_tokens), use_tc_expert(*d, n_tokens), 0};
+             use_tc_dense(*d, n_tokens), use_tc_expert(*d, n_tokens), 0, device_sms()};
     KCtx c = plain_ctx(w.status(), kDefaultTimeout, (uint32_t)op << 24);
     r = enqueue_op(L, e, op, 0, c);
     if (r == SGP_ERR_INVALID_ARG || r == SGP_ERR_CUDA) return r;
@@ -945,7 +1002,8 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
             RunEnv e{&d, &layers[l], kv_len, (const bf16*)(l == 0 ? x_in : x_out), (bf16*)x_out, T,
                      w, tki ? tki + (size_t)l * T * d.top_k : nullptr,
                      tkw ? tkw + (size_t)l * T * d.top_k : nullptr, tcd, tce,
-                     p->opts.serpentine_experts};
+                     p->opts.serpentine_experts,
+                     p->sctx[t.stage] ? p->split[t.stage] : device_sms()};
             int r = enqueue_op(L, e, op, t.mu, c);
             if (r != 0) {
                 cudaGraphDestroy(g);
