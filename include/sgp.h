@@ -251,6 +251,11 @@ typedef struct sgp_pipeline_opts {
                                    task; bit 1 = drop one TMA load of the first projection
                                    (its bounded wait then runs out)                          */
     int fault_task;             /* task index for fault bit 0                                */
+    int programmatic_launch;    /* 0 = default (on), -1 = off: consecutive kernels of one task
+                                   overlap launch and prologue with the previous kernel's tail
+                                   (programmatic dependent launch); results are identical    */
+    int trace;                  /* 1: every kernel records its first-CTA start and last-CTA
+                                   end (%globaltimer ns); read with sgp_pipeline_trace      */
 } sgp_pipeline_opts;
 
 /* Creates a pipeline for up to max_tokens sequences with KV length <= max_kv_len.
@@ -288,6 +293,15 @@ int sgp_pipeline_sync(sgp_pipeline* p);
 int sgp_pipeline_stage_times(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
                              const int32_t* kv_len, const void* x_in, void* x_out,
                              int n_tokens, int reps, float* t_us);
+
+/* Launch trace of the last run (pipeline created with opts.trace = 1).  Waits for the run,
+ * then writes n_pairs = n_layers * m * SGP_N_OPS * 2 pairs {start_ns, end_ns} to t_ns (host,
+ * at most max_pairs pairs), indexed [layer][microbatch][op][part]: part 0 is the op's main
+ * kernel, part 1 the kernel that finishes a tensor-core projection.  A pair of zeros means
+ * no such launch.  Start = earliest CTA start, end = latest CTA end, on the GPU's global
+ * timer; used to check the makespan model (Eq. 4-5) against the measured task spans.
+ * t_ns may be NULL to query n_pairs.  Returns SGP_OK, SGP_ERR_INVALID_ARG or SGP_ERR_CUDA. */
+int sgp_pipeline_trace(sgp_pipeline* p, uint64_t* t_ns, int max_pairs, int* n_pairs);
 
 /* Number of tasks of the last run's DAG and, when stamps != NULL, per-task
  * {stage, layer_first, micro, pred_data, pred_stage} as int32[5] rows (host memory). */

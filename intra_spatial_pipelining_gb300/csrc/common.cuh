@@ -27,6 +27,9 @@ struct KCtx {
     uint64_t timeout_ns;   // bounded-wait limit
     uint32_t tag;
     uint32_t fault;        // test-only fault injection bits
+    // Optional launch trace [2]: [0] = ~(earliest CTA start), [1] = latest CTA end, both
+    // %globaltimer ns, accumulated with atomicMax from a zeroed pair (NULL: off).
+    unsigned long long* trace;
 };
 
 enum : uint32_t { FAULT_SKIP_PUBLISH = 1u, FAULT_DROP_TMA = 2u };
@@ -46,22 +49,39 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// Programmatic dependent launch: the next kernel of a chain may start launching as soon as
+// every CTA of this one has called griddep_launch(); griddep_wait() blocks until the
+// previous kernel of the chain has completed and its writes are visible.  Every kernel
+// calls griddep_wait() in every thread before it reads anything a predecessor wrote (and
+// before any early return), which keeps completion transitive along the chain.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // First CTA checks that the producer task published its flag (a race detector for the
 // stage handoff: the graph edge must already have ordered the producer before us).
-__device__ __forceinline__ void task_begin(const KCtx& c) {
+__device__ __forceinline__ void task_begin(const KCtx& c, unsigned leader = 0) {
+    if (c.trace != nullptr && threadIdx.x == leader)
+        atomicMax(&c.trace[0], ~(unsigned long long)globaltimer());
     if (c.wait_flag != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
-        threadIdx.x == 0) {
+        threadIdx.x == leader) {
         uint32_t v = *((volatile const uint32_t*)c.wait_flag);
         if (v != 1u) report(c, ST_HANDOFF, v);
     }
 }
 
-// Every CTA of the task's last kernel calls this once, after its last global write.  The
-// CTA that completes the grid publishes the flag (release) and resets the counter.
+// Every CTA of every kernel calls this once, after its last global write.  In the task's
+// last kernel the CTA that completes the grid publishes the flag (release) and resets the
+// counter.
 __device__ __forceinline__ void task_end(const KCtx& c) {
-    if (c.post_flag == nullptr) return;
+    if (c.post_flag == nullptr && c.trace == nullptr) return;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && c.trace != nullptr)
+        atomicMax(&c.trace[1], (unsigned long long)globaltimer());
+    if (threadIdx.x == 0 && c.post_flag != nullptr) {
         __threadfence();
         uint32_t nblk = gridDim.x * gridDim.y * gridDim.z;
         uint32_t prev = atomicAdd(c.post_cnt, 1u);

@@ -1,15 +1,25 @@
 // GQA decode attention over a bf16 KV cache, split along the sequence (split-KV).
 //
-// One CTA = (sequence, KV head, chunk of kAttnChunk positions).  The KV cache is pure
-// streaming traffic, so it goes HBM -> shared memory by TMA with an L2 evict-first hint, in
-// stages of 128 positions: one 16 KB TMA operation for K and one for V (the per-SM rate of
-// TMA grows with the size of each operation), two stages in flight per CTA.  The four warps
-// split each stage (32 positions each) and release it through an "empty" barrier; one thread
-// refills it.  The G query heads that share a KV head form the M = 16 rows of warp-level
-// bf16 MMAs (rows >= G are zero): S = q K^T and O += P V with fp32 accumulation, an online
-// softmax with quad-shuffle row reductions in between.  The warps merge in a fixed order; a
-// sequence's chunks are merged (log-sum-exp combine) in chunk order by the last CTA to
-// finish, so the result does not depend on scheduling.  The same merge is the
+// Persistent: gridDim.x CTAs (one per SM of the pool), each of kAWarps independent streaming
+// warps.  The work is the flat list of chunks (sequence, KV head, chunk of P.chunk
+// positions); warp w of the grid owns a contiguous, equal share of that list, so the split
+// of work follows the pool size while every chunk's arithmetic does not.
+//
+// Every warp streams its chunks through a private ring of kASlots shared-memory stages of
+// 128 positions (one 16 KB TMA operation for K and one for V, L2 evict-first): lane 0
+// refills a stage as soon as the warp has consumed it, so a warp never waits on another.
+// Per stage the warp computes, on warp-level bf16 MMAs with fp32 accumulation,
+//     S^T = K q^T   (M = 16 positions, N = 8 query heads of the KV head, K = 64)
+//     O^T += V^T P^T (M = 16 dims, N = 8 heads, K = 16 positions),
+// i.e. the G query heads that share a KV head are the MMA's N dimension, so no tensor work
+// is spent on padding rows.  P goes from the accumulator layout of S^T to the operand layout
+// of the second product with movmatrix (an in-register 8x8 transpose).  An online softmax
+// (max over positions per head, base 2) runs between the two products.
+//
+// A chunk ends with its partial (running max, sum, unnormalised O) written to the workspace;
+// the warp that completes the last chunk of a (sequence, KV head) merges all its chunks in
+// chunk order (log-sum-exp combine).  Chunking and merge order are fixed by the shape, so the
+// output does not depend on the grid or on scheduling.  The same merge is the
 // partial-attention aggregation used when a sequence is split across partitions
 // ("Starscream: Reimagining LLM Sharding on AMD Instinct GPUs with GPU Partitioning",
 // sequence-length-sharded attention).
@@ -19,24 +29,28 @@ namespace sgp {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kStagePos = 128;                // positions per stage
-constexpr int kHalfBytes = kStagePos * 128;   // K (or V) of one stage: 16 KB
-constexpr int kStageBytes = 2 * kHalfBytes;   // K then V
-constexpr int kStages = 2;
-constexpr int kSub = kStagePos / kWarps;      // positions per warp per stage
+constexpr int kAWarps = 3;                   // streaming warps per CTA
+constexpr int kASlots = 2;                   // ring stages per warp
+constexpr int kAPos = 128;                   // positions per stage
+constexpr int kAHalf = kAPos * 128;          // K (or V) bytes of a stage: 16 KB
+constexpr int kAStage = 2 * kAHalf;          // K then V
+constexpr int kAMaxRows = 256;               // sequences per launch (prefix table size)
+constexpr size_t kARing = (size_t)kAWarps * kASlots * kAStage;
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 // D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col)
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -53,289 +67,394 @@ __device__ __forceinline__ uint32_t sw128(int r, int ch) {
     return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(kWarps * 32)
+// Where a warp stands in its share of the chunk list.
+struct Cursor {
+    int i;               // chunk index (>= end: done)
+    int t, kvh, c, S_t;  // sequence (launch-local), KV head, chunk of that pair, chunks/pair
+    int p0, p1;          // positions [p0, p1) of the chunk
+    int j, nst;          // stage within the chunk, stages of the chunk
+};
+
+__device__ __forceinline__ void cursor_at(Cursor& x, int i, const int* pre, const int* kvl,
+                                          int nrows, const AttnProblem& P) {
+    x.i = i;
+    int lo = 0, hi = nrows;  // largest t with pre[t] <= i  (pre[nrows] = total > i)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= i) lo = mid;
+        else hi = mid;
+    }
+    x.t = lo;
+    x.S_t = (pre[lo + 1] - pre[lo]) / P.nkv;
+    const int r = i - pre[lo];
+    x.kvh = r / x.S_t;
+    x.c = r - x.kvh * x.S_t;
+    const int L = kvl[lo];
+    const int first = P.window > 0 ? max(0, L - P.window) : 0;
+    x.p0 = first + x.c * P.chunk;
+    x.p1 = min(L, x.p0 + P.chunk);
+    x.j = 0;
+    x.nst = (x.p1 - x.p0 + kAPos - 1) / kAPos;
+}
+
+template <int NT>
+__device__ void merge_pair(const AttnProblem& P, int t, int kvh, int S_t, int lane) {
+    // lane -> head hl (fixed), dims d = lane / Gp + k * (32 / Gp)
+    constexpr int Gp = NT * 8;
+    constexpr int kPer = 64 * Gp / 32;
+    const int hl = lane % Gp, d0 = lane / Gp;
+    const size_t pair = (size_t)t * P.nkv + kvh;
+    const float* bml = P.part_ml + pair * P.S_max * 32;
+    const float* bacc = P.part_acc + pair * P.S_max * 64 * 16;
+    float M = -INFINITY;
+    for (int c = 0; c < S_t; ++c) M = fmaxf(M, __ldcg(bml + c * 32 + 2 * hl));
+    float O[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) O[k] = 0.f;
+    float Ls = 0.f;
+    int c = 0;
+    for (; c + 2 <= S_t; c += 2) {
+        const float m0 = __ldcg(bml + c * 32 + 2 * hl), l0 = __ldcg(bml + c * 32 + 2 * hl + 1);
+        const float m1 = __ldcg(bml + (c + 1) * 32 + 2 * hl);
+        const float l1 = __ldcg(bml + (c + 1) * 32 + 2 * hl + 1);
+        float a0[kPer], a1[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int d = d0 + k * (32 / Gp);
+            a0[k] = __ldcg(bacc + ((size_t)c * 64 + d) * 16 + hl);
+            a1[k] = __ldcg(bacc + ((size_t)(c + 1) * 64 + d) * 16 + hl);
+        }
+        const float w0 = exp2f(m0 - M), w1 = exp2f(m1 - M);
+        Ls = fmaf(w0, l0, Ls);
+        Ls = fmaf(w1, l1, Ls);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            O[k] = fmaf(w0, a0[k], O[k]);
+            O[k] = fmaf(w1, a1[k], O[k]);
+        }
+    }
+    for (; c < S_t; ++c) {
+        const float m0 = __ldcg(bml + c * 32 + 2 * hl), l0 = __ldcg(bml + c * 32 + 2 * hl + 1);
+        const float w0 = exp2f(m0 - M);
+        Ls = fmaf(w0, l0, Ls);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int d = d0 + k * (32 / Gp);
+            O[k] = fmaf(w0, __ldcg(bacc + ((size_t)c * 64 + d) * 16 + hl), O[k]);
+        }
+    }
+    if (hl < P.G) {
+        const float inv = 1.f / Ls;
+        bf16* o = P.o + (size_t)(P.row0 + t) * (P.nq * 64) + (size_t)(kvh * P.G + hl) * 64;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) o[d0 + k * (32 / Gp)] = __float2bfloat16_rn(O[k] * inv);
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kAWarps * 32, 1)
     attn_decode_kernel(const __grid_constant__ AttnProblem P, const KCtx ctx) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* empty = full + kStages;
-    int* sh_last = reinterpret_cast<int*>(empty + kStages);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kARing);  // [warp][slot]
+    int* pre = reinterpret_cast<int*>(full + kAWarps * kASlots);  // [kAMaxRows + 1]
+    int* kvl = pre + kAMaxRows + 1;                                 // [kAMaxRows]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int s = blockIdx.x, kvh = blockIdx.y, tl = blockIdx.z;
-    const int t = P.row0 + tl;
+    griddep_launch();
+    griddep_wait();
     task_begin(ctx);
 
-    const int L = P.kv_len[t];
-    if (L < 1 || L > P.cap) {
-        if (tid == 0) report(ctx, ST_BOUNDS, (uint32_t)L);
-        task_end(ctx);
-        return;
-    }
-    const int lo = P.window > 0 ? max(0, L - P.window) : 0;
-    const int S_t = (L - lo + P.chunk - 1) / P.chunk;
-    if (s >= S_t || S_t > P.S_max) {
-        if (S_t > P.S_max && tid == 0 && s == 0) report(ctx, ST_BOUNDS, (uint32_t)S_t);
-        task_end(ctx);
-        return;
-    }
-    const int p0 = lo + s * P.chunk;
-    const int p1 = min(L, p0 + P.chunk);
-    const int nstage = (p1 - p0 + kStagePos - 1) / kStagePos;
-    const int row_base = (t * P.nkv + kvh) * P.cap + p0;
-
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kWarps);
+    // ---- chunk counts and their prefix over the launch's sequences (warp 0) ----
+    if (warp == 0) {
+        int cnt[8], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = lane * 8 + k;
+            cnt[k] = 0;
+            if (t < P.nrows) {
+                const int L = P.kv_len[P.row0 + t];
+                kvl[t] = L;
+                if (L < 1 || L > P.cap) {
+                    if (blockIdx.x == 0) report(ctx, ST_BOUNDS, (uint32_t)L);
+                } else {
+                    const int first = P.window > 0 ? max(0, L - P.window) : 0;
+                    const int S = (L - first + P.chunk - 1) / P.chunk;
+                    if (S > P.S_max) {
+                        if (blockIdx.x == 0) report(ctx, ST_BOUNDS, (uint32_t)S);
+                    } else {
+                        cnt[k] = S * P.nkv;
+                    }
+                }
+            }
+            sum += cnt[k];
         }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = lane * 8 + k;
+            if (t < P.nrows) pre[t] = run;
+            run += cnt[k];
+        }
+        if (lane == 31) pre[P.nrows] = incl;
+        if (lane < kASlots * kAWarps) mbar_init(&full[lane], 1);
         fence_barrier_init();
-        prefetch_tensormap(&P.tmK);
-        prefetch_tensormap(&P.tmV);
+        if (lane == 0) {
+            prefetch_tensormap(&P.tmK);
+            prefetch_tensormap(&P.tmV);
+        }
     }
     __syncthreads();
 
+    const int total = pre[P.nrows];
+    const long long W = (long long)gridDim.x * kAWarps;
+    const long long gw = (long long)blockIdx.x * kAWarps + warp;
+    const int i0 = (int)(gw * total / W), i1 = (int)((gw + 1) * total / W);
+
+    uint8_t* ring = smem + (size_t)warp * kASlots * kAStage;
+    uint64_t* wfull = full + warp * kASlots;
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int i) {  // stage i -> ring slot i % kStages
-        uint8_t* sk = smem + (i % kStages) * kStageBytes;
-        uint64_t* bar = &full[i % kStages];
-        mbar_arrive_expect_tx(bar, kStageBytes);
-        tma_load_2d(sk, &P.tmK, bar, 0, row_base + i * kStagePos, pol);
-        tma_load_2d(sk + kHalfBytes, &P.tmV, bar, 0, row_base + i * kStagePos, pol);
-    };
-    int issued = 0;
-    if (tid == 0)
-        for (; issued < kStages && issued < nstage; ++issued) issue(issued);
+    const int g = lane >> 2, cq = lane & 3;
 
-    // query fragments (A operand, 16 rows x 64): rows g < G are the heads of this KV head
-    const int G = P.G;
-    const bool rows_b = G > 8;  // rows 8..15 hold heads only when a group exceeds 8
-    const int hA = lane >> 2, hB = hA + 8;
-    uint32_t aq[4][4];
-    {
-        const bf16* qa = P.q + (size_t)t * (P.nq * 64) + (size_t)(kvh * G) * 64;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const int c = kk * 16 + 2 * (lane & 3);
-            auto ld2 = [&](int h, int col) -> uint32_t {
-                if (h >= G) return 0u;
-                return *reinterpret_cast<const uint32_t*>(qa + (size_t)h * 64 + col);
-            };
-            aq[kk][0] = ld2(hA, c);
-            aq[kk][1] = ld2(hB, c);
-            aq[kk][2] = ld2(hA, c + 8);
-            aq[kk][3] = ld2(hB, c + 8);
+    Cursor cs, ld;
+    if (i0 < i1) cursor_at(cs, i0, pre, kvl, P.nrows, P);
+    else cs.i = i1;
+    ld = cs;
+    uint32_t n_iss = 0, n_con = 0;
+    auto issue = [&]() {  // next stage of `ld` -> slot n_iss % kASlots, then advance `ld`
+        if (lane == 0) {
+            uint8_t* dst = ring + (n_iss % kASlots) * kAStage;
+            uint64_t* bar = &wfull[n_iss % kASlots];
+            const int row = ((P.row0 + ld.t) * P.nkv + ld.kvh) * P.cap + ld.p0 + ld.j * kAPos;
+            mbar_arrive_expect_tx(bar, kAStage);
+            tma_load_2d(dst, &P.tmK, bar, 0, row, pol);
+            tma_load_2d(dst + kAHalf, &P.tmV, bar, 0, row, pol);
         }
-    }
+        ++n_iss;
+        if (++ld.j == ld.nst) {
+            if (ld.i + 1 < i1) cursor_at(ld, ld.i + 1, pre, kvl, P.nrows, P);
+            else ld.i = i1;
+        }
+    };
+    while (ld.i < i1 && n_iss < (uint32_t)kASlots) issue();
 
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-    float oacc[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+    uint32_t qf[NT][4][2];
+    int q_t = -1, q_h = -1;
+    float m_run[NT][2], l_run[NT][2], oacc[4][NT][4];
     bool failed = false;
 
-    for (int i = 0; i < nstage; ++i) {
-        const int st = i % kStages;
-        const uint32_t par = (uint32_t)(i / kStages) & 1u;
-        if (!mbar_wait(&full[st], par, ctx.timeout_ns)) {
+    while (cs.i < i1) {
+        if (cs.j == 0) {
+            if (cs.t != q_t || cs.kvh != q_h) {  // query fragments of the new (sequence, KV head)
+                q_t = cs.t;
+                q_h = cs.kvh;
+                const bf16* qa =
+                    P.q + (size_t)(P.row0 + cs.t) * (P.nq * 64) + (size_t)(cs.kvh * P.G) * 64;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int h = nt * 8 + g;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int col = kk * 16 + 2 * cq;
+                        qf[nt][kk][0] = h < P.G ? *reinterpret_cast<const uint32_t*>(qa + h * 64 + col) : 0u;
+                        qf[nt][kk][1] =
+                            h < P.G ? *reinterpret_cast<const uint32_t*>(qa + h * 64 + col + 8) : 0u;
+                    }
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                m_run[nt][0] = m_run[nt][1] = -INFINITY;
+                l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+                for (int md = 0; md < 4; ++md)
+                    oacc[md][nt][0] = oacc[md][nt][1] = oacc[md][nt][2] = oacc[md][nt][3] = 0.f;
+            }
+        }
+        const int slot = n_con % kASlots;
+        const bool ok = mbar_wait(&wfull[slot], (n_con / kASlots) & 1u, ctx.timeout_ns);
+        if (__any_sync(0xffffffffu, !ok)) {
             if (lane == 0) report(ctx, ST_TIMEOUT, 10);
             failed = true;
+            break;
         }
-        failed = __any_sync(0xffffffffu, failed);
-        if (failed) break;
-        // this warp's 32 positions of the stage
-        uint8_t* sk = smem + st * kStageBytes + warp * kSub * 128;
-        uint8_t* sv = sk + kHalfBytes;
-        const int valid = min(kSub, p1 - (p0 + i * kStagePos + warp * kSub));
-        if (valid > 0) {
-            if (valid < kSub) {
-                // positions past the sequence: zero K and V (the cache there is arbitrary)
-                for (int r = valid; r < kSub; ++r) {
-                    reinterpret_cast<uint32_t*>(sk + r * 128)[lane] = 0u;
-                    reinterpret_cast<uint32_t*>(sv + r * 128)[lane] = 0u;
-                }
-                __syncwarp();
-            }
-            const uint32_t ka = smem_u32(sk), va = smem_u32(sv);
+        uint8_t* sk = ring + slot * kAStage;
+        const uint32_t ka = smem_u32(sk), va = ka + kAHalf;
+        const int valid = min(kAPos, cs.p1 - (cs.p0 + cs.j * kAPos));
+        if (valid < kAPos) {
+            // positions past the chunk: zero V (the cache there is arbitrary, P is 0 there)
+            uint4* v4 = reinterpret_cast<uint4*>(sk + kAHalf);
+            for (int e = valid * 8 + lane; e < kAPos * 8; e += 32) v4[e] = make_uint4(0, 0, 0, 0);
+            __syncwarp();
+        }
 
-            // S = q K^T : 4 n-tiles of 8 positions
-            float sacc[4][4];
+        // ---- S^T = K q^T: 8 position tiles x NT head tiles ----
+        float s[8][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
-                const int r = nt * 8 + (lane & 7);
-                uint32_t b[8];
-                ldsm_x4(ka + sw128(r, (lane >> 3)), b[0], b[1], b[2], b[3]);
-                ldsm_x4(ka + sw128(r, 4 + (lane >> 3)), b[4], b[5], b[6], b[7]);
+        for (int mt = 0; mt < 8; ++mt) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma16816(sacc[nt], aq[kk], b[2 * kk], b[2 * kk + 1]);
-            }
-            // scale, mask, online softmax (rows hA -> regs 0,1 ; hB -> regs 2,3)
+            for (int nt = 0; nt < NT; ++nt) s[mt][nt][0] = s[mt][nt][1] = s[mt][nt][2] = s[mt][nt][3] = 0.f;
+            const int r = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                if (hr == 1 && !rows_b) break;
-                float mx = -INFINITY;
+            for (int kk = 0; kk < 4; ++kk) {
+                uint32_t a[4];
+                ldsm_x4(ka + sw128(r, kk * 2 + (lane >> 4)), a);
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int pos = nt * 8 + 2 * (lane & 3) + e;
-                        float v = sacc[nt][2 * hr + e] * P.scale_log2;
-                        v = pos < valid ? v : -INFINITY;
-                        sacc[nt][2 * hr + e] = v;
-                        mx = fmaxf(mx, v);
-                    }
-                }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run[hr], mx);
-                const float corr = exp2f(m_run[hr] - m_new);
-                float rs = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pv = exp2f(sacc[nt][2 * hr + e] - m_new);
-                        sacc[nt][2 * hr + e] = pv;
-                        rs += pv;
-                    }
-                }
-                rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-                rs += __shfl_xor_sync(0xffffffffu, rs, 2);
-                l_run[hr] = l_run[hr] * corr + rs;
-                m_run[hr] = m_new;
-#pragma unroll
-                for (int nd = 0; nd < 8; ++nd) {
-                    oacc[nd][2 * hr] *= corr;
-                    oacc[nd][2 * hr + 1] *= corr;
-                }
-            }
-            if (!rows_b) {
-                // rows 8..15 are padding: keep their probabilities at zero
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) sacc[nt][2] = sacc[nt][3] = 0.f;
-            }
-            // O += P V : 2 k-steps of 16 positions x 8 n-tiles of 8 dims
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                uint32_t ap[4];
-                ap[0] = pack_bf16x2(sacc[2 * kk][0], sacc[2 * kk][1]);
-                ap[1] = pack_bf16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
-                ap[2] = pack_bf16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-                ap[3] = pack_bf16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-                const int mi = lane >> 3;
-                const int r = kk * 16 + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                for (int nd = 0; nd < 8; nd += 2) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(va + sw128(r, nd + (mi >> 1)), b0, b1, b2, b3);
-                    mma16816(oacc[nd], ap, b0, b1);
-                    mma16816(oacc[nd + 1], ap, b2, b3);
-                }
+                for (int nt = 0; nt < NT; ++nt) mma16816(s[mt][nt], a, qf[nt][kk][0], qf[nt][kk][1]);
             }
         }
-        // release the stage; one thread refills it once every warp is done with it
+        // ---- online softmax over this stage's positions (heads 2cq, 2cq+1 of each tile) ----
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    float v0 = s[mt][nt][2 * hf] * P.scale_log2;
+                    float v1 = s[mt][nt][2 * hf + 1] * P.scale_log2;
+                    if (valid < kAPos && mt * 16 + hf * 8 + g >= valid) v0 = v1 = -INFINITY;
+                    s[mt][nt][2 * hf] = v0;
+                    s[mt][nt][2 * hf + 1] = v1;
+                    mx0 = fmaxf(mx0, v0);
+                    mx1 = fmaxf(mx1, v1);
+                }
+            }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float n0 = fmaxf(m_run[nt][0], mx0), n1 = fmaxf(m_run[nt][1], mx1);
+            const float c0 = m_run[nt][0] == -INFINITY ? 0.f : exp2f(m_run[nt][0] - n0);
+            const float c1 = m_run[nt][1] == -INFINITY ? 0.f : exp2f(m_run[nt][1] - n1);
+            m_run[nt][0] = n0;
+            m_run[nt][1] = n1;
+            float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const float e0 = exp2f(s[mt][nt][2 * hf] - n0);
+                    const float e1 = exp2f(s[mt][nt][2 * hf + 1] - n1);
+                    s[mt][nt][2 * hf] = e0;
+                    s[mt][nt][2 * hf + 1] = e1;
+                    r0 += e0;
+                    r1 += e1;
+                }
+            }
+            // per-lane partial sums; reduced over the position lanes at the end of the chunk
+            l_run[nt][0] = l_run[nt][0] * c0 + r0;
+            l_run[nt][1] = l_run[nt][1] * c1 + r1;
+#pragma unroll
+            for (int md = 0; md < 4; ++md) {
+                oacc[md][nt][0] *= c0;
+                oacc[md][nt][1] *= c1;
+                oacc[md][nt][2] *= c0;
+                oacc[md][nt][3] *= c1;
+            }
+        }
+        // ---- O^T += V^T P^T: 8 position steps of 16 x 4 dim tiles x NT head tiles ----
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t b0[NT], b1[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                b0[nt] = movmatrix_t(pack_bf16x2(s[ks][nt][0], s[ks][nt][1]));
+                b1[nt] = movmatrix_t(pack_bf16x2(s[ks][nt][2], s[ks][nt][3]));
+            }
+            const int r = ks * 16 + ((lane >> 4) << 3) + (lane & 7);
+#pragma unroll
+            for (int md = 0; md < 4; ++md) {
+                uint32_t a[4];
+                ldsm_x4_t(va + sw128(r, md * 2 + ((lane >> 3) & 1)), a);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816(oacc[md][nt], a, b0[nt], b1[nt]);
+            }
+        }
+        // ---- release the stage: this warp refills it ----
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        if (tid == 0 && issued < nstage) {
-            if (!mbar_wait(&empty[st], par, ctx.timeout_ns)) {
-                report(ctx, ST_TIMEOUT, 11);
-                failed = true;
-            } else {
-                issue(issued);
-                ++issued;
-            }
-        }
-        failed = __any_sync(0xffffffffu, failed);
-        if (failed) break;
-    }
+        ++n_con;
+        if (ld.i < i1) issue();
 
-    // ---- merge the four warps (fixed order) ----
-    __syncthreads();  // all stages consumed: stage memory is free (no TMA pending unless failed)
-    if (__syncthreads_or(failed)) {
-        // drain loads still in flight (bounded): every issued stage completes its full phase
-        if (tid == 0) {
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                (void)mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u, 10000000ull);
-        }
-        __syncthreads();
-        task_end(ctx);
-        return;
-    }
-    float* sm_m = reinterpret_cast<float*>(smem);   // [4][16]
-    float* sm_l = sm_m + kWarps * 16;               // [4][16]
-    float* sm_o = sm_l + kWarps * 16;               // [4][16][64]
+        if (cs.j == cs.nst - 1) {
+            // ---- end of chunk: row sums over the position lanes, then partial or output ----
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        const int h = hA + 8 * hr;
-        if ((lane & 3) == 0) {
-            sm_m[warp * 16 + h] = m_run[hr];
-            sm_l[warp * 16 + h] = l_run[hr];
-        }
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nd = 0; nd < 8; ++nd) {
-            const int d = nd * 8 + 2 * (lane & 3);
-            sm_o[(warp * 16 + h) * 64 + d] = oacc[nd][2 * hr];
-            sm_o[(warp * 16 + h) * 64 + d + 1] = oacc[nd][2 * hr + 1];
-        }
-    }
-    __syncthreads();
-
-    const size_t pair = (size_t)tl * P.nkv + kvh;
-    float* pml = P.part_ml + (pair * P.S_max + s) * 32;
-    float* pacc = P.part_acc + (pair * P.S_max + s) * 16 * 64;
-    for (int i = tid; i < G * 64; i += kWarps * 32) {
-        const int h = i >> 6, d = i & 63;
-        float M = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 16 + h]);
-        float Ls = 0.f, O = 0.f;
-        for (int w = 0; w < kWarps; ++w) {
-            const float f = exp2f(sm_m[w * 16 + h] - M);  // exp2(-inf) = 0 for idle warps
-            Ls += f * sm_l[w * 16 + h];
-            O += f * sm_o[(w * 16 + h) * 64 + d];
-        }
-        if (S_t == 1) {
-            P.o[(size_t)t * (P.nq * 64) + (size_t)(kvh * G + h) * 64 + d] =
-                __float2bfloat16_rn(O / Ls);
-        } else {
-            pacc[h * 64 + d] = O;
-            if (d == 0) {
-                pml[2 * h] = M;
-                pml[2 * h + 1] = Ls;
-            }
-        }
-    }
-    if (S_t > 1) {
-        // ---- the last chunk of this (sequence, KV head) merges all chunks in order ----
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const uint32_t prev = atomicAdd(&P.cnt[pair], 1u);
-            *sh_last = (prev == (uint32_t)S_t - 1) ? 1 : 0;
-            if (*sh_last) P.cnt[pair] = 0;
-        }
-        __syncthreads();
-        if (*sh_last) {
-            __threadfence();
-            const float* bml = P.part_ml + pair * P.S_max * 32;
-            const float* bacc = P.part_acc + pair * P.S_max * 16 * 64;
-            for (int i = tid; i < G * 64; i += kWarps * 32) {
-                const int h = i >> 6, d = i & 63;
-                float M = -INFINITY;
-                for (int c = 0; c < S_t; ++c) M = fmaxf(M, __ldcg(bml + c * 32 + 2 * h));
-                float Ls = 0.f, O = 0.f;
-                for (int c = 0; c < S_t; ++c) {
-                    const float f = exp2f(__ldcg(bml + c * 32 + 2 * h) - M);
-                    Ls += f * __ldcg(bml + c * 32 + 2 * h + 1);
-                    O += f * __ldcg(bacc + (c * 16 + h) * 64 + d);
+                for (int o = 4; o < 32; o <<= 1) {
+                    l_run[nt][0] += __shfl_xor_sync(0xffffffffu, l_run[nt][0], o);
+                    l_run[nt][1] += __shfl_xor_sync(0xffffffffu, l_run[nt][1], o);
                 }
-                P.o[(size_t)t * (P.nq * 64) + (size_t)(kvh * G + h) * 64 + d] =
-                    __float2bfloat16_rn(O / Ls);
+            const size_t pair = (size_t)cs.t * P.nkv + cs.kvh;
+            if (cs.S_t == 1) {
+                bf16* o = P.o + (size_t)(P.row0 + cs.t) * (P.nq * 64) + (size_t)(cs.kvh * P.G) * 64;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int h = nt * 8 + 2 * cq;
+                    const float i0f = 1.f / l_run[nt][0], i1f = 1.f / l_run[nt][1];
+#pragma unroll
+                    for (int md = 0; md < 4; ++md) {
+                        const int d = md * 16 + g;
+                        if (h < P.G) {
+                            o[h * 64 + d] = __float2bfloat16_rn(oacc[md][nt][0] * i0f);
+                            o[h * 64 + d + 8] = __float2bfloat16_rn(oacc[md][nt][2] * i0f);
+                        }
+                        if (h + 1 < P.G) {
+                            o[(h + 1) * 64 + d] = __float2bfloat16_rn(oacc[md][nt][1] * i1f);
+                            o[(h + 1) * 64 + d + 8] = __float2bfloat16_rn(oacc[md][nt][3] * i1f);
+                        }
+                    }
+                }
+            } else {
+                float* pml = P.part_ml + (pair * P.S_max + cs.c) * 32;
+                float* pacc = P.part_acc + (pair * P.S_max + cs.c) * 64 * 16;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int h = nt * 8 + 2 * cq;
+#pragma unroll
+                    for (int md = 0; md < 4; ++md) {
+                        const int d = md * 16 + g;
+                        *reinterpret_cast<float2*>(pacc + d * 16 + h) =
+                            make_float2(oacc[md][nt][0], oacc[md][nt][1]);
+                        *reinterpret_cast<float2*>(pacc + (d + 8) * 16 + h) =
+                            make_float2(oacc[md][nt][2], oacc[md][nt][3]);
+                    }
+                    if (g == 0)
+                        *reinterpret_cast<float4*>(pml + 2 * h) =
+                            make_float4(m_run[nt][0], l_run[nt][0], m_run[nt][1], l_run[nt][1]);
+                }
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    const uint32_t prev = atomicAdd(&P.cnt[pair], 1u);
+                    last = prev == (uint32_t)cs.S_t - 1;
+                    if (last) P.cnt[pair] = 0;
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence();
+                    merge_pair<NT>(P, cs.t, cs.kvh, cs.S_t, lane);
+                }
             }
         }
+        if (++cs.j == cs.nst) {
+            if (cs.i + 1 < i1) cursor_at(cs, cs.i + 1, pre, kvl, P.nrows, P);
+            else cs.i = i1;
+        }
+    }
+    if (failed) {
+        // drain this warp's loads still in flight (bounded)
+        for (uint32_t q = n_con; q < n_iss; ++q)
+            (void)mbar_wait(&wfull[q % kASlots], (q / kASlots) & 1u, 10000000ull);
     }
     task_end(ctx);
 }
@@ -343,10 +462,13 @@ __global__ void __launch_bounds__(kWarps * 32)
 }  // namespace
 
 int enqueue_attention(Launcher& L, const AttnProblem& p, const KCtx& c) {
-    dim3 grid(p.S_max, p.nkv, p.nrows), block(kWarps * 32);
-    size_t smem = kStages * kStageBytes + 1024 + 256;  // merge scratch reuses the stages
+    if (p.nrows < 1 || p.nrows > kAMaxRows || p.G < 1 || p.G > 16 || p.chunk % kAPos)
+        return (int)cudaErrorInvalidValue;
+    dim3 grid(p.n_cta > 0 ? p.n_cta : 1), block(kAWarps * 32);
+    size_t smem = kARing + 1024 + kAWarps * kASlots * 8 + (2 * kAMaxRows + 1) * 4;
     void* args[] = {(void*)&p, (void*)&c};
-    return L.launch((const void*)attn_decode_kernel, grid, block, smem, args);
+    const void* f = p.G > 8 ? (const void*)attn_decode_kernel<2> : (const void*)attn_decode_kernel<1>;
+    return L.launch(f, grid, block, smem, args);
 }
 
 }  // namespace sgp

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* sh_err = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    task_begin(ctx);
+    griddep_launch();
     uint32_t acc_cols = 32;
     while (acc_cols < (uint32_t)P.n_cap) acc_cols <<= 1;
 
@@ -123,6 +123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Only the producer of a dense problem may run ahead of the previous kernel: it streams
+    // constant weights into the first ring stages before it waits.  A grouped problem's
+    // token ranges come from the previous kernel, so there everyone waits now.
+    const bool run_ahead = warp == 0 && lane == 0 && P.group_offsets == nullptr;
+    if (!run_ahead) griddep_wait();
+    task_begin(ctx, 32);
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -132,6 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             uint32_t issued_mask = 0, issued_par = 0;
             bool dropped = false;
+            // activation loads deferred until the previous kernel has completed
+            bool waited = !run_ahead;
+            int pend_n = 0, pend_s[8], pend_row[8], pend_kb[8];
             for (int u = blockIdx.x; u < P.n_units && !*(volatile int*)sh_err; u += gridDim.x) {
                 const Unit x = unit_info(P, u, ctx);
                 const int rowA1 = x.g * P.rows_per_group + x.mt * P.a_tile_stride;
@@ -140,6 +149,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < x.nk; ++i, ++it) {
                         const int s = it % S;
                         const uint32_t j = it / S;
+                        if (!waited && j > 0) {
+                            // every stage holds weights; the previous kernel must be complete
+                            // before the deferred activation loads (and any reuse) go out
+                            griddep_wait();
+                            waited = true;
+                            for (int q = 0; q < pend_n; ++q)
+                                tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + kStageA,
+                                            &P.tmB, &full[pend_s[q]], 0, pend_row[q], pend_kb[q],
+                                            pol_x);
+                        }
                         if (j > 0 && !mbar_wait(&empty[s], (j - 1) & 1, ctx.timeout_ns)) {
                             report(ctx, ST_TIMEOUT, 1);
                             atomicExch(sh_err, 1);
@@ -157,12 +176,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_4d(sa, &P.tmA, &full[s], 0, rowA1, 0, kb, pol_w);
                         else
                             tma_load_3d(sa, &P.tmA, &full[s], 0, rowA1, kb, pol_w);
-                        tma_load_3d(sb, &P.tmB, &full[s], 0, x.tma_r0 + c0, kb, pol_x);
+                        if (!waited) {  // first pass over the ring: activations wait
+                            pend_s[pend_n] = s;
+                            pend_row[pend_n] = x.tma_r0 + c0;
+                            pend_kb[pend_n] = kb;
+                            ++pend_n;
+                        } else {
+                            tma_load_3d(sb, &P.tmB, &full[s], 0, x.tma_r0 + c0, kb, pol_x);
+                        }
                         issued_mask |= 1u << s;
                         issued_par = (issued_par & ~(1u << s)) | ((j & 1u) << s);
                     }
                     if (*(volatile int*)sh_err) break;
                 }
+            }
+            if (!waited) {
+                griddep_wait();
+                for (int q = 0; q < pend_n; ++q)
+                    tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + kStageA, &P.tmB,
+                                &full[pend_s[q]], 0, pend_row[q], pend_kb[q], pol_x);
             }
             if (*(volatile int*)sh_err) {
                 // drain loads still in flight into this CTA's shared memory (bounded)
@@ -300,6 +332,8 @@ __device__ __forceinline__ float4 sum_segments(const float* p, size_t sstride, i
 }
 
 __global__ void __launch_bounds__(256) gemm_finish_kernel(const FinishProblem P, const KCtx ctx) {
+    griddep_launch();
+    griddep_wait();
     task_begin(ctx);
     const EpiArgs& e = P.epi;
     const bool swiglu = e.mode == EPI_SWIGLU;
@@ -403,6 +437,8 @@ __device__ __forceinline__ void gemv_store(const EpiArgs& e, const KCtx& c, int 
 }
 
 __global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KCtx ctx) {
+    griddep_launch();
+    griddep_wait();
     task_begin(ctx);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int f = blockIdx.x * 8 + warp;

@@ -16,6 +16,8 @@ namespace {
 // RMSNorm: y = bf16(x * rsqrt(mean(x^2) + eps) * g), one CTA per row
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const NormProblem P, const KCtx ctx) {
+    griddep_launch();
+    griddep_wait();
     task_begin(ctx);
     __shared__ float red[8];
     const int row = P.row0 + blockIdx.x;
@@ -60,6 +62,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const NormProblem P, const
 constexpr int kRouterTok = 8;
 
 __global__ void __launch_bounds__(256) router_kernel(const RouterProblem P, const KCtx ctx) {
+    griddep_launch();
+    griddep_wait();
     task_begin(ctx);
     extern __shared__ uint8_t smem_raw[];
     uint4* us = reinterpret_cast<uint4*>(smem_raw);  // [8][H/8]
@@ -244,6 +248,8 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterProblem P, cons
 constexpr int kDispRows = 8;
 
 __global__ void __launch_bounds__(256) dispatch_kernel(const DispatchProblem P, const KCtx ctx) {
+    griddep_launch();
+    griddep_wait();
     task_begin(ctx);
     extern __shared__ int sm_i[];
     const int R = P.nrows * P.k;
@@ -318,6 +324,8 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const DispatchProblem P, 
 // Combine: out[t] = bf16(h[t] + sum_j w[t][j] * Y[pair_pos[t k + j]]), j in pick order
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, const KCtx ctx) {
+    griddep_launch();
+    griddep_wait();
     task_begin(ctx);
     const int tl = blockIdx.x;
     const int row = P.row0 + tl;

@@ -99,11 +99,12 @@ struct AttnProblem {
     const bf16* q;          // [T][nq * 64]
     const int* kv_len;      // [T]
     bf16* o;                // [T][nq * 64]
-    float* part_ml;         // [nrows * nkv][S_max][16][2]
-    float* part_acc;        // [nrows * nkv][S_max][16][64]
+    float* part_ml;         // [nrows * nkv][S_max][16 heads][2]  (max, sum)
+    float* part_acc;        // [nrows * nkv][S_max][64 dims][16 heads]
     uint32_t* cnt;          // [nrows * nkv]
     int row0, nrows, nq, nkv, G, cap, window, chunk, S_max;
     float scale_log2;       // log2(e) / sqrt(d)
+    int n_cta;              // persistent CTAs (one per SM of the pool)
 };
 
 struct NormProblem {
@@ -164,6 +165,6 @@ int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c);
 size_t gemm_tc_ring_bytes(int n_cap, int stages);
 size_t gemm_tc_smem_bytes(int n_cap, int stages);
 // attention chunk length (positions per split-KV work item); fixed, never SM-dependent
-constexpr int kAttnChunk = 512;
+constexpr int kAttnChunk = 1024;
 
 }  // namespace sgp

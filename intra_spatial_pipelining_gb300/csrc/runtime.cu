@@ -131,22 +131,43 @@ int ensure_smem_attr(const void* func, size_t smem) {
 // =======================================================================================
 // launchers
 // =======================================================================================
+// Every kernel of this library starts with griddepcontrol.launch_dependents and calls
+// griddepcontrol.wait before it touches memory a predecessor wrote (or may still read), so
+// consecutive launches may overlap their launch latency and prologue with the tail of the
+// previous kernel (programmatic dependent launch).
 struct StreamLauncher : Launcher {
     cudaStream_t s;
-    explicit StreamLauncher(cudaStream_t st) : s(st) {}
+    bool pdl;
+    explicit StreamLauncher(cudaStream_t st, bool programmatic = true) : s(st), pdl(programmatic) {}
     int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) override {
         int e = ensure_smem_attr(func, smem);
         if (e) return e;
-        return (int)cudaLaunchKernel(func, grid, block, args, smem, s);
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return (int)cudaLaunchKernelExC(&cfg, func, args);
     }
 };
 
-// Appends kernel nodes to a CUDA graph as a chain, bound to one (green) context.
+// Appends kernel nodes to a CUDA graph as a chain, bound to one (green) context.  When the
+// only dependency of a node is the previous kernel of the same chain and `pdl` is set, the
+// edge is programmatic (it fires once every CTA of that kernel has started).
 struct GraphLauncher : Launcher {
     CUgraph g;
     CUcontext ctx;
     std::vector<CUgraphNode> deps;
-    GraphLauncher(CUgraph graph, CUcontext c) : g(graph), ctx(c) {}
+    bool pdl = false;
+    bool chained = false;  // deps holds exactly the previous kernel of this chain
+    GraphLauncher(CUgraph graph, CUcontext c, bool programmatic = false)
+        : g(graph), ctx(c), pdl(programmatic) {}
     int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) override {
         int e = ensure_smem_attr(func, smem);
         if (e) return e;
@@ -168,13 +189,19 @@ struct GraphLauncher : Launcher {
         np.kernel.sharedMemBytes = (unsigned)smem;
         np.kernel.kernelParams = args;
         CUgraphNode n;
-        CUresult r = drv().graphAddNode(&n, g, deps.empty() ? nullptr : deps.data(), nullptr,
-                                        deps.size(), &np);
+        CUgraphEdgeData ed;
+        memset(&ed, 0, sizeof(ed));
+        ed.from_port = CU_GRAPH_KERNEL_NODE_PORT_PROGRAMMATIC;
+        ed.type = CU_GRAPH_DEPENDENCY_TYPE_PROGRAMMATIC;
+        const bool prog = pdl && chained && deps.size() == 1;
+        CUresult r = drv().graphAddNode(&n, g, deps.empty() ? nullptr : deps.data(),
+                                        prog ? &ed : nullptr, deps.size(), &np);
         if (r != CUDA_SUCCESS) {
             g_err = "cuGraphAddNode: CUresult " + std::to_string((int)r);
             return (int)cudaErrorUnknown;
         }
         deps.assign(1, n);
+        chained = true;
         return 0;
     }
 };
@@ -269,7 +296,8 @@ int attn_smax(int max_kv) { return std::max(1, cdiv(max_kv, kAttnChunk)); }
 struct Layout {
     int T = 0, m = 1, b = 0, S_max = 1, n_flags = 0;
     size_t status = 0, zero_beg = 0, zero_end = 0;
-    size_t attn_cnt = 0, router_cnt = 0, flags = 0, flag_cnt = 0;
+    size_t attn_cnt = 0, router_cnt = 0, flags = 0, flag_cnt = 0, trace = 0;
+    int n_trace = 0;  // trace pairs (0: tracing off)
     size_t a = 0, q = 0, o = 0, h = 0, u = 0;
     size_t per_mu = 0;  // bytes of one microbatch's scratch block
     size_t mu_base = 0;
@@ -282,7 +310,7 @@ struct Layout {
 
 size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
-Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags) {
+Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags, int n_trace = 0) {
     Layout L;
     L.T = T;
     L.m = m;
@@ -308,6 +336,8 @@ Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags) {
     L.router_cnt = take((size_t)m * cdiv(b, 8) * 4);
     L.flags = take((size_t)std::max(1, n_flags) * 4);
     L.flag_cnt = take((size_t)std::max(1, n_flags) * 4);
+    L.n_trace = n_trace;
+    if (n_trace > 0) L.trace = take((size_t)n_trace * 16);
     L.zero_end = off;
     L.a = take((size_t)T * H * 2);
     L.q = take((size_t)T * qw * 2);
@@ -547,6 +577,7 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     c1.post_cnt = nullptr;
     c2.wait_flag = nullptr;
     c2.fault = 0;
+    if (c.trace) c2.trace = c.trace + 2;  // the finishing kernel has the op's second slot
     if ((r = enqueue_gemm_tc(L, p, c1)) != 0) return r;
     FinishProblem f;
     memset(&f, 0, sizeof(f));
@@ -601,6 +632,7 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
             p.S_max = attn_smax(span);
             if (p.S_max > Lay.S_max) return fail_arg("kv_cap exceeds the workspace's max_kv_len");
             p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
+            p.n_cta = e.pool_sms;
             return enqueue_attention(L, p, c);
         }
         case SGP_OP_ROUTER: {
@@ -880,6 +912,7 @@ struct sgp_pipeline {
     std::vector<uint8_t> key;
     std::vector<PTask> tasks;
     cudaStream_t last_stream = nullptr;
+    int trace_pairs = 0;  // launch-trace pairs the cached graph writes
 };
 
 namespace {
@@ -929,13 +962,14 @@ std::vector<PTask> build_tasks(const sgp_pipeline& p, const sgp_layer* layers, i
     return out;
 }
 
-int ensure_ws(sgp_pipeline* p, int T, int nflags) {
-    if (p->ws && p->ws_T == T && p->ws_nflags >= nflags) return SGP_OK;
+int ensure_ws(sgp_pipeline* p, int T, int nflags, int ntrace = 0) {
+    if (p->ws && p->ws_T == T && p->ws_nflags >= nflags && p->lay.n_trace >= ntrace)
+        return SGP_OK;
     if (p->ws) {
         cudaFree(p->ws);
         p->ws = nullptr;
     }
-    Layout L = make_layout(p->dims, T, T / p->micro, p->max_kv, nflags);
+    Layout L = make_layout(p->dims, T, T / p->micro, p->max_kv, nflags, ntrace);
     cudaError_t e = cudaMalloc(&p->ws, L.total);
     if (e != cudaSuccess) {
         g_err = std::string("cudaMalloc: ") + cudaGetErrorString(e);
@@ -980,7 +1014,7 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
     for (size_t i = 0; i < tasks.size(); ++i) {
         const PTask& t = tasks[i];
         if (stage_only >= 0 && t.stage != stage_only) continue;
-        GraphLauncher L((CUgraph)g, p->sctx[t.stage]);
+        GraphLauncher L((CUgraph)g, p->sctx[t.stage], p->opts.programmatic_launch >= 0);
         const bool keep_data = stage_only < 0;
         if (keep_data && t.pred_data >= 0) L.deps.push_back(last[t.pred_data]);
         if (t.pred_stage >= 0 && last[t.pred_stage]) L.deps.push_back(last[t.pred_stage]);
@@ -999,6 +1033,9 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
                     c.fault |= FAULT_SKIP_PUBLISH;
             }
             if ((p->opts.fault_inject & 2u) && i == 0 && op == SGP_OP_QKV) c.fault |= FAULT_DROP_TMA;
+            if (p->lay.n_trace > 0)
+                c.trace = w.at<unsigned long long>(p->lay.trace) +
+                          4 * (((size_t)l * p->lay.m + t.mu) * SGP_N_OPS + op);
             RunEnv e{&d, &layers[l], kv_len, (const bf16*)(l == 0 ? x_in : x_out), (bf16*)x_out, T,
                      w, tki ? tki + (size_t)l * T * d.top_k : nullptr,
                      tkw ? tkw + (size_t)l * T * d.top_k : nullptr, tcd, tce,
@@ -1223,13 +1260,15 @@ extern "C" int sgp_pipeline_run(sgp_pipeline* p, const sgp_layer* layers, int n_
     if (!p->exec || key != p->key) {
         const int m = n_tokens / p->micro;
         std::vector<PTask> tasks = build_tasks(*p, layers, n_layers, m);
-        if ((r = ensure_ws(p, n_tokens, (int)tasks.size())) != SGP_OK) return r;
+        const int ntrace = p->opts.trace ? n_layers * m * SGP_N_OPS * 2 : 0;
+        if ((r = ensure_ws(p, n_tokens, (int)tasks.size(), ntrace)) != SGP_OK) return r;
         // ensure_ws recomputed the layout for this token count
         if (p->lay.m != m) {
             cudaFree(p->ws);
             p->ws = nullptr;
-            if ((r = ensure_ws(p, n_tokens, (int)tasks.size())) != SGP_OK) return r;
+            if ((r = ensure_ws(p, n_tokens, (int)tasks.size(), ntrace)) != SGP_OK) return r;
         }
+        p->trace_pairs = ntrace;
         cudaGraph_t g;
         if ((r = build_graph(p, tasks, layers, kv_len, x_in, x_out, n_tokens, topk_idx, topk_w, -1,
                              &g)) != SGP_OK)
@@ -1321,6 +1360,23 @@ extern "C" int sgp_pipeline_tasks(sgp_pipeline* p, int* n_tasks, int32_t* rows, 
             rows[5 * i + 3] = t.pred_data;
             rows[5 * i + 4] = t.pred_stage;
         }
+    return SGP_OK;
+}
+
+extern "C" int sgp_pipeline_trace(sgp_pipeline* p, uint64_t* t_ns, int max_pairs, int* n_pairs) {
+    if (!p || !n_pairs) return fail_arg("NULL");
+    if (!p->opts.trace) return fail_arg("pipeline was created without opts.trace");
+    if (!p->exec) return fail_arg("no run yet");
+    *n_pairs = p->trace_pairs;
+    if (!t_ns || max_pairs <= 0) return SGP_OK;
+    if (p->last_stream) CK(cudaStreamSynchronize(p->last_stream));
+    const int n = std::min(max_pairs, p->trace_pairs);
+    std::vector<unsigned long long> h((size_t)n * 2);
+    CK(cudaMemcpy(h.data(), p->ws + p->lay.trace, h.size() * 8, cudaMemcpyDeviceToHost));
+    for (int i = 0; i < n; ++i) {
+        t_ns[2 * i] = h[2 * i] ? ~h[2 * i] : 0;  // stored complemented (max of ~t = min t)
+        t_ns[2 * i + 1] = h[2 * i + 1];
+    }
     return SGP_OK;
 }
 

@@ -58,7 +58,8 @@ class sgp_pipeline_opts(C.Structure):
     _fields_ = [("custom_cut", C.c_int), ("stage_of_op", (C.c_int * N_OPS) * 2),
                 ("use_green_contexts", C.c_int), ("green_ctx_flags", C.c_int),
                 ("serpentine_experts", C.c_int), ("wait_timeout_ns", C.c_uint64),
-                ("fault_inject", C.c_uint32), ("fault_task", C.c_int)]
+                ("fault_inject", C.c_uint32), ("fault_task", C.c_int),
+                ("programmatic_launch", C.c_int), ("trace", C.c_int)]
 
 
 _lib = None
@@ -94,6 +95,8 @@ _SIGS = {
                                            C.POINTER(C.c_float)]),
     "sgp_pipeline_tasks": (C.c_int, [C.c_void_p, C.POINTER(C.c_int), C.POINTER(C.c_int32),
                                      C.c_int]),
+    "sgp_pipeline_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_int,
+                                     C.POINTER(C.c_int)]),
     "sgp_pipeline_destroy": (None, [C.c_void_p]),
     "sgp_enumerate_splits": (C.c_int, [C.c_int, C.c_int, C.c_int, C.POINTER(C.c_int), C.c_int]),
     "sgp_pipeline_balance": (C.c_int, [C.POINTER(sgp_dims), C.POINTER(sgp_layer), C.c_int,
@@ -172,7 +175,8 @@ def layer_array(layers: Sequence[sgp_layer]):
 
 def make_opts(stage_of_op=None, use_green_contexts: int = 0, green_ctx_flags: int = 0,
               serpentine_experts: int = 0, wait_timeout_ns: int = 0, fault_inject: int = 0,
-              fault_task: int = 0) -> sgp_pipeline_opts:
+              fault_task: int = 0, programmatic_launch: int = 0,
+              trace: int = 0) -> sgp_pipeline_opts:
     o = sgp_pipeline_opts()
     if stage_of_op is not None:
         o.custom_cut = 1
@@ -185,6 +189,8 @@ def make_opts(stage_of_op=None, use_green_contexts: int = 0, green_ctx_flags: in
     o.wait_timeout_ns = wait_timeout_ns
     o.fault_inject = fault_inject
     o.fault_task = fault_task
+    o.programmatic_launch = programmatic_launch
+    o.trace = trace
     return o
 
 
@@ -281,6 +287,18 @@ def sgp_pipeline_tasks(p) -> list:
     rows = (C.c_int32 * (5 * max(1, n.value)))()
     check(lib().sgp_pipeline_tasks(p, C.byref(n), rows, n.value), "sgp_pipeline_tasks")
     return [tuple(rows[5 * i:5 * i + 5]) for i in range(n.value)]
+
+
+def sgp_pipeline_trace(p):
+    """Launch trace of the last run as an int64 array [n_pairs][2] of (start_ns, end_ns),
+    indexed [layer][microbatch][op][part] (flattened); zeros mark launches that do not exist."""
+    import numpy as np
+    n = C.c_int()
+    check(lib().sgp_pipeline_trace(p, None, 0, C.byref(n)), "sgp_pipeline_trace")
+    out = np.zeros((max(1, n.value), 2), dtype=np.uint64)
+    check(lib().sgp_pipeline_trace(p, out.ctypes.data_as(C.POINTER(C.c_uint64)), n.value,
+                                   C.byref(n)), "sgp_pipeline_trace")
+    return out[:n.value].astype(np.int64)
 
 
 def sgp_pipeline_destroy(p) -> None:

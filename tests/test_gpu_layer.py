@@ -1,6 +1,8 @@
 """GPU parity of one decode layer (temporal execution) against the fp64 oracle,
 through the C ABI.  Tolerance: max|err| <= 2e-2 * max|ref| per bf16 tensor;
 routing sets bit-exact (inputs keep a top-k logit margin >= 1e-3)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -38,14 +40,18 @@ def _check_layer(inp, ref, res, T):
     errs = {}
     for name in ("a", "q", "o", "h", "u"):
         errs[name] = H.assert_close(name, dmp[name], ref[name])
-    errs["logits"] = H.assert_close("logits", dmp["logits"], ref["logits"], tol=1e-3)
+    ltol = 1e-3
+    errs["logits"] = H.assert_close("logits", dmp["logits"], ref["logits"], tol=ltol)
     assert H.routing_sets(res["idx"]) == H.routing_sets(ref["idx"])
-    # weights matched by expert index
+    # weights matched by expert index.  w = softmax over the selected logits, and
+    # sum_i |dw_j/dz_i| = 2 w_j (1 - w_j) <= 1/2, so the logit bound above implies
+    # |dw| <= ltol * max|z| / 2.
+    wtol = 0.5 * ltol * float(np.abs(np.asarray(ref["logits"])).max())
     gi, gw = res["idx"].cpu().numpy(), res["w"].cpu().numpy()
     for t in range(T):
         g = dict(zip(gi[t].tolist(), gw[t].tolist()))
         for e, wv in zip(ref["idx"][t].tolist(), ref["w"][t].tolist()):
-            assert abs(g[e] - wv) <= 1e-4, (t, e, g[e], wv)
+            assert abs(g[e] - wv) <= wtol, (t, e, g[e], wv, wtol)
     assert abs(float(gw.sum(axis=1).max()) - 1.0) < 1e-5
     # routed rows: slot order, pair positions
     off = dmp["slot_offsets"].cpu().numpy()
@@ -94,11 +100,11 @@ def test_gptoss_layer_vs_oracle():
 
 @pytest.mark.parametrize("window", [0, 16, 200])
 def test_ragged_lengths_and_windows(window):
-    """Sequence lengths at tile and chunk edges (1, 31, 32, 33, 511, 512, 513, 1100)."""
-    wl = synth.WORKLOADS["tiny"].with_(n_tokens=8, kv_len=1200, kv_cap=1200)
+    """Sequence lengths at MMA-tile, stage (128) and chunk (1024) edges."""
+    wl = synth.WORKLOADS["tiny"].with_(n_tokens=8, kv_len=2400, kv_cap=2400)
     for a in range(20):
         inp = H.make_inputs(wl, 3, [a])
-        inp.kv_len.copy_(torch.tensor([1, 31, 32, 33, 511, 512, 513, 1100], dtype=torch.int32))
+        inp.kv_len.copy_(torch.tensor([1, 17, 128, 129, 1023, 1024, 1025, 2300], dtype=torch.int32))
         # override the layer's window
         lay = inp.sgp_layers()[0]
         lay.window = window
@@ -116,6 +122,27 @@ def test_ragged_lengths_and_windows(window):
     assert sgp.sgp_status_from_workspace(ws) == sgp.SGP_OK
     H.assert_close("o", bufs["o"], ref["o"])
     H.assert_close("x_next", out, ref["x_next"])
+
+
+@pytest.mark.parametrize("G", [1, 4, 8, 12, 16])
+def test_attention_group_sizes(G):
+    """Query heads per KV head from 1 to 16 (one or two head tiles, with padding heads)."""
+    shape = dataclasses.replace(synth.SHAPE_TINY, n_q_heads=2 * G, n_kv_heads=2)
+    wl = synth.WORKLOADS["tiny"].with_(shape=shape, n_tokens=6, kv_len=2200, kv_cap=2200)
+    inp = H.make_inputs(wl, 5)
+    inp.kv_len.copy_(torch.tensor([1, 100, 1024, 1500, 2049, 2200], dtype=torch.int32))
+    lay = inp.sgp_layers()[0]
+    w = {n: (v.cpu() if v is not None else None) for n, v in inp.weights[0].items()}
+    k, v = synth.kv_cache(wl, 0, inp.seed, "cpu")
+    ref = O.layer(wl.shape, w, O.f64(inp.x), inp.kv_len.cpu().numpy(), O.f64(k), O.f64(v), 0)
+    d = H.dims(wl.shape, sgp.PATH_TC)
+    ws = H.workspace(d, wl.n_tokens, wl.cap)
+    out = torch.empty_like(inp.x)
+    bufs, st = H.dump_buffers(wl.shape, wl.n_tokens)
+    sgp.sgp_layer_temporal(d, lay, inp.kv_len, inp.x, out, wl.n_tokens, None, None, ws, st)
+    assert sgp.sgp_status_from_workspace(ws) == sgp.SGP_OK
+    H.assert_close("q", bufs["q"], ref["q"])
+    H.assert_close("o", bufs["o"], ref["o"])
 
 
 def test_invalid_arguments_are_rejected():
