@@ -62,6 +62,22 @@ def parse():
 # ------------------------------------------------------------------------------------------
 # helpers
 # ------------------------------------------------------------------------------------------
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The job's time: the slowest rank's (every rank runs an independent replica)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the tokens of all replicas over the job's time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def workload(args):
     from intra_spatial_pipelining_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
@@ -344,11 +360,8 @@ def run_sgp(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
         sgp.check(sgp.sgp_pipeline_sync(p), "timed runs")
-        ms = e0.elapsed_time(e1)
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
             dist.barrier()
         return ms / steps
 
@@ -388,12 +401,8 @@ def run_sgp(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
         sgp.check(sgp.sgp_pipeline_sync(pipe), "e2e runs")
-        ms_e2e = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": world * T / (ms_e2e * 1e-3), "unit": UNIT,
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+        e2e = {"value": job_tokens_per_s(T, world, ms_e2e), "unit": UNIT,
                "h2d_bytes_per_step": hx.numel() * hx.element_size(),
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                "ms_per_step": ms_e2e}
@@ -430,7 +439,7 @@ def run_sgp(args, rank, world, local_rank):
     if rank != 0:
         return
     total_bytes = algorithmic_bytes(wl)
-    value = world * T / (ms_pipe * 1e-3)
+    value = job_tokens_per_s(T, world, ms_pipe)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(wl, args.seed)
@@ -451,7 +460,7 @@ def run_sgp(args, rank, world, local_rank):
         "dram_algorithmic_gbs": total_bytes / (ms_pipe * 1e-3) / 1e9,
         "dram_pct_of_peak": 100.0 * total_bytes / (ms_pipe * 1e-3) / 1e9 / peak,
         "temporal": None if ms_temp is None else {
-            "iteration_us": ms_temp * 1e3, "tokens_per_s": world * T / (ms_temp * 1e-3),
+            "iteration_us": ms_temp * 1e3, "tokens_per_s": job_tokens_per_s(T, world, ms_temp),
             "dram_pct_of_peak": 100.0 * total_bytes / (ms_temp * 1e-3) / 1e9 / peak,
             "pipeline_speedup": ms_temp / ms_pipe},
         "balance": None if balance_rows is None else [

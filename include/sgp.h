@@ -251,9 +251,9 @@ typedef struct sgp_pipeline_opts {
                                    task; bit 1 = drop one TMA load of the first projection
                                    (its bounded wait then runs out)                          */
     int fault_task;             /* task index for fault bit 0                                */
-    int programmatic_launch;    /* 0 = default (on), -1 = off: consecutive kernels of one task
-                                   overlap launch and prologue with the previous kernel's tail
-                                   (programmatic dependent launch); results are identical    */
+    int programmatic_launch;    /* 1: consecutive kernels of one task overlap launch and
+                                   prologue with the previous kernel's tail (programmatic
+                                   dependent launch); 0 = default (off); results identical  */
     int trace;                  /* 1: every kernel records its first-CTA start and last-CTA
                                    end (%globaltimer ns); read with sgp_pipeline_trace      */
 } sgp_pipeline_opts;

@@ -138,7 +138,7 @@ int ensure_smem_attr(const void* func, size_t smem) {
 struct StreamLauncher : Launcher {
     cudaStream_t s;
     bool pdl;
-    explicit StreamLauncher(cudaStream_t st, bool programmatic = true) : s(st), pdl(programmatic) {}
+    explicit StreamLauncher(cudaStream_t st, bool programmatic = false) : s(st), pdl(programmatic) {}
     int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) override {
         int e = ensure_smem_attr(func, smem);
         if (e) return e;
@@ -1014,7 +1014,7 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
     for (size_t i = 0; i < tasks.size(); ++i) {
         const PTask& t = tasks[i];
         if (stage_only >= 0 && t.stage != stage_only) continue;
-        GraphLauncher L((CUgraph)g, p->sctx[t.stage], p->opts.programmatic_launch >= 0);
+        GraphLauncher L((CUgraph)g, p->sctx[t.stage], p->opts.programmatic_launch > 0);
         const bool keep_data = stage_only < 0;
         if (keep_data && t.pred_data >= 0) L.deps.push_back(last[t.pred_data]);
         if (t.pred_stage >= 0 && last[t.pred_stage]) L.deps.push_back(last[t.pred_stage]);

@@ -104,6 +104,51 @@ def test_task_dag_matches_schedule_model():
     assert g == m
 
 
+def test_measured_task_spans_respect_dag_and_eq4():
+    """Per-task spans from the device launch trace (first-CTA start of the task's first
+    kernel, last-CTA end of its last kernel): every task starts after both its data and
+    its stage predecessor ended, and the Eq. 4-5 makespan computed from the measured task
+    durations is at most the measured makespan (launch gaps only add time)."""
+    wl, inp = _stack_inputs(4, 1024, 11)
+    d = H.dims(wl.shape)
+    T, L, micro = wl.n_tokens, wl.n_layers, 16
+    m = T // micro
+    p = sgp.sgp_pipeline_create(d, _splits(2), 2, micro, T, wl.cap, sgp.make_opts(trace=1))
+    try:
+        out = torch.empty_like(inp.x)
+        for _ in range(2):
+            inp.reset_caches()
+            sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, T)
+            assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK
+        tr = sgp.sgp_pipeline_trace(p).reshape(L, m, sgp.N_OPS, 2, 2)
+        tasks = sgp.sgp_pipeline_tasks(p)
+    finally:
+        sgp.sgp_pipeline_destroy(p)
+    ops = {0: range(0, 3), 1: range(3, sgp.N_OPS)}  # default cut
+    span = []
+    for st, l, mu, _, _ in tasks:
+        k = tr[l, mu, list(ops[st])].reshape(-1, 2)
+        k = k[k[:, 1] > 0]
+        assert len(k) > 0
+        span.append((int(k[:, 0].min()), int(k[:, 1].max())))
+    for i, (st, l, mu, pd, ps) in enumerate(tasks):
+        for j in (pd, ps):
+            if j >= 0:
+                assert span[i][0] >= span[j][1], (i, j, span[i], span[j])
+    key = {(t[0], t[1], t[2]): i for i, t in enumerate(tasks)}
+    model = S.build_tasks(L, m, 2)
+    tau = []
+    for x in model:
+        s0, s1 = span[key[(x["stage"] - 1, x["layer"], x["micro"])]]
+        tau.append((s1 - s0) * 1e-3)
+    t_model, _, _ = S.makespan(model, tau)
+    t0 = min(a for a, _ in span)
+    t_meas = (max(b for _, b in span) - t0) * 1e-3
+    print(f"Eq. 4-5 makespan of measured durations {t_model:.1f} us, measured {t_meas:.1f} us")
+    assert t_model <= t_meas + 1e-6
+    assert abs(S.longest_path(model, tau) - t_model) < 1e-6
+
+
 def test_macro_cut_bit_identical():
     """Full-attention FMHA alone on stage 0, everything else (including sliding-window
     attention) on stage 1: tasks span layer boundaries."""
