@@ -54,187 +54,269 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const NormProblem P, const
 }
 
 // ---------------------------------------------------------------------------------------
-// Router.  grid = (token groups of 8, expert groups of 8).  Each CTA normalises its 8 tokens
-// (u = RMSNorm(h; g)), one warp per expert computes the 8 fp32 logits, and the last CTA of
-// a token group selects the top-k of each token (descending logit, ties to the lower
-// index) and the softmax over the selected logits.
+// Router.  grid = (token groups of 16, expert groups of 8), 16 warps.
+//   (0) the CTA's 8 router rows and the gain g go to shared memory by cp.async;
+//   (1) warp w normalises token w: u = bf16(RMSNorm(h; g)) into shared memory (rows padded
+//       by 16 bytes so ldmatrix rows fall on distinct banks) and, from the first expert
+//       group, to global memory;
+//   (2) logits z = u W_r^T on warp-level bf16 tensor-core MMAs with fp32 accumulation
+//       (M = 16 tokens, N = 8 experts); the 16 warps split K and their partial tiles are
+//       added in warp order;
+//   (3) the last CTA of a token group selects each token's top-k (descending logit, ties to
+//       the lower index, a NaN logit ranks below every number) and the softmax over the
+//       selected logits, one warp per token.
 // ---------------------------------------------------------------------------------------
-constexpr int kRouterTok = 8;
+constexpr int kRouterTok = 16;
+constexpr int kRouterWarps = 16;
 
-__global__ void __launch_bounds__(256) router_kernel(const RouterProblem P, const KCtx ctx) {
+__host__ __device__ inline int router_row_bytes(int H) { return H * 2 + 16; }
+// u rows, router rows and g (the first two reused for the logit rows of the top-k), then the
+// MMA partials
+__host__ __device__ inline size_t router_rows_bytes(int H, int E) {
+    const size_t rows = (size_t)(kRouterTok + 8 + 1) * router_row_bytes(H);
+    const size_t logit_rows = (size_t)kRouterWarps * E * sizeof(float);
+    return rows > logit_rows ? rows : logit_rows;
+}
+inline size_t router_smem_bytes(int H, int E) {
+    return router_rows_bytes(H, E) + (size_t)kRouterWarps * 16 * 8 * sizeof(float);
+}
+
+__device__ __forceinline__ void ldsm_x4_r(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_r(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kRouterWarps * 32, 1)
+    router_kernel(const RouterProblem P, const KCtx ctx) {
     griddep_launch();
     griddep_wait();
     task_begin(ctx);
-    extern __shared__ uint8_t smem_raw[];
-    uint4* us = reinterpret_cast<uint4*>(smem_raw);  // [8][H/8]
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int rb = router_row_bytes(P.H);
+    uint8_t* u_s = smem_raw;                                   // [16][rb]
+    uint8_t* w_s = u_s + (size_t)kRouterTok * rb;              // [8][rb]
+    uint8_t* g_s = w_s + (size_t)8 * rb;                       // [rb]
+    float* red = reinterpret_cast<float*>(smem_raw + router_rows_bytes(P.H, P.E));  // [16][16][8]
     __shared__ int sh_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tg = blockIdx.x;
     const int nv = P.H >> 3;
     const int ntok = min(kRouterTok, P.nrows - tg * kRouterTok);
+    const int e0 = blockIdx.y * 8;
+    const uint4 z4 = make_uint4(0, 0, 0, 0);
 
-    // Router weight row of this warp's expert: issue its loads first (registers), so they
-    // overlap the normalisation below.  H <= kMaxVec * 256.
-    constexpr int kMaxVec = 4;  // 16-byte vectors per lane per block of 32 * kMaxVec
-    const int e = blockIdx.y * 8 + warp;
-    const bool has_e = e < P.E;
-    const uint4* wrow = reinterpret_cast<const uint4*>(P.Wr + (size_t)(has_e ? e : 0) * P.H);
+    // (0) router rows of experts e0 .. e0+7 (rows past E are zero) and g, by cp.async
+    if (warp < 8) {
+        const int e = e0 + warp;
+        uint8_t* dst = w_s + (size_t)warp * rb;
+        if (e < P.E) {
+            const uint4* src = reinterpret_cast<const uint4*>(P.Wr + (size_t)e * P.H);
+            for (int v = lane; v < nv; v += 32) cp_async16(dst + v * 16, src + v);
+        } else {
+            for (int v = lane; v < nv; v += 32) *reinterpret_cast<uint4*>(dst + v * 16) = z4;
+        }
+    } else {
+        const uint4* src = reinterpret_cast<const uint4*>(P.g);
+        for (int v = threadIdx.x - 256; v < nv; v += 256) cp_async16(g_s + v * 16, src + v);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
 
-    // (1) RMSNorm of this group's tokens, warp w -> token w (row kept in registers)
-    if (warp < ntok) {
-        const int row = P.row0 + tg * kRouterTok + warp;
-        const uint4* h = reinterpret_cast<const uint4*>(P.h + (size_t)row * P.H);
-        const uint4* g = reinterpret_cast<const uint4*>(P.g);
-        uint4* uo = reinterpret_cast<uint4*>(P.u + (size_t)row * P.H);
+    // (1) u = RMSNorm(h; g) of token `warp` (rows past the group are zero)
+    constexpr int kRV = 12;  // 16-byte vectors per lane kept in registers (H <= 3072)
+    const bool has_t = warp < ntok;
+    const int row = P.row0 + tg * kRouterTok + (has_t ? warp : 0);
+    const uint4* hrow = reinterpret_cast<const uint4*>(P.h + (size_t)row * P.H);
+    uint4* uo = reinterpret_cast<uint4*>(P.u + (size_t)row * P.H);
+    uint8_t* udst = u_s + (size_t)warp * rb;
+    const uint4* gs4 = reinterpret_cast<const uint4*>(g_s);
+    auto put = [&](int v, const uint4& hq, float inv) {
+        float f[8], gg[8];
+        unpack8(hq, f);
+        unpack8(gs4[v], gg);
+        uint4 o;
+        o.x = pack_bf16x2(f[0] * inv * gg[0], f[1] * inv * gg[1]);
+        o.y = pack_bf16x2(f[2] * inv * gg[2], f[3] * inv * gg[3]);
+        o.z = pack_bf16x2(f[4] * inv * gg[4], f[5] * inv * gg[5]);
+        o.w = pack_bf16x2(f[6] * inv * gg[6], f[7] * inv * gg[7]);
+        *reinterpret_cast<uint4*>(udst + v * 16) = o;
+        if (blockIdx.y == 0) uo[v] = o;
+    };
+    if (nv <= 32 * kRV) {
+        uint4 hv[kRV];
+#pragma unroll
+        for (int i = 0; i < kRV; ++i) {
+            const int v = i * 32 + lane;
+            hv[i] = (has_t && v < nv) ? hrow[v] : z4;
+        }
         float ss = 0.f;
-        for (int v0 = 0; v0 < nv; v0 += 32 * kMaxVec) {
-            uint4 hv[kMaxVec];
 #pragma unroll
-            for (int i = 0; i < kMaxVec; ++i) {
-                const int v = v0 + i * 32 + lane;
-                hv[i] = v < nv ? h[v] : make_uint4(0, 0, 0, 0);
-            }
+        for (int i = 0; i < kRV; ++i) {
+            float f[8];
+            unpack8(hv[i], f);
 #pragma unroll
-            for (int i = 0; i < kMaxVec; ++i) {
-                float f[8];
-                unpack8(hv[i], f);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
-            }
+            for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
         }
         ss = warp_sum(ss);
         const float inv = rsqrtf(ss / (float)P.H + P.eps);
-        for (int v0 = 0; v0 < nv; v0 += 32 * kMaxVec) {
-            uint4 hv[kMaxVec], gv[kMaxVec];
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();  // g (and the router rows) visible to every warp
+        if (has_t) {
 #pragma unroll
-            for (int i = 0; i < kMaxVec; ++i) {
-                const int v = v0 + i * 32 + lane;
-                hv[i] = v < nv ? h[v] : make_uint4(0, 0, 0, 0);
-                gv[i] = v < nv ? g[v] : make_uint4(0, 0, 0, 0);
+            for (int i = 0; i < kRV; ++i) {
+                const int v = i * 32 + lane;
+                if (v < nv) put(v, hv[i], inv);
             }
+        } else {
+            for (int v = lane; v < nv; v += 32) *reinterpret_cast<uint4*>(udst + v * 16) = z4;
+        }
+    } else {
+        float ss = 0.f;
+        if (has_t)
+            for (int v = lane; v < nv; v += 32) {
+                float f[8];
+                unpack8(hrow[v], f);
 #pragma unroll
-            for (int i = 0; i < kMaxVec; ++i) {
-                const int v = v0 + i * 32 + lane;
-                if (v < nv) {
-                    float f[8], gg[8];
-                    unpack8(hv[i], f);
-                    unpack8(gv[i], gg);
-                    uint4 o;
-                    o.x = pack_bf16x2(f[0] * inv * gg[0], f[1] * inv * gg[1]);
-                    o.y = pack_bf16x2(f[2] * inv * gg[2], f[3] * inv * gg[3]);
-                    o.z = pack_bf16x2(f[4] * inv * gg[4], f[5] * inv * gg[5]);
-                    o.w = pack_bf16x2(f[6] * inv * gg[6], f[7] * inv * gg[7]);
-                    us[warp * nv + v] = o;
-                    if (blockIdx.y == 0) uo[v] = o;
-                }
+                for (int q = 0; q < 8; ++q) ss = fmaf(f[q], f[q], ss);
             }
+        ss = warp_sum(ss);
+        const float inv = rsqrtf(ss / (float)P.H + P.eps);
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        if (has_t) {
+            for (int v = lane; v < nv; v += 32) put(v, hrow[v], inv);
+        } else {
+            for (int v = lane; v < nv; v += 32) *reinterpret_cast<uint4*>(udst + v * 16) = z4;
         }
     }
     __syncthreads();
 
-    // (2) logits, warp w -> expert e
-    if (has_e) {
-        float acc[kRouterTok];
-#pragma unroll
-        for (int i = 0; i < kRouterTok; ++i) acc[i] = 0.f;
-        for (int v0 = 0; v0 < nv; v0 += 32 * kMaxVec) {
-            uint4 wv[kMaxVec];
-#pragma unroll
-            for (int i = 0; i < kMaxVec; ++i) {
-                const int v = v0 + i * 32 + lane;
-                wv[i] = v < nv ? __ldg(wrow + v) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int i = 0; i < kMaxVec; ++i) {
-                const int v = v0 + i * 32 + lane;
-                if (v < nv) {
-                    float wf[8];
-                    unpack8(wv[i], wf);
-#pragma unroll
-                    for (int t = 0; t < kRouterTok; ++t) {
-                        if (t < ntok) {
-                            float uf[8];
-                            unpack8(us[t * nv + v], uf);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) acc[t] = fmaf(wf[q], uf[q], acc[t]);
-                        }
-                    }
-                }
-            }
+    // (2) logits: warp w takes k-steps [w * KS / 16, (w + 1) * KS / 16) of KS = H / 16
+    {
+        const int KS = P.H >> 4;
+        const int k0 = warp * KS / kRouterWarps, k1 = (warp + 1) * KS / kRouterWarps;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t ua = smem_u32(u_s) + (uint32_t)((lane & 15) * rb + (lane >> 4) * 16);
+        const uint32_t wa = smem_u32(w_s) + (uint32_t)((lane & 7) * rb + ((lane >> 3) & 1) * 16);
+        for (int kk = k0; kk < k1; ++kk) {
+            uint32_t a[4], b0, b1;
+            ldsm_x4_r(ua + kk * 32, a);
+            ldsm_x2_r(wa + kk * 32, b0, b1);
+            mma_bf16_16816(acc, a, b0, b1);
         }
-        const float b = P.bias ? P.bias[e] : 0.f;
+        // partial tile: rows (tokens) lane/4 and lane/4 + 8, columns (experts) 2(lane%4), +1
+        float* rw = red + warp * 128;
+        const int rr = lane >> 2, cc = 2 * (lane & 3);
+        rw[rr * 8 + cc] = acc[0];
+        rw[rr * 8 + cc + 1] = acc[1];
+        rw[(rr + 8) * 8 + cc] = acc[2];
+        rw[(rr + 8) * 8 + cc + 1] = acc[3];
+    }
+    __syncthreads();
+    if (threadIdx.x < 128) {
+        const int r = threadIdx.x >> 3, c = threadIdx.x & 7, e = e0 + c;
+        if (r < ntok && e < P.E) {
+            float z = 0.f;
 #pragma unroll
-        for (int i = 0; i < kRouterTok; ++i) {
-            const float z = warp_sum(acc[i]);
-            if (lane == 0 && i < ntok)
-                P.logits[(size_t)(tg * kRouterTok + i) * P.E + e] = z + b;
+            for (int w = 0; w < kRouterWarps; ++w) z += red[w * 128 + r * 8 + c];
+            P.logits[(size_t)(tg * kRouterTok + r) * P.E + e] = z + (P.bias ? P.bias[e] : 0.f);
         }
     }
 
-    // (3) last CTA of the token group: top-k + softmax over the selection
-    __threadfence();
+    // (3) the last CTA of the token group: top-k + softmax over the selection
     __syncthreads();
     if (threadIdx.x == 0) {
+        __threadfence();  // release the CTA's logits (ordered before by the barrier)
         const uint32_t prev = atomicAdd(&P.cnt[tg], 1u);
         sh_last = (prev == gridDim.y - 1) ? 1 : 0;
-        if (sh_last) P.cnt[tg] = 0;
+        if (sh_last) {
+            P.cnt[tg] = 0;
+            __threadfence();  // acquire the other CTAs' logits for the whole CTA (barrier below)
+        }
     }
     __syncthreads();
     if (sh_last && warp < ntok) {
-        __threadfence();
         const int tl = tg * kRouterTok + warp;
         const float* z = P.logits + (size_t)tl * P.E;
-        constexpr int kMaxPer = 32;  // E <= 1024
-        float zv[kMaxPer];
-        const int per = (P.E + 31) / 32;
-#pragma unroll
-        for (int i = 0; i < kMaxPer; ++i) {
-            const int ee = i * 32 + lane;
-            float v = (i < per && ee < P.E) ? __ldcg(z + ee) : -INFINITY;
-            zv[i] = isnan(v) ? -INFINITY : v;  // a NaN logit ranks below every number
+        float* zs = reinterpret_cast<float*>(smem_raw) + (size_t)warp * P.E;  // u is done
+        for (int ee = lane; ee < P.E; ee += 32) {
+            const float v = __ldcg(z + ee);
+            zs[ee] = isnan(v) ? -INFINITY : v;
         }
-        uint32_t taken = 0;
+        __syncwarp();
+        const int per = (P.E + 31) / 32;
+        uint32_t taken = 0;  // bit i: candidate i * 32 + lane was selected
         float selz[8];
         int seli[8];
-        for (int j = 0; j < P.k; ++j) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
 #pragma unroll
-            for (int i = 0; i < kMaxPer; ++i) {
-                const int ee = i * 32 + lane;
-                if (i < per && ee < P.E && !(taken & (1u << i)) &&
-                    (zv[i] > bv || (zv[i] == bv && ee < bi) || bi == 0x7fffffff)) {
-                    bv = zv[i];
-                    bi = ee;
+        for (int j = 0; j < 8; ++j) {
+            selz[j] = -INFINITY;
+            seli[j] = 0;
+            if (j < P.k) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+                for (int i = 0; i < per; ++i) {
+                    const int ee = i * 32 + lane;
+                    if (ee < P.E && !(taken & (1u << i))) {
+                        const float v = zs[ee];
+                        if (v > bv || (v == bv && ee < bi)) {
+                            bv = v;
+                            bi = ee;
+                        }
+                    }
                 }
-            }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                    if (ov > bv || (ov == bv && oi < bi)) {
+                        bv = ov;
+                        bi = oi;
+                    }
                 }
+                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+                selz[j] = bv;
+                seli[j] = bi;
             }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            selz[j] = bv;
-            seli[j] = bi;
         }
-        if (lane == 0) {
-            float den = 0.f, ex[8];
-            for (int j = 0; j < P.k; ++j) {
-                ex[j] = expf(selz[j] - selz[0]);
-                den += ex[j];
+        // lane j < k writes pick j: w_j = exp(z_j - z_0) / sum_i exp(z_i - z_0)
+        float den = 0.f, mine = 0.f;
+        int idx = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < P.k) {
+                const float ex = expf(selz[j] - selz[0]);
+                den += ex;
+                if (lane == j) {
+                    mine = ex;
+                    idx = seli[j];
+                }
             }
-            const int row = P.row0 + tl;
-            for (int j = 0; j < P.k; ++j) {
-                const float wj = ex[j] / den;
-                P.idx[tl * P.k + j] = seli[j];
-                P.wts[tl * P.k + j] = wj;
-                if (P.user_idx) P.user_idx[(size_t)row * P.k + j] = seli[j];
-                if (P.user_w) P.user_w[(size_t)row * P.k + j] = wj;
-            }
+        }
+        if (lane < P.k) {
+            const float wj = mine / den;
+            const int row_g = P.row0 + tl;
+            P.idx[tl * P.k + lane] = idx;
+            P.wts[tl * P.k + lane] = wj;
+            if (P.user_idx) P.user_idx[(size_t)row_g * P.k + lane] = idx;
+            if (P.user_w) P.user_w[(size_t)row_g * P.k + lane] = wj;
         }
     }
     task_end(ctx);
@@ -383,8 +465,8 @@ int enqueue_rmsnorm(Launcher& L, const NormProblem& p, const KCtx& c) {
 int enqueue_router(Launcher& L, const RouterProblem& p, const KCtx& c) {
     void* args[] = {(void*)&p, (void*)&c};
     dim3 grid((p.nrows + kRouterTok - 1) / kRouterTok, (p.E + 7) / 8);
-    return L.launch((const void*)router_kernel, grid, dim3(256),
-                    (size_t)kRouterTok * p.H * sizeof(bf16), args);
+    return L.launch((const void*)router_kernel, grid, dim3(kRouterWarps * 32),
+                    router_smem_bytes(p.H, p.E), args);
 }
 
 int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c) {
@@ -467,14 +549,14 @@ extern "C" int sgp_router_topk_noalloc(const sgp_dims* d, const void* h, const v
     memset(&c, 0, sizeof(c));
     c.status = status;
     c.timeout_ns = 2000000000ull;
-    const size_t smem = (size_t)kRouterTok * d->hidden * sizeof(bf16);
+    const size_t smem = router_smem_bytes(d->hidden, d->n_experts);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute((const void*)router_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return SGP_ERR_CUDA;
     void* args[] = {(void*)&p, (void*)&c};
     dim3 grid(groups, (d->n_experts + 7) / 8);
-    if (cudaLaunchKernel((const void*)router_kernel, grid, dim3(256), args, smem, s) !=
+    if (cudaLaunchKernel((const void*)router_kernel, grid, dim3(kRouterWarps * 32), args, smem, s) !=
         cudaSuccess)
         return SGP_ERR_CUDA;
     return SGP_OK;

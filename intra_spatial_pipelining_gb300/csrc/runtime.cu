@@ -112,14 +112,21 @@ int ensure_smem_attr(const void* func, size_t smem) {
     static std::unordered_set<const void*> done;
     std::lock_guard<std::mutex> lk(mu);
     if (done.count(func)) return 0;
-    const int max_smem = 227 * 1024;
-    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    // the opt-in limit covers static + dynamic shared memory of a block
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return (int)e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) return (int)e;
+    const int max_smem = optin - (int)fa.sharedSizeBytes;
+    if ((size_t)max_smem < smem) return (int)cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return (int)e;
     Driver& d = drv();
     if (d.core) {
         cudaKernel_t k;
-        int dev = 0;
-        cudaGetDevice(&dev);
         if (cudaGetKernel(&k, func) == cudaSuccess)
             d.kernelSetAttribute(CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, max_smem,
                                  (CUkernel)k, (CUdevice)dev);
