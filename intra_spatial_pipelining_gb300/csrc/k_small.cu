@@ -409,6 +409,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, co
     griddep_launch();
     griddep_wait();
     task_begin(ctx);
+    constexpr int kKeep = 8;  // 4-element vectors per thread kept for the fused RMSNorm
+    __shared__ float red[8];
     const int tl = blockIdx.x;
     const int row = P.row0 + tl;
     const int n4 = P.H >> 2;
@@ -425,7 +427,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, co
     }
     const uint2* h = reinterpret_cast<const uint2*>(P.h + (size_t)row * P.H);
     uint2* out = reinterpret_cast<uint2*>(P.out + (size_t)row * P.H);
-    for (int v = threadIdx.x; v < n4; v += 256) {
+    uint2 keep[kKeep];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) keep[i] = make_uint2(0, 0);
+    int i = 0;
+    for (int v = threadIdx.x; v < n4; v += 256, ++i) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < P.k; ++j) {
             const float4 y = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
@@ -441,6 +448,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, co
         o.x = pack_bf16x2(h01.x + acc[0], h01.y + acc[1]);
         o.y = pack_bf16x2(h23.x + acc[2], h23.y + acc[3]);
         out[v] = o;
+        if (P.a_next != nullptr) {
+            // the next layer normalises the stored (bf16) residual
+            const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.x));
+            const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.y));
+            ss = fmaf(x01.x, x01.x, ss);
+            ss = fmaf(x01.y, x01.y, ss);
+            ss = fmaf(x23.x, x23.x, ss);
+            ss = fmaf(x23.y, x23.y, ss);
+#pragma unroll
+            for (int q = 0; q < kKeep; ++q)
+                if (q == i) keep[q] = o;
+        }
+    }
+    if (P.a_next != nullptr) {
+        ss = warp_sum(ss);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int wq = 0; wq < 8; ++wq) tot += red[wq];
+        const float inv = rsqrtf(tot / (float)P.H + P.eps);
+        const uint2* g = reinterpret_cast<const uint2*>(P.g_next);
+        uint2* a = reinterpret_cast<uint2*>(P.a_next + (size_t)row * P.H);
+#pragma unroll
+        for (int q = 0; q < kKeep; ++q) {
+            const int v = threadIdx.x + q * 256;
+            if (v < n4) {
+                const uint2 gv = g[v];
+                const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&keep[q].x));
+                const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&keep[q].y));
+                const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv.x));
+                const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv.y));
+                uint2 r;
+                r.x = pack_bf16x2(x01.x * inv * g01.x, x01.y * inv * g01.y);
+                r.y = pack_bf16x2(x23.x * inv * g23.x, x23.y * inv * g23.y);
+                a[v] = r;
+            }
+        }
     }
     task_end(ctx);
 }

@@ -449,7 +449,14 @@ struct RunEnv {
     bool tc_dense, tc_expert;
     int serpentine;
     int pool_sms;       // SMs of the pool the kernels run on (persistent grid size)
+    // RMSNorm-1 of the next layer fused into this layer's combine (NULL: not fused), and
+    // whether this layer's own RMSNorm-1 was produced by the previous layer's combine
+    const sgp_layer* next = nullptr;
+    bool norm_fused = false;
 };
+
+// The combine can produce the next layer's RMSNorm-1 while it holds the row (H <= 8192).
+bool can_fuse_norm(const sgp_dims& d) { return d.hidden <= 8192; }
 
 int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     const sgp_dims& d = *e.d;
@@ -605,6 +612,7 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     int r = 0;
     switch (op) {
         case SGP_OP_RMSNORM_ATTN: {
+            if (e.norm_fused) return 0;  // written by the previous layer's combine
             NormProblem p{e.x_cur, (const bf16*)e.layer->g_attn, e.ws.at<bf16>(Lay.a), row0, b,
                           d.hidden, d.rms_eps};
             return enqueue_rmsnorm(L, p, c);
@@ -674,7 +682,9 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
         case SGP_OP_COMBINE: {
             CombineProblem p{e.ws.at<bf16>(Lay.h), e.ws.mu<float>(mu, Lay.ybuf),
                              e.ws.mu<float>(mu, Lay.wts), e.ws.mu<int>(mu, Lay.pair_pos),
-                             e.x_out, row0, b, d.top_k, d.hidden};
+                             e.x_out, row0, b, d.top_k, d.hidden,
+                             e.next ? (const bf16*)e.next->g_attn : nullptr,
+                             e.next ? e.ws.at<bf16>(Lay.a) : nullptr, d.rms_eps};
             return enqueue_combine(L, p, c);
         }
         default:
@@ -715,10 +725,12 @@ constexpr uint64_t kDefaultTimeout = 2000000000ull;
 
 int run_layer_stream(const sgp_dims& d, const sgp_layer* layer, int li, const int32_t* kv_len,
                      const bf16* x_cur, bf16* x_out, int T, int32_t* tki, float* tkw, Ws ws,
-                     cudaStream_t s) {
+                     cudaStream_t s, const sgp_layer* next, bool norm_fused) {
     StreamLauncher L(s);
     RunEnv e{&d, layer, kv_len, x_cur, x_out, T, ws, tki, tkw, use_tc_dense(d, T),
              use_tc_expert(d, T), 0, device_sms()};
+    e.next = next;
+    e.norm_fused = norm_fused;
     for (int op = 0; op < SGP_N_OPS; ++op) {
         KCtx c = plain_ctx(ws.status(), kDefaultTimeout, ((uint32_t)op << 24) | ((uint32_t)li << 12));
         int r = enqueue_op(L, e, op, 0, c);
@@ -810,8 +822,10 @@ static int temporal_common(const sgp_dims* d, const sgp_layer* layers, int n_lay
         const bf16* xc = (const bf16*)(l == 0 ? x_in : x_out);
         int32_t* ti = tki ? tki + (size_t)l * T * d->top_k : nullptr;
         float* tw = tkw ? tkw + (size_t)l * T * d->top_k : nullptr;
-        if ((r = run_layer_stream(*d, &layers[l], l, kv_len, xc, (bf16*)x_out, T, ti, tw, w, s)) !=
-            SGP_OK)
+        const bool fuse = can_fuse_norm(*d);
+        const sgp_layer* next = (fuse && l + 1 < n_layers) ? &layers[l + 1] : nullptr;
+        if ((r = run_layer_stream(*d, &layers[l], l, kv_len, xc, (bf16*)x_out, T, ti, tw, w, s,
+                                  next, fuse && l > 0)) != SGP_OK)
             return r;
     }
     if (dump) {
@@ -1015,6 +1029,17 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
     }
     std::vector<CUgraphNode> last(tasks.size(), nullptr);
     const bool tcd = use_tc_dense(d, T), tce = use_tc_expert(d, T);
+    // Layer l's RMSNorm-1 comes from layer l-1's combine unless it is the last op of its task
+    // (the task's last kernel publishes the stage handoff flag, so it must be launched).
+    int n_layers = 0;
+    for (const PTask& t : tasks) n_layers = std::max(n_layers, t.l1 + 1);
+    std::vector<char> fused(n_layers + 1, 0);
+    if (can_fuse_norm(d))
+        for (int l = 1; l < n_layers; ++l) {
+            fused[l] = 1;
+            for (const PTask& t : tasks)
+                if (t.mu == 0 && t.l1 == l && t.op1 == 0) fused[l] = 0;
+        }
     const uint64_t timeout = p->opts.wait_timeout_ns ? p->opts.wait_timeout_ns : kDefaultTimeout;
     uint32_t* flags = w.at<uint32_t>(p->lay.flags);
     uint32_t* fcnt = w.at<uint32_t>(p->lay.flag_cnt);
@@ -1048,6 +1073,15 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
                      tkw ? tkw + (size_t)l * T * d.top_k : nullptr, tcd, tce,
                      p->opts.serpentine_experts,
                      p->sctx[t.stage] ? p->split[t.stage] : device_sms()};
+            e.next = fused[l + 1] ? &layers[l + 1] : nullptr;
+            e.norm_fused = fused[l] != 0;
+            if (op == SGP_OP_RMSNORM_ATTN && e.norm_fused) {  // nothing to launch
+                if (++op == SGP_N_OPS) {
+                    op = 0;
+                    ++l;
+                }
+                continue;
+            }
             int r = enqueue_op(L, e, op, t.mu, c);
             if (r != 0) {
                 cudaGraphDestroy(g);

@@ -90,6 +90,44 @@ def make_inputs_with_margin(wl: synth.Workload, seed: int, max_attempts: int = 2
     raise RuntimeError("no router draw with the required margin")
 
 
+def make_stack_inputs_with_margin(wl: synth.Workload, seed: int, tokens=None,
+                                  max_attempts: int = 30):
+    """Multi-layer workloads: redraw the router weights of the first layer whose oracle
+    top-k margin (over ``tokens``) is below MARGIN, until every layer keeps the margin.
+    Returns (inputs, oracle result of the stack for ``tokens``)."""
+    attempts = [0] * wl.n_layers
+    for _ in range(max_attempts):
+        inp = make_inputs(wl, seed, attempts)
+        ref = oracle_stack(inp, tokens)
+        bad = [l for l in range(wl.n_layers)
+               if min(O.topk_margin(z, wl.shape.top_k) for z in ref["logits"][l]) < MARGIN]
+        if not bad:
+            return inp, ref
+        attempts[bad[0]] += 1
+    raise RuntimeError("no router draws with the required margin")
+
+
+def oracle_stack_rows(inp: Inputs, seqs) -> dict:
+    """fp64 oracle of the whole stack for the sequences ``seqs`` only (every result of a
+    sequence depends on that sequence alone).  The layer weights and those sequences' KV rows
+    are copied from the generator's tensors one layer at a time, so the full-size stack never
+    has to be held on the host."""
+    wl = inp.wl
+    x = O.f64(inp.x.cpu())[seqs]
+    kvl = inp.kv_len.cpu().numpy()[seqs]
+    idxs, ws, zs = [], [], []
+    for l in range(wl.n_layers):
+        w = {n: (v.cpu() if v is not None else None) for n, v in inp.weights[l].items()}
+        k, v = inp.caches[l]
+        kc, vc = O.f64(k[seqs].cpu()), O.f64(v[seqs].cpu())
+        r = O.layer(wl.shape, w, x, kvl, kc, vc, wl.layer_window(l))
+        x = r["x_next"]
+        idxs.append(r["idx"])
+        ws.append(r["w"])
+        zs.append(r["logits"])
+    return {"x_out": x, "idx": np.array(idxs), "w": np.array(ws), "logits": np.array(zs)}
+
+
 def rel_err(gpu, ref) -> float:
     g = gpu.detach().to("cpu", torch.float64).numpy() if hasattr(gpu, "detach") else np.asarray(gpu)
     r = np.asarray(ref, dtype=np.float64).reshape(g.shape)
