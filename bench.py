@@ -305,10 +305,12 @@ def run_sgp(args, rank, world, local_rank):
     n_stages = args.stages
     micro = args.micro or (T // max(1, wl.microbatches))
     opts = None
+    opts_kw = {}
     if args.cut == "macro":
         full = [1] * sgp.N_OPS
         full[sgp.OPS.index("attention")] = 0
-        opts = sgp.make_opts(stage_of_op=[full, [1] * sgp.N_OPS])
+        opts_kw = {"stage_of_op": [full, [1] * sgp.N_OPS]}
+        opts = sgp.make_opts(**opts_kw)
     balance_rows = None
     if n_stages == 1:
         split = [N]
@@ -406,7 +408,7 @@ def run_sgp(args, rank, world, local_rank):
                "h2d_bytes_per_step": hx.numel() * hx.element_size(),
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                "ms_per_step": ms_e2e}
-    n_tasks = len(sgp.sgp_pipeline_tasks(pipe))
+    n_launch = launches_per_run(make, n_stages, split, micro, opts_kw, layers, kv_len, x, out, T)
     sgp.sgp_pipeline_destroy(pipe)
 
     # ---- roofline of the dominant kernel (full-attention decode), timed alone ----
@@ -468,18 +470,25 @@ def run_sgp(args, rank, world, local_rank):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * n_tasks_kernels(wl, T // micro),
+        "gpu_launches": args.steps * n_launch,
         "clocks": clk,
         "algorithmic_bytes_per_step": total_bytes,
     }
     print(json.dumps(line), flush=True)
 
 
-def n_tasks_kernels(wl, m):
-    """Kernels one iteration launches: 9 ops per layer and microbatch, plus the finishing
-    kernel of each of the 4 projections that run on tensor cores."""
+def launches_per_run(make, n_stages, split, micro, opts_kw, layers, kv_len, x, out, T):
+    """Kernels one pipelined run launches, counted from the device launch trace of a run of
+    the same configuration (every kernel records its start; fused ops record nothing)."""
     from intra_spatial_pipelining_gb300 import sgp
-    return wl.n_layers * (sgp.N_OPS + 4) * m
+    p = make(n_stages, split, micro, sgp.make_opts(trace=1, **opts_kw))
+    try:
+        sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
+        sgp.check(sgp.sgp_pipeline_sync(p), "traced run")
+        tr = sgp.sgp_pipeline_trace(p)
+    finally:
+        sgp.sgp_pipeline_destroy(p)
+    return int((tr[:, 1] > 0).sum())
 
 
 def main():

@@ -256,6 +256,11 @@ typedef struct sgp_pipeline_opts {
                                    dependent launch); 0 = default (off); results identical  */
     int trace;                  /* 1: every kernel records its first-CTA start and last-CTA
                                    end (%globaltimer ns); read with sgp_pipeline_trace      */
+    int weight_reuse;           /* 1: projection weights read by a microbatch that is not the
+                                   last are loaded with an L2 evict-last hint (the next
+                                   microbatch rereads them), the last microbatch's with
+                                   evict-first; 0 = default (off: every weight load is
+                                   evict-first; the hint measured no faster here)           */
 } sgp_pipeline_opts;
 
 /* Creates a pipeline for up to max_tokens sequences with KV length <= max_kv_len.

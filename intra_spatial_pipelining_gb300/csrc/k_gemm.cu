@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_w = P.keep_weights ? policy_evict_last() : policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             uint32_t it = 0;
             uint32_t issued_mask = 0, issued_par = 0;

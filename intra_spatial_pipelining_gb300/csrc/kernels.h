@@ -70,6 +70,8 @@ struct GemmProblem {
     int stages;             // shared-memory pipeline depth
     int ring_bytes;         // bytes of the stage ring (also holds the staged accumulator)
     int serpentine;         // visit groups in reverse order
+    int keep_weights;       // 1: weight loads hint L2 evict-last (a later microbatch rereads
+                            //    them), 0: evict-first
     float* partial;         // [m_tiles][ksplit][R][128] fp32 tiles (token-major rows)
     int n_units;            // n_groups * m_tiles * ksplit
     int grid;               // persistent CTAs (one per SM of the pool)
@@ -151,6 +153,10 @@ struct CombineProblem {
     const bf16* g_next;     // or NULL
     bf16* a_next;           // [T][H] batch-wide
     float eps;
+    // optional: y is read as the expert-down GEMM's K-segment partials and summed here in
+    // segment order, [H/128][ksplit][Rp][128] fp32 (NULL: read Y)
+    const float* Ypart;
+    int ksplit, Rp;
 };
 
 // --------------------------------------------------------------------------------------

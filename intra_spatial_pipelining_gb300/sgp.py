@@ -59,7 +59,8 @@ class sgp_pipeline_opts(C.Structure):
                 ("use_green_contexts", C.c_int), ("green_ctx_flags", C.c_int),
                 ("serpentine_experts", C.c_int), ("wait_timeout_ns", C.c_uint64),
                 ("fault_inject", C.c_uint32), ("fault_task", C.c_int),
-                ("programmatic_launch", C.c_int), ("trace", C.c_int)]
+                ("programmatic_launch", C.c_int), ("trace", C.c_int),
+                ("weight_reuse", C.c_int)]
 
 
 _lib = None
@@ -176,7 +177,7 @@ def layer_array(layers: Sequence[sgp_layer]):
 def make_opts(stage_of_op=None, use_green_contexts: int = 0, green_ctx_flags: int = 0,
               serpentine_experts: int = 0, wait_timeout_ns: int = 0, fault_inject: int = 0,
               fault_task: int = 0, programmatic_launch: int = 0,
-              trace: int = 0) -> sgp_pipeline_opts:
+              trace: int = 0, weight_reuse: int = 0) -> sgp_pipeline_opts:
     o = sgp_pipeline_opts()
     if stage_of_op is not None:
         o.custom_cut = 1
@@ -191,6 +192,7 @@ def make_opts(stage_of_op=None, use_green_contexts: int = 0, green_ctx_flags: in
     o.fault_task = fault_task
     o.programmatic_launch = programmatic_launch
     o.trace = trace
+    o.weight_reuse = weight_reuse
     return o
 
 
