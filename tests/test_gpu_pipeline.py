@@ -108,21 +108,17 @@ def test_stack_three_layers_vs_oracle():
     assert torch.equal(got[0], out_t)
 
 
-def test_full_size_stack_sampled_sequences_vs_oracle():
-    """The configuration the benchmark times -- 36 layers, KV 8192, 64 sequences, two-stage
-    pipeline with 2 microbatches -- checked layer by layer on sequences sampled from both
-    microbatches.  Layer l of the oracle starts from the GPU's own input to layer l (the
-    output of the first l layers, from the temporal stack, which the pipelined output of all
-    36 layers must equal bit for bit): bf16 rounding makes two 36-layer chains drift apart
-    by itself, so comparing chained outputs would test the drift, not the layer.  Routing
-    is compared where the oracle's top-k margin is at least MARGIN; elsewhere the GPU's
-    picks must be valid top-k picks of the oracle's logits within twice the margin."""
-    wl = synth.WORKLOADS["gptoss_36l"]
-    seed, L, k, T = 13, wl.n_layers, wl.shape.top_k, wl.n_tokens
-    inp = H.make_inputs(wl, seed)
-    seqs = [5, 40]
+def _teacher_forced_check(inp, seqs, n_stages=2, micro=None, min_checked=0.9):
+    """Runs the stack as a pipeline, then layer by layer as temporal stacks of the first l+1
+    layers; checks, for the sequences ``seqs``, every layer's output and routing against the
+    oracle started from the GPU's own input to that layer, and that the pipelined output and
+    routing equal the temporal ones bit for bit.  Routing is compared where the oracle's
+    top-k margin is at least MARGIN; elsewhere the GPU's picks must be valid top-k picks of
+    the oracle's logits within twice the margin.  Returns the number of checked pairs."""
+    wl = inp.wl
+    L, k, T = wl.n_layers, wl.shape.top_k, wl.n_tokens
     d = H.dims(wl.shape)
-    out_p, tki_p, _, _ = _pipelined(inp, d, 2, T // 2, reps=1)
+    out_p, tki_p, _, _ = _pipelined(inp, d, n_stages, micro or T // 2, reps=1)
     ws = H.workspace(d, T, wl.cap)
     layers = inp.sgp_layers()
     x_l = inp.x.clone()
@@ -150,7 +146,48 @@ def test_full_size_stack_sampled_sequences_vs_oracle():
                 assert all(z[e] >= kth - 2 * H.MARGIN for e in gi[i]), (l, seqs[i])
         x_l = out
     assert torch.equal(x_l, out_p), "temporal stack and pipeline outputs differ"
-    assert checked >= 0.9 * L * len(seqs)
+    assert checked >= min_checked * L * len(seqs)
+    return checked
+
+
+def test_full_size_stack_sampled_sequences_vs_oracle():
+    """The configuration the benchmark times -- 36 layers, KV 8192, 64 sequences, two-stage
+    pipeline with 2 microbatches -- checked layer by layer on sequences sampled from both
+    microbatches.  Layer l of the oracle starts from the GPU's own input to layer l (the
+    output of the first l layers, from the temporal stack, which the pipelined output of all
+    36 layers must equal bit for bit): bf16 rounding makes two 36-layer chains drift apart
+    by itself, so comparing chained outputs would test the drift, not the layer."""
+    wl = synth.WORKLOADS["gptoss_36l"]
+    _teacher_forced_check(H.make_inputs(wl, 13), [5, 40])
+
+
+@pytest.mark.parametrize("n_tokens", [8, 16, 32, 64, 128, 256])
+def test_batch_length_sweep(n_tokens):
+    """Batch/length sweep shapes: ragged KV lengths uniform in [512, 16384], one sliding and
+    one full layer; 8 sequences take the CUDA-core GEMV path, 16 and more the tcgen05 path."""
+    wl = synth.sweep_workload(n_tokens, n_layers=2)
+    inp = H.make_inputs(wl, 14)
+    seqs = sorted({0, n_tokens // 2, n_tokens - 1})
+    _teacher_forced_check(inp, seqs, micro=max(1, n_tokens // 2), min_checked=0.5)
+
+
+def test_skewed_routing_block_slots():
+    """Zipf(1.2)-shaped router bias with the block slot map: local slots get very different
+    row counts; every sequence of a 2-layer stack against the oracle, pipelined == temporal."""
+    wl = synth.skew_workload(n_layers=2).with_(kv_len=1024)
+    inp, ref = H.make_stack_inputs_with_margin(wl, 15)
+    d = H.dims(wl.shape)
+    k = wl.shape.top_k
+    out_t, tki, _, _ = _temporal(inp, d)
+    H.assert_close("x_out (temporal)", out_t, ref["x_out"])
+    assert _routing_sets_per_layer(tki, 2, k) == [H.routing_sets(ref["idx"][l]) for l in range(2)]
+    slots = np.array([[O.slot_of(int(e), wl.shape.n_experts, wl.shape.n_local_experts,
+                                 wl.shape.slot_map) for e in row] for row in ref["idx"][0]])
+    counts = np.bincount(slots.ravel(), minlength=wl.shape.n_local_experts)
+    print("rows per slot", counts.tolist())
+    assert counts.max() >= 4 * max(1, counts.min())   # the skew is real
+    got = _pipelined(inp, d, 2, wl.n_tokens // 2)
+    assert torch.equal(got[0], out_t)
 
 
 def test_task_dag_matches_schedule_model():
