@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--stages", type=int, default=2)
     ap.add_argument("--micro", type=int, default=None, help="sequences per microbatch")
     ap.add_argument("--split", default="auto", help="'auto' (balancer) or comma list of SMs")
-    ap.add_argument("--cut", default="layer", choices=["layer", "macro"])
+    ap.add_argument("--cut", default="macro", choices=["layer", "macro"],
+                    help="macro: full-attention decode alone on stage A, everything else on B")
     ap.add_argument("--no-temporal", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -251,9 +251,12 @@ typedef struct sgp_pipeline_opts {
                                    task; bit 1 = drop one TMA load of the first projection
                                    (its bounded wait then runs out)                          */
     int fault_task;             /* task index for fault bit 0                                */
-    int programmatic_launch;    /* 1: consecutive kernels of one task overlap launch and
-                                   prologue with the previous kernel's tail (programmatic
-                                   dependent launch); 0 = default (off); results identical  */
+    int programmatic_launch;    /* programmatic dependent launch between consecutive kernels
+                                   of a task (a kernel's launch and prologue overlap the
+                                   previous kernel's tail; results are identical):
+                                   0 = default: only into the projection kernels and their
+                                   finishing passes (the weight stream starts early);
+                                   1 = into every kernel; -1 = off                            */
     int trace;                  /* 1: every kernel records its first-CTA start and last-CTA
                                    end (%globaltimer ns); read with sgp_pipeline_trace      */
     int weight_reuse;           /* 1: projection weights read by a microbatch that is not the

@@ -521,7 +521,7 @@ int enqueue_gemm_tc(Launcher& L, const GemmProblem& p, const KCtx& c) {
         return (int)cudaErrorInvalidValue;
     void* args[] = {(void*)&p, (void*)&c};
     return L.launch((const void*)gemm_tc_kernel, grid, block,
-                    gemm_tc_smem_bytes(p.n_cap, p.stages), args);
+                    gemm_tc_smem_bytes(p.n_cap, p.stages), args, true);
 }
 
 int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c) {
@@ -530,7 +530,7 @@ int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c) {
     const int blocks = (int)std::min<long>((total + 255) / 256, 4096);
     void* args[] = {(void*)&p, (void*)&c};
     return L.launch((const void*)gemm_finish_kernel, dim3(std::max(1, blocks)), dim3(256), 0,
-                    args);
+                    args, true);
 }
 
 int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c) {

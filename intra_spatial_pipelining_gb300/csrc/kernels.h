@@ -17,7 +17,10 @@ namespace sgp {
 // convention); the launcher copies the values before returning.  Returns a cudaError_t.
 struct Launcher {
     virtual ~Launcher() {}
-    virtual int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) = 0;
+    // overlap_ok: the kernel may be launched programmatically after its predecessor (it only
+    // touches memory the predecessor writes after griddep_wait)
+    virtual int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args,
+                       bool overlap_ok = false) = 0;
 };
 
 // --------------------------------------------------------------------------------------

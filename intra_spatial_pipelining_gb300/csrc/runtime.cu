@@ -141,12 +141,15 @@ int ensure_smem_attr(const void* func, size_t smem) {
 // Every kernel of this library starts with griddepcontrol.launch_dependents and calls
 // griddepcontrol.wait before it touches memory a predecessor wrote (or may still read), so
 // consecutive launches may overlap their launch latency and prologue with the tail of the
-// previous kernel (programmatic dependent launch).
+// previous kernel (programmatic dependent launch).  Only launches that declare overlap_ok
+// (the projection kernels and their finishing passes) use it by default: measured on the
+// 36-layer slice, overlapping every kernel is slower than overlapping none.
 struct StreamLauncher : Launcher {
     cudaStream_t s;
     bool pdl;
-    explicit StreamLauncher(cudaStream_t st, bool programmatic = false) : s(st), pdl(programmatic) {}
-    int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) override {
+    explicit StreamLauncher(cudaStream_t st, bool programmatic = true) : s(st), pdl(programmatic) {}
+    int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args,
+               bool overlap_ok = false) override {
         int e = ensure_smem_attr(func, smem);
         if (e) return e;
         cudaLaunchConfig_t cfg;
@@ -159,7 +162,7 @@ struct StreamLauncher : Launcher {
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = pdl ? 1 : 0;
+        cfg.numAttrs = (pdl && overlap_ok) ? 1 : 0;
         return (int)cudaLaunchKernelExC(&cfg, func, args);
     }
 };
@@ -171,11 +174,12 @@ struct GraphLauncher : Launcher {
     CUgraph g;
     CUcontext ctx;
     std::vector<CUgraphNode> deps;
-    bool pdl = false;
+    int pdl = 0;  // 0: off, 1: every chained kernel, 2: kernels that declare overlap_ok
     bool chained = false;  // deps holds exactly the previous kernel of this chain
-    GraphLauncher(CUgraph graph, CUcontext c, bool programmatic = false)
+    GraphLauncher(CUgraph graph, CUcontext c, int programmatic = 0)
         : g(graph), ctx(c), pdl(programmatic) {}
-    int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args) override {
+    int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args,
+               bool overlap_ok = false) override {
         int e = ensure_smem_attr(func, smem);
         if (e) return e;
         cudaKernel_t k;
@@ -200,7 +204,7 @@ struct GraphLauncher : Launcher {
         memset(&ed, 0, sizeof(ed));
         ed.from_port = CU_GRAPH_KERNEL_NODE_PORT_PROGRAMMATIC;
         ed.type = CU_GRAPH_DEPENDENCY_TYPE_PROGRAMMATIC;
-        const bool prog = pdl && chained && deps.size() == 1;
+        const bool prog = (pdl == 1 || (pdl == 2 && overlap_ok)) && chained && deps.size() == 1;
         CUresult r = drv().graphAddNode(&n, g, deps.empty() ? nullptr : deps.data(),
                                         prog ? &ed : nullptr, deps.size(), &np);
         if (r != CUDA_SUCCESS) {
@@ -1061,7 +1065,8 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
     for (size_t i = 0; i < tasks.size(); ++i) {
         const PTask& t = tasks[i];
         if (stage_only >= 0 && t.stage != stage_only) continue;
-        GraphLauncher L((CUgraph)g, p->sctx[t.stage], p->opts.programmatic_launch > 0);
+        GraphLauncher L((CUgraph)g, p->sctx[t.stage],
+                        p->opts.programmatic_launch < 0 ? 0 : (p->opts.programmatic_launch == 1 ? 1 : 2));
         const bool keep_data = stage_only < 0;
         if (keep_data && t.pred_data >= 0) L.deps.push_back(last[t.pred_data]);
         if (t.pred_stage >= 0 && last[t.pred_stage]) L.deps.push_back(last[t.pred_stage]);
