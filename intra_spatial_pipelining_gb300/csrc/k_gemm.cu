@@ -310,17 +310,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // K-segment reduction + fused epilogue: one thread = 4 consecutive outputs of one token.  The
 // K-segment loads are issued before they are summed (in segment order).
 // ---------------------------------------------------------------------------------------
-constexpr int kFinUnroll = 8;
-
+// U loads in flight per thread and sum; the kernel is instantiated for U = 4 and 8 so that a
+// small K split does not pay the registers (and the occupancy) of a large one.
+template <int U>
 __device__ __forceinline__ float4 sum_segments(const float* p, size_t sstride, int ks) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < ks; s0 += kFinUnroll) {
-        float4 v[kFinUnroll];
+    for (int s0 = 0; s0 < ks; s0 += U) {
+        float4 v[U];
 #pragma unroll
-        for (int i = 0; i < kFinUnroll; ++i)
+        for (int i = 0; i < U; ++i)
             if (s0 + i < ks) v[i] = __ldcg(reinterpret_cast<const float4*>(p + (s0 + i) * sstride));
 #pragma unroll
-        for (int i = 0; i < kFinUnroll; ++i)
+        for (int i = 0; i < U; ++i)
             if (s0 + i < ks) {
                 acc.x += v[i].x;
                 acc.y += v[i].y;
@@ -331,12 +332,15 @@ __device__ __forceinline__ float4 sum_segments(const float* p, size_t sstride, i
     return acc;
 }
 
-__global__ void __launch_bounds__(256) gemm_finish_kernel(const FinishProblem P, const KCtx ctx) {
+// Instantiated per epilogue (MODE) so that each variant keeps only its own registers.
+template <int U, int MODE>
+__global__ void __launch_bounds__(256, U <= 4 ? 4 : 2)
+    gemm_finish_kernel(const FinishProblem P, const KCtx ctx) {
     griddep_launch();
     griddep_wait();
     task_begin(ctx);
     const EpiArgs& e = P.epi;
-    const bool swiglu = e.mode == EPI_SWIGLU;
+    constexpr bool swiglu = MODE == EPI_SWIGLU;
     const int per_tok = swiglu ? 16 : 32;         // 4-output groups per (tile, token)
     const int total = P.m_tiles * P.rows * per_tok;
     const size_t sstride = (size_t)P.R * 128;     // next K segment
@@ -346,11 +350,11 @@ __global__ void __launch_bounds__(256) gemm_finish_kernel(const FinishProblem P,
         const int mt = u / (per_tok * P.rows);
         const float* base = P.partial + ((size_t)mt * P.ksplit * P.R + lr) * 128;
         const int trow = P.out_row0 + lr;
-        if (swiglu) {
+        if constexpr (swiglu) {
             const int i0 = mt * 64 + 4 * q4;
             if (i0 >= e.n_out) continue;
-            const float4 g = sum_segments(base + 4 * q4, sstride, P.ksplit);
-            const float4 up = sum_segments(base + 64 + 4 * q4, sstride, P.ksplit);
+            const float4 g = sum_segments<U>(base + 4 * q4, sstride, P.ksplit);
+            const float4 up = sum_segments<U>(base + 64 + 4 * q4, sstride, P.ksplit);
             uint2 o;
             o.x = pack_bf16x2(silu_f(g.x) * up.x, silu_f(g.y) * up.y);
             o.y = pack_bf16x2(silu_f(g.z) * up.z, silu_f(g.w) * up.w);
@@ -359,12 +363,12 @@ __global__ void __launch_bounds__(256) gemm_finish_kernel(const FinishProblem P,
         }
         const int f0 = mt * 128 + 4 * q4;  // first of the 4 output features
         if (f0 >= e.n_out) continue;
-        float4 v = sum_segments(base + 4 * q4, sstride, P.ksplit);
-        if (e.mode == EPI_F32) {
+        float4 v = sum_segments<U>(base + 4 * q4, sstride, P.ksplit);
+        if constexpr (MODE == EPI_F32) {
             *reinterpret_cast<float4*>(e.out_f32 + (size_t)trow * e.ld + f0) = v;
             continue;
         }
-        if (e.mode == EPI_RESID) {
+        if constexpr (MODE == EPI_RESID) {
             const uint2 rr = *reinterpret_cast<const uint2*>(e.resid + (size_t)trow * e.ld + f0);
             const float2 r01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.x));
             const float2 r23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.y));
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__(256) gemm_finish_kernel(const FinishProblem P,
         o.x = pack_bf16x2(v.x, v.y);
         o.y = pack_bf16x2(v.z, v.w);
         bf16* dst;
-        if (e.mode == EPI_RESID) {
+        if constexpr (MODE == EPI_RESID) {
             dst = e.out + (size_t)trow * e.ld + f0;
         } else if (f0 < e.q_width) {  // EPI_QKV: query heads
             dst = e.q + (size_t)trow * e.q_width + f0;
@@ -529,8 +533,25 @@ int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c) {
     const long total = (long)p.m_tiles * p.rows * per_tok;
     const int blocks = (int)std::min<long>((total + 255) / 256, 4096);
     void* args[] = {(void*)&p, (void*)&c};
-    return L.launch((const void*)gemm_finish_kernel, dim3(std::max(1, blocks)), dim3(256), 0,
-                    args, true);
+    const bool small = p.ksplit <= 4;
+    const void* f = nullptr;
+    switch (p.epi.mode) {
+        case EPI_QKV:
+            f = small ? (const void*)gemm_finish_kernel<4, EPI_QKV> : (const void*)gemm_finish_kernel<8, EPI_QKV>;
+            break;
+        case EPI_RESID:
+            f = small ? (const void*)gemm_finish_kernel<4, EPI_RESID>
+                      : (const void*)gemm_finish_kernel<8, EPI_RESID>;
+            break;
+        case EPI_SWIGLU:
+            f = small ? (const void*)gemm_finish_kernel<4, EPI_SWIGLU>
+                      : (const void*)gemm_finish_kernel<8, EPI_SWIGLU>;
+            break;
+        default:
+            f = small ? (const void*)gemm_finish_kernel<4, EPI_F32> : (const void*)gemm_finish_kernel<8, EPI_F32>;
+            break;
+    }
+    return L.launch(f, dim3(std::max(1, blocks)), dim3(256), 0, args, true);
 }
 
 int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c) {

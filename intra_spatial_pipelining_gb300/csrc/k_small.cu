@@ -435,32 +435,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, co
     for (int v = threadIdx.x; v < n4; v += 256, ++i) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < P.k; ++j) {
-            float4 y;
-            if (P.Ypart != nullptr) {
-                // y = sum of the K segments in segment order (as a separate finishing pass)
-                const int f0 = 4 * v, mt = f0 >> 7;
-                const float* pp = P.Ypart + ((size_t)mt * P.ksplit * P.Rp + pos[j]) * 128 + (f0 & 127);
-                const size_t sstride = (size_t)P.Rp * 128;
-                y = make_float4(0.f, 0.f, 0.f, 0.f);
-                constexpr int kU = 8;
-                for (int s0 = 0; s0 < P.ksplit; s0 += kU) {
-                    float4 t[kU];
-#pragma unroll
-                    for (int q = 0; q < kU; ++q)
-                        if (s0 + q < P.ksplit)
-                            t[q] = __ldcg(reinterpret_cast<const float4*>(pp + (s0 + q) * sstride));
-#pragma unroll
-                    for (int q = 0; q < kU; ++q)
-                        if (s0 + q < P.ksplit) {
-                            y.x += t[q].x;
-                            y.y += t[q].y;
-                            y.z += t[q].z;
-                            y.w += t[q].w;
-                        }
-                }
-            } else {
-                y = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
-            }
+            const float4 y = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
             acc[0] = fmaf(w[j], y.x, acc[0]);
             acc[1] = fmaf(w[j], y.y, acc[1]);
             acc[2] = fmaf(w[j], y.z, acc[2]);

@@ -156,10 +156,6 @@ struct CombineProblem {
     const bf16* g_next;     // or NULL
     bf16* a_next;           // [T][H] batch-wide
     float eps;
-    // optional: y is read as the expert-down GEMM's K-segment partials and summed here in
-    // segment order, [H/128][ksplit][Rp][128] fp32 (NULL: read Y)
-    const float* Ypart;
-    int ksplit, Rp;
 };
 
 // --------------------------------------------------------------------------------------

@@ -457,9 +457,6 @@ struct RunEnv {
     // whether this layer's own RMSNorm-1 was produced by the previous layer's combine
     const sgp_layer* next = nullptr;
     bool norm_fused = false;
-    // the expert-down K segments are summed by the combine (no separate finishing pass);
-    // off when the caller asks for the routed rows y
-    bool down_in_combine = true;
     // weight loads of this microbatch keep the lines in L2 for the next microbatch
     bool keep_weights = false;
 };
@@ -602,7 +599,6 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     c2.wait_flag = nullptr;
     c2.fault = 0;
     if (c.trace) c2.trace = c.trace + 2;  // the finishing kernel has the op's second slot
-    if (op == SGP_OP_EXPERT_DOWN && e.down_in_combine) return enqueue_gemm_tc(L, p, c);
     if ((r = enqueue_gemm_tc(L, p, c1)) != 0) return r;
     FinishProblem f;
     memset(&f, 0, sizeof(f));
@@ -695,13 +691,7 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
                              e.ws.mu<float>(mu, Lay.wts), e.ws.mu<int>(mu, Lay.pair_pos),
                              e.x_out, row0, b, d.top_k, d.hidden,
                              e.next ? (const bf16*)e.next->g_attn : nullptr,
-                             e.next ? e.ws.at<bf16>(Lay.a) : nullptr, d.rms_eps,
-                             nullptr, 0, 0};
-            if (e.tc_expert && e.down_in_combine) {
-                p.Ypart = e.ws.mu<float>(mu, Lay.gemm_part);
-                p.ksplit = gemm_shape(d, SGP_OP_EXPERT_DOWN).ksplit;
-                p.Rp = b * d.top_k;
-            }
+                             e.next ? e.ws.at<bf16>(Lay.a) : nullptr, d.rms_eps};
             return enqueue_combine(L, p, c);
         }
         default:
@@ -742,14 +732,12 @@ constexpr uint64_t kDefaultTimeout = 2000000000ull;
 
 int run_layer_stream(const sgp_dims& d, const sgp_layer* layer, int li, const int32_t* kv_len,
                      const bf16* x_cur, bf16* x_out, int T, int32_t* tki, float* tkw, Ws ws,
-                     cudaStream_t s, const sgp_layer* next, bool norm_fused,
-                     bool down_in_combine) {
+                     cudaStream_t s, const sgp_layer* next, bool norm_fused) {
     StreamLauncher L(s);
     RunEnv e{&d, layer, kv_len, x_cur, x_out, T, ws, tki, tkw, use_tc_dense(d, T),
              use_tc_expert(d, T), 0, device_sms()};
     e.next = next;
     e.norm_fused = norm_fused;
-    e.down_in_combine = down_in_combine;
     for (int op = 0; op < SGP_N_OPS; ++op) {
         KCtx c = plain_ctx(ws.status(), kDefaultTimeout, ((uint32_t)op << 24) | ((uint32_t)li << 12));
         int r = enqueue_op(L, e, op, 0, c);
@@ -844,7 +832,7 @@ static int temporal_common(const sgp_dims* d, const sgp_layer* layers, int n_lay
         const bool fuse = can_fuse_norm(*d);
         const sgp_layer* next = (fuse && l + 1 < n_layers) ? &layers[l + 1] : nullptr;
         if ((r = run_layer_stream(*d, &layers[l], l, kv_len, xc, (bf16*)x_out, T, ti, tw, w, s,
-                                  next, fuse && l > 0, dump == nullptr)) != SGP_OK)
+                                  next, fuse && l > 0)) != SGP_OK)
             return r;
     }
     if (dump) {
