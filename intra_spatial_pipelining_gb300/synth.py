@@ -136,6 +136,7 @@ class LayerShape:
     inter: int
     rms_eps: float = 1e-5
     slot_map: str = "mod"          # "mod": g % E_local, "block": g * E_local // E
+    rope_theta: float = 0.0        # RoPE base (0: no rotation)
 
     @property
     def qkv_rows(self) -> int:

@@ -18,7 +18,9 @@ layers alternate as described in Section 5.1 of the same paper.
 
 Where the page leaves a step open, the readings are:
   * RMSNorm: y = x / sqrt(mean(x^2) + eps) * g, eps = 1e-5.
-  * No RoPE, no biases, no attention sinks, plain SwiGLU silu(gate) * up.
+  * No biases, no attention sinks, plain SwiGLU silu(gate) * up.  RoPE only when
+    the shape sets rope_theta > 0 (half-split pairs, applied to q and k_new at
+    position L-1 before rounding; cached keys are taken as already rotated).
   * The current token's k, v are written to cache slot L-1 (L = kv_len counts
     the current token); attention runs over [lo, L), lo = max(0, L - W) for a
     sliding window W, else 0.  Scale 1/sqrt(d).  Query head h reads KV head
@@ -88,6 +90,22 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, lo: int, hi: int) -> 
     return p @ v[lo:hi]
 
 
+def rope(x: np.ndarray, pos: int, theta: float) -> np.ndarray:
+    """Rotary position embedding of head vectors x [..][d] at position ``pos`` (unrounded).
+
+    Dimension pairs (i, i + d/2), i < d/2, are rotated by the angle pos * theta^(-2i/d)
+    (the half-split pairing; "SubGPU Pipelining: Intra-GPU Fine-Grained Spatial Parallelism
+    for LLM Inference", Fig. 3 lists RoPE in the operator chain without its variant)."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    freq = theta ** (-2.0 * np.arange(half) / d)
+    ang = pos * freq
+    c, s_ = np.cos(ang), np.sin(ang)
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b * s_, a * s_ + b * c], axis=-1)
+
+
 def topk(z: np.ndarray, k: int):
     """Indices of the k largest logits (descending, ties to the lower index) and
     the softmax over the selected logits."""
@@ -152,10 +170,16 @@ def layer(shape, weights: dict, x: np.ndarray, kv_len: np.ndarray, k_cache: np.n
         # stage A: RMSNorm -> QKV projection -> KV append -> attention
         a = bf16(rmsnorm(xt, W["g_attn"], shape.rms_eps))
         qkv = linear(a, W["w_qkv"])
-        q = bf16(qkv[: nq * d]).reshape(nq, d)
-        kn = bf16(qkv[nq * d:(nq + nkv) * d]).reshape(nkv, d)
-        vn = bf16(qkv[(nq + nkv) * d:]).reshape(nkv, d)
         L = int(kv_len[t])
+        qr = qkv[: nq * d].reshape(nq, d)
+        kr = qkv[nq * d:(nq + nkv) * d].reshape(nkv, d)
+        theta = getattr(shape, "rope_theta", 0.0)
+        if theta:
+            # the new token sits at position L-1; cached keys are already rotated
+            qr, kr = rope(qr, L - 1, theta), rope(kr, L - 1, theta)
+        q = bf16(qr)
+        kn = bf16(kr)
+        vn = bf16(qkv[(nq + nkv) * d:]).reshape(nkv, d)
         k_cache[t, :, L - 1, :] = kn
         v_cache[t, :, L - 1, :] = vn
         lo = max(0, L - window) if window > 0 else 0

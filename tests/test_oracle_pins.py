@@ -371,3 +371,58 @@ def test_makespan_equals_longest_path_random():
         for st in {t["stage"] for t in tasks}:
             iv = sorted((A[t["id"]], C[t["id"]]) for t in tasks if t["stage"] == st)
             assert all(iv[i][1] <= iv[i + 1][0] + 1e-12 for i in range(len(iv) - 1))
+
+
+# ---------------------------------------------------------------------------
+# RoPE (half-split pairs), pinned by properties of rotations and by the complex form
+# ---------------------------------------------------------------------------
+def test_rope_position_zero_is_identity_and_norm_is_kept():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((3, 64))
+    assert np.array_equal(O.rope(x, 0, 150000.0), x)
+    y = O.rope(x, 12345, 150000.0)
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-13)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    rng = np.random.default_rng(12)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    s1 = O.rope(q, 5, 10000.0) @ O.rope(k, 2, 10000.0)
+    s2 = O.rope(q, 30003, 10000.0) @ O.rope(k, 30000, 10000.0)
+    assert abs(s1 - s2) < 1e-9 * max(1.0, abs(s1))
+    # and composition adds positions
+    x = rng.standard_normal(64)
+    assert np.allclose(O.rope(O.rope(x, 7, 500.0), 11, 500.0), O.rope(x, 18, 500.0), atol=1e-12)
+
+
+def test_rope_matches_complex_rotation():
+    """Pair i (x_i, x_{i+d/2}) is the complex number x_i + j x_{i+d/2} times e^{j pos w_i},
+    w_i = theta^(-2i/d): a second formulation of the same rotation."""
+    rng = np.random.default_rng(13)
+    d, pos, theta = 8, 3, 100.0
+    x = rng.standard_normal(d)
+    zc = (x[: d // 2] + 1j * x[d // 2:]) * np.exp(1j * pos * theta ** (-np.arange(0, d, 2) / d))
+    assert np.allclose(O.rope(x, pos, theta), np.concatenate([zc.real, zc.imag]), atol=1e-13)
+
+
+def test_layer_rope_rotates_q_and_new_key_only():
+    """With RoPE on, q and the appended key are the unrotated ones rotated at L-1; the
+    appended value is untouched (tiny layer, brute-force comparison with RoPE off)."""
+    import dataclasses
+    wl = synth.WORKLOADS["tiny"].with_(n_tokens=3, kv_len=40)
+    w = synth.layer_weights(wl, 0, 21, "cpu")
+    x = O.f64(synth.x_in(wl, 21))
+    kvl = np.array([1, 17, 40])
+    k, v = synth.kv_cache(wl, 0, 21, "cpu")
+    plain = O.layer(wl.shape, w, x, kvl, O.f64(k), O.f64(v), 0)
+    shape_r = dataclasses.replace(wl.shape, rope_theta=10000.0)
+    rot = O.layer(shape_r, w, x, kvl, O.f64(k), O.f64(v), 0)
+    nq, d = wl.shape.n_q_heads, wl.shape.head_dim
+    for i, L in enumerate(kvl):
+        # rounding happens after the rotation: compare through the unrounded projection
+        a = plain["a"][i]
+        qkv = O.linear(a, O.f64(w["w_qkv"]))
+        q_ref = O.bf16(O.rope(qkv[: nq * d].reshape(nq, d), int(L) - 1, 10000.0)).reshape(-1)
+        assert np.array_equal(rot["q"][i], q_ref)
+        assert np.array_equal(rot["v_new"][i], plain["v_new"][i])
+    assert np.array_equal(rot["q"][0], plain["q"][0])   # L = 1: position 0, no rotation
