@@ -96,7 +96,8 @@ def describe(wl, extra):
                         f"({'alternating sliding-' + str(wl.window) + '/full' if wl.layer_pattern == 'alternate' else 'full'}"
                         f" attention), {wl.n_tokens} sequences, KV {wl.kv_len}, hidden {s.hidden}, "
                         f"{s.n_q_heads}q/{s.n_kv_heads}kv heads x {s.head_dim}, {s.n_experts} experts "
-                        f"top-{s.top_k}, {s.n_local_experts} local experts, SwiGLU {s.inter}"),
+                        f"top-{s.top_k}, {s.n_local_experts} local experts, SwiGLU {s.inter}"
+                        + (f", RoPE base {s.rope_theta:g}" if s.rope_theta else "")),
            "layers": wl.n_layers, "n_tokens": wl.n_tokens, "kv_len": wl.kv_len,
            "l2": "inputs larger than L2 (no flush)"}
     cfg.update(extra)

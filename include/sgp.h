@@ -74,7 +74,7 @@ enum {
     SGP_PATH_TC = 2     /* always the tcgen05 tensor-core GEMM                                  */
 };
 
-/* Layer dimensions.  Supported: head_dim == 64; hidden, inter and n_q_heads*head_dim
+/* Layer dimensions.  Up to 512 sequences per call.  Supported: head_dim == 64; hidden, inter and n_q_heads*head_dim
  * multiples of 64; n_q_heads a multiple of n_kv_heads with n_q_heads/n_kv_heads <= 16;
  * top_k <= 8; n_experts <= 1024; n_local_experts <= n_experts. */
 typedef struct sgp_dims {
@@ -91,6 +91,9 @@ typedef struct sgp_dims {
                              1: g -> g * E_local / E (expert-parallel loopback)      */
     int path;             /* SGP_PATH_*                                              */
     int gemv_max_tokens;  /* threshold of SGP_PATH_AUTO (16)                         */
+    float rope_theta;     /* RoPE base for q and the new key at position kv_len-1
+                             (half-split pairs i, i + d/2); 0 = no rotation.  Needs the
+                             tensor-core QKV path (SGP_ERR_UNSUPPORTED otherwise)      */
 } sgp_dims;
 
 /* One layer's weights and KV cache (all device pointers, caller-owned).

@@ -37,7 +37,8 @@ constexpr int kASlots = 1;                   // ring stages per warp
 constexpr int kAPos = 128;                   // positions per stage
 constexpr int kAHalf = kAPos * 128;          // K (or V) bytes of a stage: 16 KB
 constexpr int kAStage = 2 * kAHalf;          // K then V
-constexpr int kAMaxRows = 256;               // sequences per launch (prefix table size)
+constexpr int kAMaxRows = 512;               // sequences per launch (prefix table size)
+constexpr int kAPerLane = kAMaxRows / 32;    // sequences per lane of the prefix scan
 constexpr size_t kARing = (size_t)kAWarps * kASlots * kAStage;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -171,10 +172,10 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
 
     // ---- chunk counts and their prefix over the launch's sequences (warp 0) ----
     if (warp == 0) {
-        int cnt[8], sum = 0;
+        int cnt[kAPerLane], sum = 0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int t = lane * 8 + k;
+        for (int k = 0; k < kAPerLane; ++k) {
+            const int t = lane * kAPerLane + k;
             cnt[k] = 0;
             if (t < P.nrows) {
                 const int L = P.kv_len[P.row0 + t];
@@ -201,8 +202,8 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
         }
         int run = incl - sum;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int t = lane * 8 + k;
+        for (int k = 0; k < kAPerLane; ++k) {
+            const int t = lane * kAPerLane + k;
             if (t < P.nrows) pre[t] = run;
             run += cnt[k];
         }

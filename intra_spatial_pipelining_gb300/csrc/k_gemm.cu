@@ -332,6 +332,34 @@ __device__ __forceinline__ float4 sum_segments(const float* p, size_t sstride, i
     return acc;
 }
 
+// Rotates 4 consecutive features of one head (head-local index hf, a multiple of 4) by the
+// RoPE angles at position pos; p holds the pair partners (features hf +- 32).  The angle
+// pos * w_i is formed in float-float (w_i = hi + lo from the host) and reduced modulo 2 pi
+// with a two-constant Cody-Waite split before sincosf, so positions up to 2^24 keep
+// about 1e-6 rad of accuracy.
+__device__ __forceinline__ void rope_rotate(float4& v, const float4& p, int hf, int pos,
+                                            const EpiArgs& e) {
+    const float x[4] = {v.x, v.y, v.z, v.w}, y[4] = {p.x, p.y, p.z, p.w};
+    float o[4];
+    const bool first = hf < 32;
+    const float fp = (float)pos;
+    constexpr float kTwoPiHi = 6.28318548202514648f;      // nearest float to 2 pi
+    constexpr float kTwoPiLo = -1.7484555314695172e-07f;  // 2 pi - kTwoPiHi
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int i = (hf + c) & 31;
+        const float hi = e.rope_fhi[i], lo = e.rope_flo[i];
+        const float a = fp * hi;
+        const float a_err = fmaf(fp, hi, -a) + fp * lo;   // a + a_err = pos * w_i
+        const float k = rintf(a * 0.159154943091895336f);   // turns
+        const float r = (fmaf(-k, kTwoPiHi, a) + fmaf(-k, kTwoPiLo, 0.f)) + a_err;
+        float sn, cs;
+        sincosf(r, &sn, &cs);
+        o[c] = first ? fmaf(x[c], cs, -y[c] * sn) : fmaf(y[c], sn, x[c] * cs);
+    }
+    v = make_float4(o[0], o[1], o[2], o[3]);
+}
+
 // Instantiated per epilogue (MODE) so that each variant keeps only its own registers.
 template <int U, int MODE>
 __global__ void __launch_bounds__(256, U <= 4 ? 4 : 2)
@@ -362,8 +390,23 @@ __global__ void __launch_bounds__(256, U <= 4 ? 4 : 2)
             continue;
         }
         const int f0 = mt * 128 + 4 * q4;  // first of the 4 output features
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (f0 < e.n_out) v = sum_segments<U>(base + 4 * q4, sstride, P.ksplit);
+        if constexpr (MODE == EPI_QKV) {
+            // RoPE on q and k: the pair partner (feature +-32 of the same head) sits in lane
+            // q4 ^ 8 of this warp (32 lanes per token row, loop stride a multiple of 32), so
+            // the whole warp exchanges before any lane leaves the iteration
+            if (e.rope_theta > 0.f) {
+                float4 pv;
+                pv.x = __shfl_xor_sync(0xffffffffu, v.x, 8);
+                pv.y = __shfl_xor_sync(0xffffffffu, v.y, 8);
+                pv.z = __shfl_xor_sync(0xffffffffu, v.z, 8);
+                pv.w = __shfl_xor_sync(0xffffffffu, v.w, 8);
+                if (f0 < e.n_out && f0 < e.q_width + e.nkv * e.d)
+                    rope_rotate(v, pv, f0 & 63, e.kv_len[trow] - 1, e);
+            }
+        }
         if (f0 >= e.n_out) continue;
-        float4 v = sum_segments<U>(base + 4 * q4, sstride, P.ksplit);
         if constexpr (MODE == EPI_F32) {
             *reinterpret_cast<float4*>(e.out_f32 + (size_t)trow * e.ld + f0) = v;
             continue;

@@ -39,6 +39,8 @@ struct EpiArgs {
     bf16* vc;
     const int* kv_len;
     int nkv, cap, d;
+    float rope_theta;       // EPI_QKV: RoPE base for q and k (0: none)
+    float rope_fhi[32], rope_flo[32];  // theta^(-2i/64) as hi + lo float pairs (host, in double)
     // EPI_RESID: out = resid + acc (bf16); EPI_SWIGLU: out = silu(gate) * up (bf16)
     const bf16* resid;
     bf16* out;

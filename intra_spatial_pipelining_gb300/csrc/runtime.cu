@@ -222,6 +222,8 @@ struct GraphLauncher : Launcher {
 // =======================================================================================
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+constexpr int kMaxTokens = 512;  // sequences per call (attention prefix table, router groups)
+
 int check_dims(const sgp_dims* d) {
     if (!d) return fail_arg("dims is NULL");
     if (d->head_dim != 64) return fail_arg("head_dim must be 64");
@@ -236,6 +238,7 @@ int check_dims(const sgp_dims* d) {
         return fail_arg("n_local_experts out of range");
     if (d->slot_map != 0 && d->slot_map != 1) return fail_arg("slot_map must be 0 or 1");
     if (d->path < 0 || d->path > 2) return fail_arg("path must be SGP_PATH_*");
+    if (!(d->rope_theta >= 0.f)) return fail_arg("rope_theta must be >= 0");
     if (!(d->rms_eps > 0.f)) return fail_arg("rms_eps must be positive");
     if (d->hidden > 8192) return fail_arg("hidden above 8192 is not supported");
     return SGP_OK;
@@ -489,6 +492,13 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
             epi.nkv = d.n_kv_heads;
             epi.cap = e.layer->kv_cap;
             epi.d = d.head_dim;
+            epi.rope_theta = d.rope_theta;
+            if (d.rope_theta > 0.f)
+                for (int i = 0; i < 32; ++i) {
+                    const double f = std::pow((double)d.rope_theta, -2.0 * i / d.head_dim);
+                    epi.rope_fhi[i] = (float)f;
+                    epi.rope_flo[i] = (float)(f - (double)epi.rope_fhi[i]);
+                }
             break;
         case SGP_OP_OPROJ:
             W = (const bf16*)e.layer->w_o;
@@ -807,7 +817,9 @@ static int temporal_common(const sgp_dims* d, const sgp_layer* layers, int n_lay
                            const sgp_layer_dump* dump, cudaStream_t s) {
     int r;
     if ((r = check_dims(d)) != SGP_OK) return r;
-    if (T < 1 || T > 256) return fail_arg("n_tokens must be in [1, 256]");
+    if (T < 1 || T > kMaxTokens) return fail_arg("n_tokens must be in [1, 512]");
+    if (d->rope_theta > 0.f && !use_tc_dense(*d, T))
+        return fail_arg("RoPE needs the tensor-core QKV path");
     if (n_layers < 1 || !layers) return fail_arg("no layers");
     if (!kv_len || !x_in || !x_out || !ws) return fail_arg("NULL pointer");
     if (!aligned16(x_in) || !aligned16(x_out) || (reinterpret_cast<uintptr_t>(ws) & 255))
@@ -878,7 +890,9 @@ extern "C" int sgp_layer_op(const sgp_dims* d, const sgp_layer* layer, int op,
     int r;
     if ((r = check_dims(d)) != SGP_OK) return r;
     if (op < 0 || op >= SGP_N_OPS) return fail_arg("op index");
-    if (n_tokens < 1 || n_tokens > 256) return fail_arg("n_tokens must be in [1, 256]");
+    if (n_tokens < 1 || n_tokens > kMaxTokens) return fail_arg("n_tokens must be in [1, 512]");
+    if (d->rope_theta > 0.f && !use_tc_dense(*d, n_tokens))
+        return fail_arg("RoPE needs the tensor-core QKV path");
     if (!kv_len || !x_in || !x_out || !ws) return fail_arg("NULL pointer");
     if ((reinterpret_cast<uintptr_t>(ws) & 255) || !aligned16(x_in) || !aligned16(x_out))
         return fail_arg("alignment");
@@ -1179,7 +1193,9 @@ extern "C" int sgp_pipeline_create(const sgp_dims* d, const int* sm_split, int n
     if (n_stages < 1 || n_stages > 3) return fail_arg("n_stages must be 1, 2 or 3");
     if (microbatch < 1 || max_tokens < 1 || max_tokens % microbatch)
         return fail_arg("microbatch must divide max_tokens");
-    if (microbatch > 256) return fail_arg("microbatch above 256 sequences");
+    if (max_tokens > kMaxTokens) return fail_arg("more than 512 sequences");
+    if (d && d->rope_theta > 0.f && !use_tc_dense(*d, max_tokens))
+        return fail_arg("RoPE needs the tensor-core QKV path");
     if (max_kv_len < 1) return fail_arg("max_kv_len");
     if (!drv().core) {
         g_err = "CUDA driver entry points unavailable";
@@ -1270,6 +1286,8 @@ static int pipeline_prepare(sgp_pipeline* p, const sgp_layer* layers, int n_laye
     if (!p) return fail_arg("pipeline is NULL");
     if (!layers || n_layers < 1) return fail_arg("no layers");
     if (T < 1 || T > p->max_tokens || T % p->micro) return fail_arg("n_tokens vs microbatch");
+    if (p->dims.rope_theta > 0.f && !use_tc_dense(p->dims, T))
+        return fail_arg("RoPE needs the tensor-core QKV path");
     if (!kv_len || !x_in || !x_out || !aligned16(x_in) || !aligned16(x_out))
         return fail_arg("NULL or unaligned pointer");
     for (int l = 0; l < n_layers; ++l) {

@@ -33,7 +33,8 @@ class sgp_dims(C.Structure):
     _fields_ = [("hidden", C.c_int), ("n_q_heads", C.c_int), ("n_kv_heads", C.c_int),
                 ("head_dim", C.c_int), ("n_experts", C.c_int), ("top_k", C.c_int),
                 ("n_local_experts", C.c_int), ("inter", C.c_int), ("rms_eps", C.c_float),
-                ("slot_map", C.c_int), ("path", C.c_int), ("gemv_max_tokens", C.c_int)]
+                ("slot_map", C.c_int), ("path", C.c_int), ("gemv_max_tokens", C.c_int),
+                ("rope_theta", C.c_float)]
 
 
 class sgp_layer(C.Structure):
@@ -157,7 +158,8 @@ def _stream(stream) -> Optional[int]:
 def make_dims(shape, path: int = PATH_AUTO, gemv_max_tokens: int = 16) -> sgp_dims:
     return sgp_dims(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
                     shape.n_experts, shape.top_k, shape.n_local_experts, shape.inter,
-                    shape.rms_eps, 0 if shape.slot_map == "mod" else 1, path, gemv_max_tokens)
+                    shape.rms_eps, 0 if shape.slot_map == "mod" else 1, path, gemv_max_tokens,
+                    float(getattr(shape, "rope_theta", 0.0)))
 
 
 def make_layer(w: dict, k_cache, v_cache, window: int) -> sgp_layer:

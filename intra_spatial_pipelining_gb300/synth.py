@@ -184,6 +184,11 @@ SHAPE_TINY = LayerShape(hidden=256, n_q_heads=4, n_kv_heads=1, head_dim=64, n_ex
 SHAPE_GPTOSS = LayerShape(hidden=2880, n_q_heads=64, n_kv_heads=8, head_dim=64, n_experts=128,
                           top_k=4, n_local_experts=4, inter=2880)
 
+# the pages' own per-GPU slice: TP8 attention (8 query heads, 1 KV head per GPU), DP4 (512
+# sequences per TP group), KV 32,768, RoPE; EP32 experts (4 local slots)
+SHAPE_PAPER = LayerShape(hidden=2880, n_q_heads=8, n_kv_heads=1, head_dim=64, n_experts=128,
+                         top_k=4, n_local_experts=4, inter=2880, rope_theta=150000.0)
+
 WORKLOADS = {
     # tiny layer: 8 sequences, KV 128, 8 experts top-2, 2 microbatches of 4
     "tiny": Workload("tiny", SHAPE_TINY, n_tokens=8, n_layers=1, kv_len=128,
@@ -194,6 +199,9 @@ WORKLOADS = {
     # 36-layer stack, alternating sliding-128 / full attention, KV 8192
     "gptoss_36l": Workload("gptoss_36l", SHAPE_GPTOSS, n_tokens=64, n_layers=36,
                            kv_len=8192, layer_pattern="alternate", microbatches=2),
+    # the pages' decode configuration: 512 sequences x KV 32,768 per GPU, 36 layers
+    "paper_32k": Workload("paper_32k", SHAPE_PAPER, n_tokens=512, n_layers=36,
+                          kv_len=32768, layer_pattern="alternate", microbatches=2),
 }
 
 

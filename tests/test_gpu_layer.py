@@ -145,6 +145,40 @@ def test_attention_group_sizes(G):
     H.assert_close("o", bufs["o"], ref["o"])
 
 
+def test_rope_layer_vs_oracle_long_positions():
+    """RoPE on q and the new key (tensor-core QKV path) at positions up to 32,767."""
+    shape = dataclasses.replace(synth.SHAPE_TINY, rope_theta=150000.0)
+    wl = synth.WORKLOADS["tiny"].with_(shape=shape, n_tokens=16, kv_len=32768, kv_cap=32768)
+    lens = [1, 2, 3, 64, 1000, 1023, 1024, 4096, 9999, 16384, 20000, 30000, 32000, 32766,
+            32767, 32768]
+    for a in range(20):
+        inp = H.make_inputs(wl, 16, [a])
+        inp.kv_len.copy_(torch.tensor(lens, dtype=torch.int32))
+        w = {n: (v.cpu() if v is not None else None) for n, v in inp.weights[0].items()}
+        k, v = synth.kv_cache(wl, 0, inp.seed, "cpu")
+        ref = O.layer(wl.shape, w, O.f64(inp.x), inp.kv_len.cpu().numpy(), O.f64(k), O.f64(v), 0)
+        if min(O.topk_margin(z, wl.shape.top_k) for z in ref["logits"]) >= H.MARGIN:
+            break
+    lay = inp.sgp_layers()[0]
+    d = H.dims(wl.shape, sgp.PATH_TC)
+    ws = H.workspace(d, wl.n_tokens, wl.cap)
+    out = torch.empty_like(inp.x)
+    bufs, st = H.dump_buffers(wl.shape, wl.n_tokens)
+    sgp.sgp_layer_temporal(d, lay, inp.kv_len, inp.x, out, wl.n_tokens, None, None, ws, st)
+    assert sgp.sgp_status_from_workspace(ws) == sgp.SGP_OK
+    H.assert_close("q (rotated)", bufs["q"], ref["q"])
+    kc = inp.caches[0][0]
+    got_k = torch.stack([kc[t, :, lens[t] - 1] for t in range(wl.n_tokens)])
+    H.assert_close("appended key (rotated)", got_k, ref["k_new"])
+    H.assert_close("o", bufs["o"], ref["o"])
+    H.assert_close("x_next", out, ref["x_next"])
+    # RoPE needs the tensor-core QKV path
+    with pytest.raises(sgp.SgpError) as e:
+        sgp.sgp_layer_temporal(H.dims(wl.shape, sgp.PATH_GEMV), lay, inp.kv_len, inp.x, out,
+                               wl.n_tokens, None, None, ws)
+    assert e.value.code == sgp.SGP_ERR_INVALID_ARG
+
+
 def test_invalid_arguments_are_rejected():
     wl = synth.WORKLOADS["tiny"]
     inp = H.make_inputs(wl, 4)

@@ -161,6 +161,14 @@ def test_full_size_stack_sampled_sequences_vs_oracle():
     _teacher_forced_check(H.make_inputs(wl, 13), [5, 40])
 
 
+def test_paper_shape_two_layers():
+    """The pages' per-GPU decode shape -- 512 sequences, 8 query heads on 1 KV head, KV
+    32,768, RoPE -- one sliding and one full layer, layer by layer against the oracle on
+    sampled sequences, pipelined (2 microbatches of 256) == temporal."""
+    wl = synth.WORKLOADS["paper_32k"].with_(n_layers=2)
+    _teacher_forced_check(H.make_inputs(wl, 17), [3, 300, 511], min_checked=0.5)
+
+
 @pytest.mark.parametrize("n_tokens", [8, 16, 32, 64, 128, 256])
 def test_batch_length_sweep(n_tokens):
     """Batch/length sweep shapes: ragged KV lengths uniform in [512, 16384], one sliding and
