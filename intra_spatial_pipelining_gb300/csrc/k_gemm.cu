@@ -133,7 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
-            const uint64_t pol_w = P.keep_weights ? policy_evict_last() : policy_evict_first();
+            // a weight tile read again by a later token pass of the same unit (or by a later
+            // microbatch) is kept in L2; its last read lets it go first
+            const uint64_t pol_keep = policy_evict_last();
+            const uint64_t pol_drop = P.keep_weights ? pol_keep : policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             uint32_t it = 0;
             uint32_t issued_mask = 0, issued_par = 0;
@@ -146,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rowA1 = x.g * P.rows_per_group + x.mt * P.a_tile_stride;
                 for (int pass = 0; pass < x.npass; ++pass) {
                     const int c0 = pass * P.n_cap;
+                    const uint64_t pol_w = pass + 1 < x.npass ? pol_keep : pol_drop;
                     for (int i = 0; i < x.nk; ++i, ++it) {
                         const int s = it % S;
                         const uint32_t j = it / S;
