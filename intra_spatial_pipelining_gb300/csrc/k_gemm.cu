@@ -43,6 +43,84 @@ __device__ __forceinline__ bool epi_bar_or(bool v) {
     return r != 0;
 }
 
+// Rotates 4 consecutive features of one head (head-local index hf, a multiple of 4) by the
+// RoPE angles at position pos; p holds the pair partners (features hf +- 32).  The angle
+// pos * w_i is formed in float-float (w_i = hi + lo from the host) and reduced modulo 2 pi
+// with a two-constant Cody-Waite split before sincosf, so positions up to 2^24 keep
+// about 1e-6 rad of accuracy.
+__device__ __forceinline__ void rope_rotate(float4& v, const float4& p, int hf, int pos,
+                                            const EpiArgs& e) {
+    const float x[4] = {v.x, v.y, v.z, v.w}, y[4] = {p.x, p.y, p.z, p.w};
+    float o[4];
+    const bool first = hf < 32;
+    const float fp = (float)pos;
+    constexpr float kTwoPiHi = 6.28318548202514648f;      // nearest float to 2 pi
+    constexpr float kTwoPiLo = -1.7484555314695172e-07f;  // 2 pi - kTwoPiHi
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int i = (hf + c) & 31;
+        const float hi = e.rope_fhi[i], lo = e.rope_flo[i];
+        const float a = fp * hi;
+        const float a_err = fmaf(fp, hi, -a) + fp * lo;   // a + a_err = pos * w_i
+        const float k = rintf(a * 0.159154943091895336f);   // turns
+        const float r = (fmaf(-k, kTwoPiHi, a) + fmaf(-k, kTwoPiLo, 0.f)) + a_err;
+        float sn, cs;
+        sincosf(r, &sn, &cs);
+        o[c] = first ? fmaf(x[c], cs, -y[c] * sn) : fmaf(y[c], sn, x[c] * cs);
+    }
+    v = make_float4(o[0], o[1], o[2], o[3]);
+}
+
+// ---------------------------------------------------------------------------------------
+// Epilogue stores shared by the finishing pass and the GEMM's own epilogue (K split 1).
+// v holds 4 consecutive output features f0..f0+3 of token row trow (RoPE already applied).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void store_out4(const EpiArgs& e, const KCtx& ctx, int mode, int trow,
+                                           int f0, float4 v) {
+    if (mode == EPI_F32) {
+        *reinterpret_cast<float4*>(e.out_f32 + (size_t)trow * e.ld + f0) = v;
+        return;
+    }
+    if (mode == EPI_RESID) {
+        const uint2 rr = *reinterpret_cast<const uint2*>(e.resid + (size_t)trow * e.ld + f0);
+        const float2 r01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.x));
+        const float2 r23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.y));
+        v.x += r01.x;
+        v.y += r01.y;
+        v.z += r23.x;
+        v.w += r23.y;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    bf16* dst;
+    if (mode == EPI_RESID) {
+        dst = e.out + (size_t)trow * e.ld + f0;
+    } else if (f0 < e.q_width) {  // EPI_QKV: query heads
+        dst = e.q + (size_t)trow * e.q_width + f0;
+    } else {                      // EPI_QKV: append k / v at slot kv_len - 1
+        const int r = f0 - e.q_width;
+        const int which = r / (e.nkv * e.d);
+        const int kh = (r / e.d) % e.nkv;
+        const int pos = e.kv_len[trow] - 1;
+        if (pos < 0 || pos >= e.cap) {
+            report(ctx, ST_BOUNDS, (uint32_t)pos);
+            return;
+        }
+        bf16* cache = which == 0 ? e.kc : e.vc;
+        dst = cache + (((size_t)trow * e.nkv + kh) * e.cap + pos) * e.d + (r % e.d);
+    }
+    *reinterpret_cast<uint2*>(dst) = o;
+}
+
+__device__ __forceinline__ void store_swiglu4(const EpiArgs& e, int trow, int i0, float4 g,
+                                              float4 up) {
+    uint2 o;
+    o.x = pack_bf16x2(silu_f(g.x) * up.x, silu_f(g.y) * up.y);
+    o.y = pack_bf16x2(silu_f(g.z) * up.z, silu_f(g.w) * up.w);
+    *reinterpret_cast<uint2*>(e.out + (size_t)trow * e.ld + i0) = o;
+}
+
 // One work unit = (group, 128-row weight tile, K segment) and its token range.
 struct Unit {
     int g, mt, ks, kb0, nk, n, npass, tma_r0, lr0;
@@ -290,13 +368,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[b]);  // the accumulator may be reused
-                fence_proxy_async();
-                epi_bar();
-                if (issuer) {
-                    const int nv = min(np, x.n - c0);
-                    bulk_store(P.partial + (((size_t)x.mt * P.ksplit + x.ks) * P.R + x.lr0 + c0) * 128,
-                               Ts, (uint32_t)nv * 512u);
-                    bulk_commit();
+                const int nv = min(np, x.n - c0);
+                if (P.fused_epi) {
+                    // K split 1: the tile is the final sum; apply the epilogue from shared
+                    // memory (the next job's barrier above keeps Ts until every warp is done)
+                    epi_bar();
+                    const EpiArgs& e = P.epi;
+                    const int ew = warp - 2;  // 0..3
+                    const int prow0 = x.lr0 + c0;  // partial-row numbering of token 0
+                    if (e.mode == EPI_SWIGLU) {
+                        const int h = lane >> 4, q4 = lane & 15;
+                        const int i0 = x.mt * 64 + 4 * q4;
+                        for (int t = 2 * ew + h; t < nv; t += 8) {
+                            if (i0 < e.n_out) {
+                                const float4 g = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * q4);
+                                const float4 up = *reinterpret_cast<const float4*>(Ts + t * 128 + 64 + 4 * q4);
+                                store_swiglu4(e, P.out_row0 + prow0 + t, i0, g, up);
+                            }
+                        }
+                    } else {
+                        const int f0 = x.mt * 128 + 4 * lane;
+                        for (int t = ew; t < nv; t += 4) {
+                            const int trow = P.out_row0 + prow0 + t;
+                            float4 v = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * lane);
+                            if (e.mode == EPI_QKV && e.rope_theta > 0.f) {
+                                // pair partner (feature +-32 of the same head): lane ^ 8
+                                const float4 pv = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * (lane ^ 8));
+                                if (f0 < e.n_out && f0 < e.q_width + e.nkv * e.d)
+                                    rope_rotate(v, pv, f0 & 63, e.kv_len[trow] - 1, e);
+                            }
+                            if (f0 < e.n_out) store_out4(e, ctx, e.mode, trow, f0, v);
+                        }
+                    }
+                } else {
+                    fence_proxy_async();
+                    epi_bar();
+                    if (issuer) {
+                        bulk_store(P.partial + (((size_t)x.mt * P.ksplit + x.ks) * P.R + x.lr0 + c0) * 128,
+                                   Ts, (uint32_t)nv * 512u);
+                        bulk_commit();
+                    }
                 }
             }
         }
@@ -336,34 +447,6 @@ __device__ __forceinline__ float4 sum_segments(const float* p, size_t sstride, i
     return acc;
 }
 
-// Rotates 4 consecutive features of one head (head-local index hf, a multiple of 4) by the
-// RoPE angles at position pos; p holds the pair partners (features hf +- 32).  The angle
-// pos * w_i is formed in float-float (w_i = hi + lo from the host) and reduced modulo 2 pi
-// with a two-constant Cody-Waite split before sincosf, so positions up to 2^24 keep
-// about 1e-6 rad of accuracy.
-__device__ __forceinline__ void rope_rotate(float4& v, const float4& p, int hf, int pos,
-                                            const EpiArgs& e) {
-    const float x[4] = {v.x, v.y, v.z, v.w}, y[4] = {p.x, p.y, p.z, p.w};
-    float o[4];
-    const bool first = hf < 32;
-    const float fp = (float)pos;
-    constexpr float kTwoPiHi = 6.28318548202514648f;      // nearest float to 2 pi
-    constexpr float kTwoPiLo = -1.7484555314695172e-07f;  // 2 pi - kTwoPiHi
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int i = (hf + c) & 31;
-        const float hi = e.rope_fhi[i], lo = e.rope_flo[i];
-        const float a = fp * hi;
-        const float a_err = fmaf(fp, hi, -a) + fp * lo;   // a + a_err = pos * w_i
-        const float k = rintf(a * 0.159154943091895336f);   // turns
-        const float r = (fmaf(-k, kTwoPiHi, a) + fmaf(-k, kTwoPiLo, 0.f)) + a_err;
-        float sn, cs;
-        sincosf(r, &sn, &cs);
-        o[c] = first ? fmaf(x[c], cs, -y[c] * sn) : fmaf(y[c], sn, x[c] * cs);
-    }
-    v = make_float4(o[0], o[1], o[2], o[3]);
-}
-
 // Instantiated per epilogue (MODE) so that each variant keeps only its own registers.
 template <int U, int MODE>
 __global__ void __launch_bounds__(256, U <= 4 ? 4 : 2)
@@ -387,10 +470,7 @@ __global__ void __launch_bounds__(256, U <= 4 ? 4 : 2)
             if (i0 >= e.n_out) continue;
             const float4 g = sum_segments<U>(base + 4 * q4, sstride, P.ksplit);
             const float4 up = sum_segments<U>(base + 64 + 4 * q4, sstride, P.ksplit);
-            uint2 o;
-            o.x = pack_bf16x2(silu_f(g.x) * up.x, silu_f(g.y) * up.y);
-            o.y = pack_bf16x2(silu_f(g.z) * up.z, silu_f(g.w) * up.w);
-            *reinterpret_cast<uint2*>(e.out + (size_t)trow * e.ld + i0) = o;
+            store_swiglu4(e, trow, i0, g, up);
             continue;
         }
         const int f0 = mt * 128 + 4 * q4;  // first of the 4 output features
@@ -411,40 +491,7 @@ __global__ void __launch_bounds__(256, U <= 4 ? 4 : 2)
             }
         }
         if (f0 >= e.n_out) continue;
-        if constexpr (MODE == EPI_F32) {
-            *reinterpret_cast<float4*>(e.out_f32 + (size_t)trow * e.ld + f0) = v;
-            continue;
-        }
-        if constexpr (MODE == EPI_RESID) {
-            const uint2 rr = *reinterpret_cast<const uint2*>(e.resid + (size_t)trow * e.ld + f0);
-            const float2 r01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.x));
-            const float2 r23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.y));
-            v.x += r01.x;
-            v.y += r01.y;
-            v.z += r23.x;
-            v.w += r23.y;
-        }
-        uint2 o;
-        o.x = pack_bf16x2(v.x, v.y);
-        o.y = pack_bf16x2(v.z, v.w);
-        bf16* dst;
-        if constexpr (MODE == EPI_RESID) {
-            dst = e.out + (size_t)trow * e.ld + f0;
-        } else if (f0 < e.q_width) {  // EPI_QKV: query heads
-            dst = e.q + (size_t)trow * e.q_width + f0;
-        } else {                      // EPI_QKV: append k / v at slot kv_len - 1
-            const int r = f0 - e.q_width;
-            const int which = r / (e.nkv * e.d);
-            const int kh = (r / e.d) % e.nkv;
-            const int pos = e.kv_len[trow] - 1;
-            if (pos < 0 || pos >= e.cap) {
-                report(ctx, ST_BOUNDS, (uint32_t)pos);
-                continue;
-            }
-            bf16* cache = which == 0 ? e.kc : e.vc;
-            dst = cache + (((size_t)trow * e.nkv + kh) * e.cap + pos) * e.d + (r % e.d);
-        }
-        *reinterpret_cast<uint2*>(dst) = o;
+        store_out4(e, ctx, MODE, trow, f0, v);
     }
     task_end(ctx);
 }

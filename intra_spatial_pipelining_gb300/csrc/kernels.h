@@ -80,6 +80,11 @@ struct GemmProblem {
     float* partial;         // [m_tiles][ksplit][R][128] fp32 tiles (token-major rows)
     int n_units;            // n_groups * m_tiles * ksplit
     int grid;               // persistent CTAs (one per SM of the pool)
+    // ksplit == 1: the epilogue is applied here from the staged tile (no partials, no
+    // finishing pass); out_row0 = output row of partial row 0
+    int fused_epi;
+    int out_row0;
+    EpiArgs epi;
 };
 
 // Sum of the K segments of every partial tile + fused epilogue.

@@ -260,6 +260,8 @@ int q_width(const sgp_dims& d) { return d.n_q_heads * d.head_dim; }
 // Fixed K split of a projection (a function of the shape only, so the fp32 summation order
 // never depends on the SM pool): ~456 work units for the persistent GEMM (3 per SM of a
 // 152-SM part), at least 4 k-blocks per segment.
+// tiles counts (weight tile, 128-token pass) pairs of the full batch: with many tokens the
+// passes alone give every SM work and no K split is needed.
 int choose_ksplit(int tiles, int kb_total) {
     const int n_sb = cdiv(kb_total, kGemmKps);  // K segments are made of whole stage blocks
     int ks = (int)std::lround(456.0 / tiles);
@@ -270,7 +272,9 @@ int choose_ksplit(int tiles, int kb_total) {
 struct GemmShape {
     int K, rows_per_group, n_groups, m_tiles, a_tile_stride, a_second_off, ksplit;
 };
-GemmShape gemm_shape(const sgp_dims& d, int op) {
+// T is the full batch of the call (never the microbatch), so the K split -- and with it every
+// summation order -- is the same for temporal and pipelined execution.
+GemmShape gemm_shape(const sgp_dims& d, int op, int T) {
     GemmShape g{};
     switch (op) {
         case SGP_OP_QKV:
@@ -286,7 +290,9 @@ GemmShape gemm_shape(const sgp_dims& d, int op) {
             g = {d.inter, d.hidden, d.n_local_experts, cdiv(d.hidden, 128), 128, 64, 1};
             break;
     }
-    g.ksplit = choose_ksplit(g.n_groups * g.m_tiles, g.K / 64);
+    const bool grouped = op == SGP_OP_EXPERT_UP || op == SGP_OP_EXPERT_DOWN;
+    const int rows = grouped ? cdiv(T * d.top_k, d.n_local_experts) : T;
+    g.ksplit = choose_ksplit(g.n_groups * g.m_tiles * cdiv(std::max(1, rows), 128), g.K / 64);
     return g;
 }
 
@@ -342,7 +348,7 @@ Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags, int
     L.zero_beg = off;
     int max_tiles = 0;
     for (int op : {SGP_OP_QKV, SGP_OP_OPROJ, SGP_OP_EXPERT_UP, SGP_OP_EXPERT_DOWN}) {
-        GemmShape g = gemm_shape(d, op);
+        GemmShape g = gemm_shape(d, op, T);
         max_tiles = std::max(max_tiles, g.n_groups * g.m_tiles);
     }
     L.max_tiles = max_tiles;
@@ -377,7 +383,7 @@ Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags, int
     L.ybuf = mtake((size_t)R * H * 4);
     size_t gp = 0;
     for (int op : {SGP_OP_QKV, SGP_OP_OPROJ, SGP_OP_EXPERT_UP, SGP_OP_EXPERT_DOWN}) {
-        GemmShape g = gemm_shape(d, op);
+        GemmShape g = gemm_shape(d, op, T);
         const int rows = (op == SGP_OP_QKV || op == SGP_OP_OPROJ) ? b : R;
         gp = std::max(gp, (size_t)g.ksplit * rows * g.m_tiles * 128 * 4);
     }
@@ -470,7 +476,7 @@ bool can_fuse_norm(const sgp_dims& d) { return d.hidden <= 8192; }
 int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     const sgp_dims& d = *e.d;
     const int b = e.ws.L->b, row0 = mu * b, R = b * d.top_k;
-    GemmShape gs = gemm_shape(d, op);
+    GemmShape gs = gemm_shape(d, op, e.T);
     const bool grouped = (op == SGP_OP_EXPERT_UP || op == SGP_OP_EXPERT_DOWN);
     const bool tc = grouped ? e.tc_expert : e.tc_dense;
     const bf16* W = nullptr;
@@ -602,6 +608,12 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     p.serpentine = grouped && e.serpentine && (mu & 1);
     p.keep_weights = e.keep_weights ? 1 : 0;
     p.partial = e.ws.mu<float>(mu, e.ws.L->gemm_part);
+    if (p.ksplit == 1) {  // the GEMM applies the epilogue itself: one launch for the op
+        p.fused_epi = 1;
+        p.out_row0 = grouped ? 0 : row0;
+        p.epi = epi;
+        return enqueue_gemm_tc(L, p, c);
+    }
     // the flag check belongs to the first launch, the publish to the last
     KCtx c1 = c, c2 = c;
     c1.post_flag = nullptr;
