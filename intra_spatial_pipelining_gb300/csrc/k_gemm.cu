@@ -358,55 +358,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t tbase = tmem + b * acc_cols + ((uint32_t)(q * 32) << 16);
-                for (int cc = 0; cc < np; cc += 16) {
-                    uint32_t v[16];
-                    tmem_ld_x16(tbase + (uint32_t)cc, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) Ts[(cc + t) * 128 + row] = __uint_as_float(v[t]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[b]);  // the accumulator may be reused
                 const int nv = min(np, x.n - c0);
-                if (P.fused_epi) {
-                    // K split 1: the tile is the final sum; apply the epilogue from shared
-                    // memory (the next job's barrier above keeps Ts until every warp is done)
-                    epi_bar();
-                    const EpiArgs& e = P.epi;
-                    const int ew = warp - 2;  // 0..3
-                    const int prow0 = x.lr0 + c0;  // partial-row numbering of token 0
-                    if (e.mode == EPI_SWIGLU) {
-                        const int h = lane >> 4, q4 = lane & 15;
-                        const int i0 = x.mt * 64 + 4 * q4;
-                        for (int t = 2 * ew + h; t < nv; t += 8) {
-                            if (i0 < e.n_out) {
-                                const float4 g = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * q4);
-                                const float4 up = *reinterpret_cast<const float4*>(Ts + t * 128 + 64 + 4 * q4);
-                                store_swiglu4(e, P.out_row0 + prow0 + t, i0, g, up);
+                // the accumulator leaves TMEM in chunks of kTsRows tokens through Ts
+                for (int ch = 0; ch < np; ch += kTsRows) {
+                    const int cn = min(kTsRows, np - ch);
+                    if (ch > 0) {
+                        // the previous chunk's readers (bulk store / epilogue) are done with Ts
+                        if (issuer) bulk_wait_read();
+                        epi_bar();
+                    }
+                    for (int cc = 0; cc < cn; cc += 16) {
+                        uint32_t v[16];
+                        tmem_ld_x16(tbase + (uint32_t)(ch + cc), v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) Ts[(cc + t) * 128 + row] = __uint_as_float(v[t]);
+                    }
+                    if (ch + kTsRows >= np) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty[b]);  // the accumulator may be reused
+                    }
+                    const int cv = min(cn, nv - ch);  // valid tokens of this chunk
+                    if (P.fused_epi) {
+                        // K split 1: the tile is the final sum; apply the epilogue from Ts
+                        // (the next chunk's or job's barrier keeps Ts until every warp is done)
+                        epi_bar();
+                        const EpiArgs& e = P.epi;
+                        const int ew = warp - 2;  // 0..3
+                        const int prow0 = x.lr0 + c0 + ch;  // partial-row numbering of token 0
+                        if (e.mode == EPI_SWIGLU) {
+                            const int h = lane >> 4, q4 = lane & 15;
+                            const int i0 = x.mt * 64 + 4 * q4;
+                            for (int t = 2 * ew + h; t < cv; t += 8) {
+                                if (i0 < e.n_out) {
+                                    const float4 g = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * q4);
+                                    const float4 up = *reinterpret_cast<const float4*>(Ts + t * 128 + 64 + 4 * q4);
+                                    store_swiglu4(e, P.out_row0 + prow0 + t, i0, g, up);
+                                }
                             }
+                        } else {
+                            const int f0 = x.mt * 128 + 4 * lane;
+                            for (int t = ew; t < cv; t += 4) {
+                                const int trow = P.out_row0 + prow0 + t;
+                                float4 v = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * lane);
+                                if (e.mode == EPI_QKV && e.rope_theta > 0.f) {
+                                    // pair partner (feature +-32 of the same head): lane ^ 8
+                                    const float4 pv = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * (lane ^ 8));
+                                    if (f0 < e.n_out && f0 < e.q_width + e.nkv * e.d)
+                                        rope_rotate(v, pv, f0 & 63, e.kv_len[trow] - 1, e);
+                                }
+                                if (f0 < e.n_out) store_out4(e, ctx, e.mode, trow, f0, v);
+                            }
+                        }
+                    } else if (cv > 0) {
+                        fence_proxy_async();
+                        epi_bar();
+                        if (issuer) {
+                            bulk_store(P.partial + (((size_t)x.mt * P.ksplit + x.ks) * P.R + x.lr0 + c0 + ch) * 128,
+                                       Ts, (uint32_t)cv * 512u);
+                            bulk_commit();
                         }
                     } else {
-                        const int f0 = x.mt * 128 + 4 * lane;
-                        for (int t = ew; t < nv; t += 4) {
-                            const int trow = P.out_row0 + prow0 + t;
-                            float4 v = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * lane);
-                            if (e.mode == EPI_QKV && e.rope_theta > 0.f) {
-                                // pair partner (feature +-32 of the same head): lane ^ 8
-                                const float4 pv = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * (lane ^ 8));
-                                if (f0 < e.n_out && f0 < e.q_width + e.nkv * e.d)
-                                    rope_rotate(v, pv, f0 & 63, e.kv_len[trow] - 1, e);
-                            }
-                            if (f0 < e.n_out) store_out4(e, ctx, e.mode, trow, f0, v);
-                        }
-                    }
-                } else {
-                    fence_proxy_async();
-                    epi_bar();
-                    if (issuer) {
-                        bulk_store(P.partial + (((size_t)x.mt * P.ksplit + x.ks) * P.R + x.lr0 + c0) * 128,
-                                   Ts, (uint32_t)nv * 512u);
-                        bulk_commit();
+                        epi_bar();
                     }
                 }
             }
@@ -605,8 +619,9 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KC
 }  // namespace
 
 size_t gemm_tc_ring_bytes(int n_cap, int stages) {
-    // stage ring, then the accumulator staging area [n_cap][128] fp32
-    return (size_t)stages * (kStageA + kGemmKps * n_cap * 128) + (size_t)n_cap * 512;
+    // stage ring, then the accumulator staging area [min(n_cap, kTsRows)][128] fp32
+    return (size_t)stages * (kStageA + kGemmKps * n_cap * 128) +
+           (size_t)std::min(n_cap, kTsRows) * 512;
 }
 
 size_t gemm_tc_smem_bytes(int n_cap, int stages) {

@@ -54,6 +54,10 @@ struct EpiArgs {
 // Each pipeline stage holds kGemmKps consecutive 64-wide k-blocks: the 128-row weight tile
 // arrives in ONE TMA operation (32 KB) and the stage's activation rows in one more.
 constexpr int kGemmKps = 2;
+// tokens per pass go up to 256 (one MMA's N); the accumulator is drained through shared
+// memory kTsRows tokens at a time
+constexpr int kGemmMaxN = 256;
+constexpr int kTsRows = 64;
 
 struct GemmProblem {
     // weights: plain  3-D {64, rows, k-blocks} box {64, 128, 2};
@@ -71,7 +75,7 @@ struct GemmProblem {
     const int* group_offsets;  // device [n_groups + 1] token-row ranges, or NULL (dense)
     int row0, nrows;        // dense: token rows [row0, row0 + nrows)
     int R;                  // rows of the partial-sum buffer
-    int n_cap;              // tokens per pass (multiple of 16, <= 256)
+    int n_cap;              // tokens per pass (multiple of 16, <= kGemmMaxN)
     int stages;             // shared-memory pipeline depth
     int ring_bytes;         // bytes of the stage ring (also holds the staged accumulator)
     int serpentine;         // visit groups in reverse order

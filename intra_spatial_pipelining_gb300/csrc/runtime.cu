@@ -292,7 +292,7 @@ GemmShape gemm_shape(const sgp_dims& d, int op, int T) {
     }
     const bool grouped = op == SGP_OP_EXPERT_UP || op == SGP_OP_EXPERT_DOWN;
     const int rows = grouped ? cdiv(T * d.top_k, d.n_local_experts) : T;
-    g.ksplit = choose_ksplit(g.n_groups * g.m_tiles * cdiv(std::max(1, rows), 128), g.K / 64);
+    g.ksplit = choose_ksplit(g.n_groups * g.m_tiles * cdiv(std::max(1, rows), kGemmMaxN), g.K / 64);
     return g;
 }
 
@@ -559,7 +559,7 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     // plus a quarter (grouped; a fuller slot takes a second pass)
     int expect = grouped ? cdiv(R, gs.n_groups) : b;
     if (grouped) expect += expect / 4;
-    p.n_cap = std::min(128, std::max(16, (expect + 15) & ~15));
+    p.n_cap = std::min(kGemmMaxN, std::max(16, (expect + 15) & ~15));
     const uint64_t kb_total = gs.K / 64, rowb = (uint64_t)gs.K * 2;
     const uint64_t total_rows = (uint64_t)gs.n_groups * gs.rows_per_group;
     if (op == SGP_OP_EXPERT_UP) {
@@ -601,7 +601,8 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     p.R = grouped ? R : b;
     const int stage_bytes = kGemmKps * (16384 + p.n_cap * 128);
     // one persistent CTA per SM: ring + accumulator staging within the 227 KB limit
-    p.stages = std::max(2, std::min(8, (232448 - 1280 - p.n_cap * 512) / stage_bytes));
+    p.stages = std::max(2, std::min(8, (232448 - 1280 - std::min(p.n_cap, kTsRows) * 512) /
+                                          stage_bytes));
     p.ring_bytes = (int)gemm_tc_ring_bytes(p.n_cap, p.stages);
     p.n_units = gs.n_groups * gs.m_tiles * gs.ksplit;
     p.grid = e.pool_sms;
