@@ -205,6 +205,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // constant weights into the first ring stages before it waits.  A grouped problem's
     // token ranges come from the previous kernel, so there everyone waits now.
     const bool run_ahead = warp == 0 && lane == 0 && P.group_offsets == nullptr;
+    if (warp == 0 && lane == 0 && !run_ahead) {
+        // grouped problem: which tokens a unit covers is known only after the previous kernel,
+        // but its weight tiles are not -- pull the first ring's worth of them into L2 while
+        // that kernel drains (a plain wait when the launch is not programmatic)
+        int q = 0;
+        const int per_group = P.m_tiles * P.ksplit;
+        for (int u = blockIdx.x; u < P.n_units && q < S; u += gridDim.x) {
+            int g = u / per_group;
+            const int rem = u % per_group, mt = rem / P.ksplit, ks = rem % P.ksplit;
+            if (P.serpentine) g = P.n_groups - 1 - g;
+            const int sb0 = (ks * P.n_sb) / P.ksplit, nk = ((ks + 1) * P.n_sb) / P.ksplit - sb0;
+            const int rowA1 = g * P.rows_per_group + mt * P.a_tile_stride;
+            for (int i = 0; i < nk && q < S; ++i, ++q) {
+                const int kb = sb0 * kGemmKps + i * kGemmKps;
+                if (P.a_4d) tma_prefetch_4d(&P.tmA, 0, rowA1, 0, kb);
+                else tma_prefetch_3d(&P.tmA, 0, rowA1, kb);
+            }
+        }
+    }
     if (!run_ahead) griddep_wait();
     task_begin(ctx, 32);
 
