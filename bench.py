@@ -50,7 +50,9 @@ def parse():
     ap.add_argument("--kv-len", type=int, default=None, help="override the KV length")
     ap.add_argument("--stages", type=int, default=2)
     ap.add_argument("--micro", type=int, default=None, help="sequences per microbatch")
-    ap.add_argument("--split", default="auto", help="'auto' (balancer) or comma list of SMs")
+    ap.add_argument("--split", default="auto",
+                    help="'auto' (balancer, checked on its 4 best picks), 'sweep' (every legal "
+                         "split as a full run) or a comma list of SMs")
     ap.add_argument("--cut", default="macro", choices=["layer", "macro"],
                     help="macro: full-attention decode alone on stage A, everything else on B")
     ap.add_argument("--no-temporal", action="store_true")
@@ -80,8 +82,15 @@ def job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
 
 
 def workload(args):
+    """A named workload: synth.WORKLOADS, 'skew' (Zipf routing, block slot map) or
+    'sweep_b<N>' (N sequences, ragged KV lengths in [512, 16384])."""
     from intra_spatial_pipelining_gb300 import synth
-    wl = synth.WORKLOADS[args.workload]
+    if args.workload == "skew":
+        wl = synth.skew_workload()
+    elif args.workload.startswith("sweep_b"):
+        wl = synth.sweep_workload(int(args.workload[len("sweep_b"):]))
+    else:
+        wl = synth.WORKLOADS[args.workload]
     kw = {}
     if args.layers:
         kw["n_layers"] = args.layers
@@ -308,21 +317,22 @@ def run_sgp(args, rank, world, local_rank):
     micro = args.micro or (T // max(1, wl.microbatches))
     opts = None
     opts_kw = {}
-    if args.cut == "macro":
+    if args.cut == "macro" and n_stages == 2:   # 3 stages use A | o-proj+router | experts
         full = [1] * sgp.N_OPS
         full[sgp.OPS.index("attention")] = 0
         opts_kw = {"stage_of_op": [full, [1] * sgp.N_OPS]}
         opts = sgp.make_opts(**opts_kw)
     balance_rows = None
+    sweep_rows = None
+    balancer_pick = None
     if n_stages == 1:
         split = [N]
-    elif args.split == "auto" and n_stages == 2:
+    elif args.split in ("auto", "sweep") and n_stages == 2:
         best, balance_rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro,
                                                       wl.cap, quantum=8, reps=3, opts=opts)
-        # check the model's pick against full pipelined runs of the best few candidates
-        ranked = sorted(balance_rows, key=lambda r: max(r[1], r[2]))[:4]
-        best_t = None
-        for pa, _, _ in ranked:
+        balancer_pick = best
+
+        def full_run_ms(pa):
             p = sgp.sgp_pipeline_create(d, [pa, N - pa], 2, micro, T, wl.cap, opts)
             sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
             sgp.check(sgp.sgp_pipeline_sync(p), "pipeline")
@@ -335,9 +345,20 @@ def run_sgp(args, rank, world, local_rank):
             t1.synchronize()
             sgp.check(sgp.sgp_pipeline_sync(p), "pipeline")
             sgp.sgp_pipeline_destroy(p)
-            ms = t0.elapsed_time(t1) / 3
-            if best_t is None or ms < best_t:
-                best_t, best = ms, pa
+            return t0.elapsed_time(t1) / 3
+
+        if args.split == "sweep":
+            # every legal split as a full pipelined run: the balancer's pick against the best
+            sweep_rows = [(r[0], full_run_ms(r[0])) for r in balance_rows]
+            best = min(sweep_rows, key=lambda r: r[1])[0]
+        else:
+            # check the model's pick against full pipelined runs of the best few candidates
+            ranked = sorted(balance_rows, key=lambda r: max(r[1], r[2]))[:4]
+            best_t = None
+            for pa, _, _ in ranked:
+                ms = full_run_ms(pa)
+                if best_t is None or ms < best_t:
+                    best_t, best = ms, pa
         split = [best, N - best]
     elif args.split == "auto":
         a = max(1, info.sm_alignment)
@@ -456,7 +477,8 @@ def run_sgp(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms_pipe, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": describe(wl, {"mode": f"spatial pipeline, {n_stages} stages",
-                                "cut": args.cut, "sm_split": split,
+                                "cut": args.cut if n_stages == 2 else "A | B1-B4 | B5-B8",
+                                "sm_split": split,
                                 "microbatches": T // micro, "microbatch": micro,
                                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
         "iteration_us": iter_us,
@@ -469,6 +491,10 @@ def run_sgp(args, rank, world, local_rank):
             "pipeline_speedup": ms_temp / ms_pipe},
         "balance": None if balance_rows is None else [
             {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in balance_rows],
+        "split_sweep": None if sweep_rows is None else {
+            "balancer_pick": balancer_pick,
+            "sweep_best": min(sweep_rows, key=lambda r: r[1])[0],
+            "full_run_us": [{"p_A": pa, "us": ms * 1e3} for pa, ms in sweep_rows]},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
