@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kStageA = kGemmKps * 128 * 128;  // A: kGemmKps k-blocks of 128 rows x 64 bf16
+constexpr int kRunAheadL2 = 8;  // weight stages a dense producer pulls into L2 before its wait
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
@@ -201,10 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // Only the producer of a dense problem may run ahead of the previous kernel: it streams
-    // constant weights into the first ring stages before it waits.  A grouped problem's
+    // Only the producer warp of a dense problem may run ahead of the previous kernel: its
+    // elected lane streams constant weights into the ring before it waits.  The decision is
+    // per warp: were the other lanes to wait here, the producer lane would be held at the
+    // warp's reconvergence point until the previous kernel completes.  A grouped problem's
     // token ranges come from the previous kernel, so there everyone waits now.
-    const bool run_ahead = warp == 0 && lane == 0 && P.group_offsets == nullptr;
+    const bool run_ahead = warp == 0 && P.group_offsets == nullptr;
     if (warp == 0 && lane == 0 && !run_ahead) {
         // grouped problem: which tokens a unit covers is known only after the previous kernel,
         // but its weight tiles are not -- pull the first ring's worth of them into L2 while
@@ -229,7 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================= TMA producer =================
-        if (lane == 0) {
+        // One elected lane of the converged warp walks the whole job sequence while the other
+        // lanes wait at the warp barrier below (issue from a lane whose warp-mates sit at the
+        // CTA barrier is measurably slower).
+        if (elect_one()) {
             // a weight tile read again by a later token pass of the same unit (or by a later
             // microbatch) is kept in L2; its last read lets it go first
             const uint64_t pol_keep = policy_evict_last();
@@ -251,8 +257,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int s = it % S;
                         const uint32_t j = it / S;
                         if (!waited && j > 0) {
-                            // every stage holds weights; the previous kernel must be complete
-                            // before the deferred activation loads (and any reuse) go out
+                            // every stage holds weights; pull the weight tiles that come next
+                            // into L2 as well.  The previous kernel must be complete before
+                            // the deferred activation loads (and any reuse) go out.
+                            int q = 0;
+                            for (int u2 = u; u2 < P.n_units && q < kRunAheadL2; u2 += gridDim.x) {
+                                const Unit y = unit_info(P, u2, ctx);
+                                const int rowA2 = y.g * P.rows_per_group + y.mt * P.a_tile_stride;
+                                for (int i2 = u2 == u ? i : 0; i2 < y.nk && q < kRunAheadL2; ++i2, ++q) {
+                                    const int kb2 = y.kb0 + i2 * kGemmKps;
+                                    if (P.a_4d) tma_prefetch_4d(&P.tmA, 0, rowA2, 0, kb2);
+                                    else tma_prefetch_3d(&P.tmA, 0, rowA2, kb2);
+                                }
+                            }
                             griddep_wait();
                             waited = true;
                             for (int q = 0; q < pend_n; ++q)
@@ -304,9 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (void)mbar_wait(&full[s], (issued_par >> s) & 1u, 10000000ull);
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ================= MMA issuer =================
-        if (lane == 0) {
+        // One elected lane issues every MMA and commit (single-thread semantics); see above.
+        if (elect_one()) {
             uint32_t it = 0, job = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < P.n_units && ok; u += gridDim.x) {
@@ -349,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        __syncwarp();
     } else {
         // ================= epilogue: TMEM -> shared -> one bulk store per job =================
         const int q = warp & 3;  // TMEM lane quadrant this warp may read

@@ -58,6 +58,9 @@ constexpr int kGemmKps = 2;
 // memory kTsRows tokens at a time
 constexpr int kGemmMaxN = 256;
 constexpr int kTsRows = 64;
+// shared memory of one projection CTA (ring + staging + barriers): well under the SM's
+// 228 KB, so that a small kernel's CTA fits beside it
+constexpr int kGemmSmemBudget = 200 * 1024;
 
 struct GemmProblem {
     // weights: plain  3-D {64, rows, k-blocks} box {64, 128, 2};

@@ -600,8 +600,10 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     p.nrows = b;
     p.R = grouped ? R : b;
     const int stage_bytes = kGemmKps * (16384 + p.n_cap * 128);
-    // one persistent CTA per SM: ring + accumulator staging within the 227 KB limit
-    p.stages = std::max(2, std::min(8, (232448 - 1280 - std::min(p.n_cap, kTsRows) * 512) /
+    // one persistent CTA per SM: ring + accumulator staging within kGemmSmemBudget, which
+    // leaves room beside it for a CTA of the small kernel before it (a programmatic launch
+    // lets this kernel's CTAs start, and prefetch weights, while that kernel still runs)
+    p.stages = std::max(2, std::min(8, (kGemmSmemBudget - 2304 - std::min(p.n_cap, kTsRows) * 512) /
                                           stage_bytes));
     p.ring_bytes = (int)gemm_tc_ring_bytes(p.n_cap, p.stages);
     p.n_units = gs.n_groups * gs.m_tiles * gs.ksplit;
