@@ -23,7 +23,6 @@ namespace sgp {
 namespace {
 
 constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kStageA = kGemmKps * 128 * 128;  // A: kGemmKps k-blocks of 128 rows x 64 bf16
 constexpr int kRunAheadL2 = 8;  // weight stages a dense producer pulls into L2 before its wait
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
@@ -137,7 +136,7 @@ __device__ __forceinline__ Unit unit_info(const GemmProblem& P, int u, const KCt
     if (P.serpentine) x.g = P.n_groups - 1 - x.g;
     // K segment = stage blocks [sb0, sb1); k-blocks beyond K are zero-filled by the loads
     const int sb0 = (x.ks * P.n_sb) / P.ksplit;
-    x.kb0 = sb0 * kGemmKps;
+    x.kb0 = sb0 * P.kps;
     x.nk = ((x.ks + 1) * P.n_sb) / P.ksplit - sb0;  // stage blocks of this segment
     if (P.group_offsets != nullptr) {
         x.tma_r0 = P.group_offsets[x.g];
@@ -165,8 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = P.stages;
-    const int stage_b = kGemmKps * P.n_cap * 128;  // B: kGemmKps k-blocks of n_cap rows
-    const int stage_bytes = kStageA + stage_b;
+    const int stage_a = P.kps * 128 * 128;      // A: kps k-blocks of 128 rows x 64 bf16
+    const int stage_b = P.kps * P.n_cap * 128;  // B: kps k-blocks of n_cap rows
+    const int stage_bytes = stage_a + stage_b;
     float* Ts = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);  // [n_cap][128]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + P.ring_bytes);
     uint64_t* empty = full + S;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sb0 = (ks * P.n_sb) / P.ksplit, nk = ((ks + 1) * P.n_sb) / P.ksplit - sb0;
             const int rowA1 = g * P.rows_per_group + mt * P.a_tile_stride;
             for (int i = 0; i < nk && q < S; ++i, ++q) {
-                const int kb = sb0 * kGemmKps + i * kGemmKps;
+                const int kb = (sb0 + i) * P.kps;
                 if (P.a_4d) tma_prefetch_4d(&P.tmA, 0, rowA1, 0, kb);
                 else tma_prefetch_3d(&P.tmA, 0, rowA1, kb);
             }
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const Unit y = unit_info(P, u2, ctx);
                                 const int rowA2 = y.g * P.rows_per_group + y.mt * P.a_tile_stride;
                                 for (int i2 = u2 == u ? i : 0; i2 < y.nk && q < kRunAheadL2; ++i2, ++q) {
-                                    const int kb2 = y.kb0 + i2 * kGemmKps;
+                                    const int kb2 = y.kb0 + i2 * P.kps;
                                     if (P.a_4d) tma_prefetch_4d(&P.tmA, 0, rowA2, 0, kb2);
                                     else tma_prefetch_3d(&P.tmA, 0, rowA2, kb2);
                                 }
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             griddep_wait();
                             waited = true;
                             for (int q = 0; q < pend_n; ++q)
-                                tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + kStageA,
+                                tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + stage_a,
                                             &P.tmB, &full[pend_s[q]], 0, pend_row[q], pend_kb[q],
                                             pol_x);
                         }
@@ -287,9 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             continue;
                         }
                         uint8_t* sa = smem + (size_t)s * stage_bytes;
-                        uint8_t* sb = sa + kStageA;
-                        const int kb = x.kb0 + i * kGemmKps;
-                        mbar_arrive_expect_tx(&full[s], (uint32_t)(kStageA + stage_b));
+                        uint8_t* sb = sa + stage_a;
+                        const int kb = x.kb0 + i * P.kps;
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
                         if (P.a_4d)
                             tma_load_4d(sa, &P.tmA, &full[s], 0, rowA1, 0, kb, pol_w);
                         else
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!waited) {
                 griddep_wait();
                 for (int q = 0; q < pend_n; ++q)
-                    tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + kStageA, &P.tmB,
+                    tma_load_3d(smem + (size_t)pend_s[q] * stage_bytes + stage_a, &P.tmB,
                                 &full[pend_s[q]], 0, pend_row[q], pend_kb[q], pol_x);
             }
             if (*(volatile int*)sh_err) {
@@ -354,14 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-                        const uint32_t sb = sa + kStageA;
+                        const uint32_t sb = sa + stage_a;
 #pragma unroll
-                        for (int kk = 0; kk < kGemmKps; ++kk)
+                        for (int kk = 0; kk < kGemmKpsMax; ++kk)
+                            if (kk < P.kps) {
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                tc_mma_bf16(acc, smem_desc_sw128(sa + kk * 16384 + 32 * k),
-                                            smem_desc_sw128(sb + kk * (P.n_cap * 128) + 32 * k),
-                                            idesc, (i > 0 || kk > 0 || k > 0) ? 1u : 0u);
+                                for (int k = 0; k < 4; ++k)
+                                    tc_mma_bf16(acc, smem_desc_sw128(sa + kk * 16384 + 32 * k),
+                                                smem_desc_sw128(sb + kk * (P.n_cap * 128) + 32 * k),
+                                                idesc, (i > 0 || kk > 0 || k > 0) ? 1u : 0u);
+                            }
                         tc_commit(&empty[s]);
                     }
                     if (ok) tc_commit(&tfull[b]);
@@ -657,23 +659,24 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KC
 
 }  // namespace
 
-size_t gemm_tc_ring_bytes(int n_cap, int stages) {
+size_t gemm_tc_ring_bytes(int n_cap, int stages, int kps) {
     // stage ring, then the accumulator staging area [min(n_cap, kTsRows)][128] fp32
-    return (size_t)stages * (kStageA + kGemmKps * n_cap * 128) +
+    return (size_t)stages * kps * (128 * 128 + n_cap * 128) +
            (size_t)std::min(n_cap, kTsRows) * 512;
 }
 
-size_t gemm_tc_smem_bytes(int n_cap, int stages) {
-    return gemm_tc_ring_bytes(n_cap, stages) + 1024 + 256;
+size_t gemm_tc_smem_bytes(int n_cap, int stages, int kps) {
+    return gemm_tc_ring_bytes(n_cap, stages, kps) + 1024 + 256;
 }
 
 int enqueue_gemm_tc(Launcher& L, const GemmProblem& p, const KCtx& c) {
     dim3 grid(std::max(1, std::min(p.n_units, p.grid))), block(kThreads);
-    if ((size_t)p.ring_bytes != gemm_tc_ring_bytes(p.n_cap, p.stages))
+    if ((p.kps != 1 && p.kps != 2) ||
+        (size_t)p.ring_bytes != gemm_tc_ring_bytes(p.n_cap, p.stages, p.kps))
         return (int)cudaErrorInvalidValue;
     void* args[] = {(void*)&p, (void*)&c};
     return L.launch((const void*)gemm_tc_kernel, grid, block,
-                    gemm_tc_smem_bytes(p.n_cap, p.stages), args, true);
+                    gemm_tc_smem_bytes(p.n_cap, p.stages, p.kps), args, true);
 }
 
 int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c) {

@@ -107,8 +107,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __global__ void __launch_bounds__(kRouterWarps * 32, 1)
     router_kernel(const RouterProblem P, const KCtx ctx) {
     griddep_launch();
-    griddep_wait();
-    task_begin(ctx);
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int rb = router_row_bytes(P.H);
     uint8_t* u_s = smem_raw;                                   // [16][rb]
@@ -123,7 +121,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32, 1)
     const int e0 = blockIdx.y * 8;
     const uint4 z4 = make_uint4(0, 0, 0, 0);
 
-    // (0) router rows of experts e0 .. e0+7 (rows past E are zero) and g, by cp.async
+    // (0) router rows of experts e0 .. e0+7 (rows past E are zero) and g, by cp.async: layer
+    // constants, so they are requested before the previous kernel has finished
     if (warp < 8) {
         const int e = e0 + warp;
         uint8_t* dst = w_s + (size_t)warp * rb;
@@ -138,6 +137,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32, 1)
         for (int v = threadIdx.x - 256; v < nv; v += 256) cp_async16(g_s + v * 16, src + v);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+    griddep_wait();
+    task_begin(ctx);
 
     // (1) u = RMSNorm(h; g) of token `warp` (rows past the group are zero)
     constexpr int kRV = 12;  // 16-byte vectors per lane kept in registers (H <= 3072)

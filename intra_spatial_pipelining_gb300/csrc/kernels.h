@@ -51,9 +51,12 @@ struct EpiArgs {
 // Skinny GEMM  D[out_feature][token] = sum_k W[out_feature][k] * X[token][k]  on tcgen05.
 // Work unit = (group, 128-row tile, K segment); the K split is fixed by the shape so the
 // fp32 summation order never depends on the grid or on the token count.
-// Each pipeline stage holds kGemmKps consecutive 64-wide k-blocks: the 128-row weight tile
-// arrives in ONE TMA operation (32 KB) and the stage's activation rows in one more.
-constexpr int kGemmKps = 2;
+// Each pipeline stage holds kps (1 or 2) consecutive 64-wide k-blocks: the 128-row weight
+// tile arrives in ONE TMA operation (16 or 32 KB) and the stage's activation rows in one
+// more.  Two k-blocks per stage when a pass carries few tokens (larger weight boxes stream
+// faster); one when it carries many, so that the ring stays deep although the activation
+// rows dominate the stage.
+constexpr int kGemmKpsMax = 2;
 // tokens per pass go up to 256 (one MMA's N); the accumulator is drained through shared
 // memory kTsRows tokens at a time
 constexpr int kGemmMaxN = 256;
@@ -69,7 +72,8 @@ struct GemmProblem {
     CUtensorMap tmB;        // activations, 3-D {64, rows, k-blocks}, box {64, n_cap, 2}, SW128
     int a_4d;               // 1: SwiGLU (4-D weight map)
     int K, kb_total, ksplit;
-    int n_sb;               // stage blocks = ceil(kb_total / kGemmKps); K segments split these
+    int kps;                // k-blocks per stage (1 or 2)
+    int n_sb;               // stage blocks = ceil(kb_total / kps); K segments split these
     int m_tiles;            // 128-row tiles per group
     int n_groups;
     int rows_per_group;     // weight rows of one group
@@ -185,8 +189,8 @@ int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c);
 int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c);
 
 // shared-memory bytes a tcgen05 GEMM launch needs for (n_cap, stages)
-size_t gemm_tc_ring_bytes(int n_cap, int stages);
-size_t gemm_tc_smem_bytes(int n_cap, int stages);
+size_t gemm_tc_ring_bytes(int n_cap, int stages, int kps);
+size_t gemm_tc_smem_bytes(int n_cap, int stages, int kps);
 // attention chunk length (positions per split-KV work item); fixed, never SM-dependent
 constexpr int kAttnChunk = 1024;
 

@@ -262,8 +262,8 @@ int q_width(const sgp_dims& d) { return d.n_q_heads * d.head_dim; }
 // 152-SM part), at least 4 k-blocks per segment.
 // tiles counts (weight tile, 128-token pass) pairs of the full batch: with many tokens the
 // passes alone give every SM work and no K split is needed.
-int choose_ksplit(int tiles, int kb_total) {
-    const int n_sb = cdiv(kb_total, kGemmKps);  // K segments are made of whole stage blocks
+int choose_ksplit(int tiles, int kb_total, int kps) {
+    const int n_sb = cdiv(kb_total, kps);  // K segments are made of whole stage blocks
     int ks = (int)std::lround(456.0 / tiles);
     ks = std::max(1, std::min(ks, n_sb / 2));
     return std::max(1, ks);
@@ -271,6 +271,7 @@ int choose_ksplit(int tiles, int kb_total) {
 
 struct GemmShape {
     int K, rows_per_group, n_groups, m_tiles, a_tile_stride, a_second_off, ksplit;
+    int kps;  // k-blocks per stage
 };
 // T is the full batch of the call (never the microbatch), so the K split -- and with it every
 // summation order -- is the same for temporal and pipelined execution.
@@ -292,7 +293,11 @@ GemmShape gemm_shape(const sgp_dims& d, int op, int T) {
     }
     const bool grouped = op == SGP_OP_EXPERT_UP || op == SGP_OP_EXPERT_DOWN;
     const int rows = grouped ? cdiv(T * d.top_k, d.n_local_experts) : T;
-    g.ksplit = choose_ksplit(g.n_groups * g.m_tiles * cdiv(std::max(1, rows), kGemmMaxN), g.K / 64);
+    // a pass of 128+ tokens makes the activation rows the larger part of a stage: one k-block
+    // per stage keeps the ring deep (both choices follow the full batch, like the K split)
+    g.kps = rows >= 128 ? 1 : 2;
+    g.ksplit = choose_ksplit(g.n_groups * g.m_tiles * cdiv(std::max(1, rows), kGemmMaxN), g.K / 64,
+                             g.kps);
     return g;
 }
 
@@ -567,13 +572,13 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
         // 128-row tile per k-block.  Rows are bounded so that row + half * I stays in range.
         const uint64_t dims[4] = {64, total_rows - (uint64_t)d.inter, 2, kb_total};
         const uint64_t str[3] = {rowb, (uint64_t)d.inter * rowb, 128};
-        const uint32_t box[4] = {64, 64, 2, (uint32_t)kGemmKps};
+        const uint32_t box[4] = {64, 64, 2, (uint32_t)gs.kps};
         if ((r = make_tmap_nd(&p.tmA, W, 4, dims, str, box)) != SGP_OK) return r;
         p.a_4d = 1;
     } else {
         const uint64_t dims[3] = {64, total_rows, kb_total};
         const uint64_t str[2] = {rowb, 128};
-        const uint32_t box[3] = {64, 128, (uint32_t)kGemmKps};
+        const uint32_t box[3] = {64, 128, (uint32_t)gs.kps};
         if ((r = make_tmap_nd(&p.tmA, W, 3, dims, str, box)) != SGP_OK) return r;
         p.a_4d = 0;
     }
@@ -583,12 +588,13 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
         const bf16* xb = grouped ? X : X + (size_t)row0 * gs.K;
         const uint64_t dims[3] = {64, (uint64_t)(grouped ? xrows : b), kb_total};
         const uint64_t str[2] = {rowb, 128};
-        const uint32_t box[3] = {64, (uint32_t)p.n_cap, (uint32_t)kGemmKps};
+        const uint32_t box[3] = {64, (uint32_t)p.n_cap, (uint32_t)gs.kps};
         if ((r = make_tmap_nd(&p.tmB, xb, 3, dims, str, box)) != SGP_OK) return r;
     }
     p.K = gs.K;
     p.kb_total = gs.K / 64;
-    p.n_sb = cdiv(p.kb_total, kGemmKps);
+    p.kps = gs.kps;
+    p.n_sb = cdiv(p.kb_total, p.kps);
     p.ksplit = gs.ksplit;
     p.m_tiles = gs.m_tiles;
     p.n_groups = gs.n_groups;
@@ -599,13 +605,15 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     p.row0 = row0;
     p.nrows = b;
     p.R = grouped ? R : b;
-    const int stage_bytes = kGemmKps * (16384 + p.n_cap * 128);
+    const int stage_bytes = p.kps * (16384 + p.n_cap * 128);
     // one persistent CTA per SM: ring + accumulator staging within kGemmSmemBudget, which
     // leaves room beside it for a CTA of the small kernel before it (a programmatic launch
-    // lets this kernel's CTAs start, and prefetch weights, while that kernel still runs)
-    p.stages = std::max(2, std::min(8, (kGemmSmemBudget - 2304 - std::min(p.n_cap, kTsRows) * 512) /
+    // lets this kernel's CTAs start, and prefetch weights, while that kernel still runs).
+    // Passes of 128+ tokens take the whole 227 KB instead: there a deep ring matters more.
+    const int budget = p.n_cap >= 128 ? 232448 : kGemmSmemBudget;
+    p.stages = std::max(2, std::min(8, (budget - 2304 - std::min(p.n_cap, kTsRows) * 512) /
                                           stage_bytes));
-    p.ring_bytes = (int)gemm_tc_ring_bytes(p.n_cap, p.stages);
+    p.ring_bytes = (int)gemm_tc_ring_bytes(p.n_cap, p.stages, p.kps);
     p.n_units = gs.n_groups * gs.m_tiles * gs.ksplit;
     p.grid = e.pool_sms;
     p.serpentine = grouped && e.serpentine && (mu & 1);
