@@ -6,11 +6,13 @@
 // of work follows the pool size while every chunk's arithmetic does not.
 //
 // Every warp streams its chunks through a private ring of kASlots shared-memory stages of
-// 128 positions (one 16 KB TMA operation for K and one for V, L2 evict-first): lane 0
+// kAPos = 64 positions (one 8 KB TMA operation for K and one for V, L2 evict-first): lane 0
 // refills a stage as soon as the warp has consumed it, so a warp never waits on another.
 // A warp's arithmetic on a stage takes about as long as the stage's load, so the ring is
-// spent on more warps rather than on deeper per-warp buffering: six warps with one stage
-// each stream faster than three with two (measured on pools of 32 to 152 SMs).
+// spent on more warps rather than on deeper per-warp buffering: twelve warps with one
+// 64-position stage each stream faster on a partial pool than six with 128 positions (at
+// 512 sequences x KV 32768: 100 against 87 GB/s per SM on 56 SMs), and six with one stage
+// faster than three with two.
 // Per stage the warp computes, on warp-level bf16 MMAs with fp32 accumulation,
 //     S^T = K q^T   (M = 16 positions, N = 8 query heads of the KV head, K = 64)
 //     O^T += V^T P^T (M = 16 dims, N = 8 heads, K = 16 positions),
@@ -32,10 +34,11 @@ namespace sgp {
 
 namespace {
 
-constexpr int kAWarps = 6;                   // streaming warps per CTA
+constexpr int kAWarps = 12;                  // streaming warps per CTA
 constexpr int kASlots = 1;                   // ring stages per warp
-constexpr int kAPos = 128;                   // positions per stage
-constexpr int kAHalf = kAPos * 128;          // K (or V) bytes of a stage: 16 KB
+constexpr int kAPos = kAttnStagePos;         // positions per stage (64)
+constexpr int kAPT = kAPos / 16;             // 16-position MMA tiles per stage
+constexpr int kAHalf = kAPos * 128;          // K (or V) bytes of a stage: 8 KB
 constexpr int kAStage = 2 * kAHalf;          // K then V
 constexpr int kAMaxRows = 512;               // sequences per launch (prefix table size)
 constexpr int kAPerLane = kAMaxRows / 32;    // sequences per lane of the prefix scan
@@ -300,9 +303,9 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
         }
 
         // ---- S^T = K q^T: 8 position tiles x NT head tiles ----
-        float s[8][NT][4];
+        float s[kAPT][NT][4];
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
+        for (int mt = 0; mt < kAPT; ++mt) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) s[mt][nt][0] = s[mt][nt][1] = s[mt][nt][2] = s[mt][nt][3] = 0.f;
             const int r = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
         for (int nt = 0; nt < NT; ++nt) {
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
+            for (int mt = 0; mt < kAPT; ++mt) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     float v0 = s[mt][nt][2 * hf] * P.scale_log2;
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
             m_run[nt][1] = n1;
             float r0 = 0.f, r1 = 0.f;
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
+            for (int mt = 0; mt < kAPT; ++mt) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const float e0 = exp2f(s[mt][nt][2 * hf] - n0);
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
         }
         // ---- O^T += V^T P^T: 8 position steps of 16 x 4 dim tiles x NT head tiles ----
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
+        for (int ks = 0; ks < kAPT; ++ks) {
             uint32_t b0[NT], b1[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {

@@ -193,5 +193,6 @@ size_t gemm_tc_ring_bytes(int n_cap, int stages, int kps);
 size_t gemm_tc_smem_bytes(int n_cap, int stages, int kps);
 // attention chunk length (positions per split-KV work item); fixed, never SM-dependent
 constexpr int kAttnChunk = 1024;
+constexpr int kAttnStagePos = 64;  // KV positions per attention stage (the K / V TMA box height)
 
 }  // namespace sgp

@@ -666,8 +666,8 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
             AttnProblem p;
             memset(&p, 0, sizeof(p));
             const uint64_t rows = (uint64_t)e.T * d.n_kv_heads * e.layer->kv_cap;
-            if ((r = make_tmap(&p.tmK, e.layer->k_cache, 64, rows, 64, 128)) != SGP_OK) return r;
-            if ((r = make_tmap(&p.tmV, e.layer->v_cache, 64, rows, 64, 128)) != SGP_OK) return r;
+            if ((r = make_tmap(&p.tmK, e.layer->k_cache, 64, rows, 64, kAttnStagePos)) != SGP_OK) return r;
+            if ((r = make_tmap(&p.tmV, e.layer->v_cache, 64, rows, 64, kAttnStagePos)) != SGP_OK) return r;
             p.q = e.ws.at<bf16>(Lay.q);
             p.kv_len = e.kv_len;
             p.o = e.ws.at<bf16>(Lay.o);
