@@ -100,11 +100,12 @@ def test_gptoss_layer_vs_oracle():
 
 @pytest.mark.parametrize("window", [0, 16, 200])
 def test_ragged_lengths_and_windows(window):
-    """Sequence lengths at MMA-tile, stage (128) and chunk (1024) edges."""
-    wl = synth.WORKLOADS["tiny"].with_(n_tokens=8, kv_len=2400, kv_cap=2400)
+    """Sequence lengths at MMA-tile (16), stage (64), half-chunk (512) and chunk (1024) edges."""
+    wl = synth.WORKLOADS["tiny"].with_(n_tokens=12, kv_len=2400, kv_cap=2400)
     for a in range(20):
         inp = H.make_inputs(wl, 3, [a])
-        inp.kv_len.copy_(torch.tensor([1, 17, 128, 129, 1023, 1024, 1025, 2300], dtype=torch.int32))
+        inp.kv_len.copy_(torch.tensor([1, 17, 63, 64, 65, 511, 512, 513, 1023, 1024, 1025, 2300],
+                                      dtype=torch.int32))
         # override the layer's window
         lay = inp.sgp_layers()[0]
         lay.window = window

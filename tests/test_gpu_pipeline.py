@@ -96,16 +96,22 @@ def _routing_sets_per_layer(tki, L, k, rows=None):
 def test_stack_three_layers_vs_oracle():
     """Three GPT-OSS-shaped layers (sliding, full, sliding; KV 1024), every sequence, against
     the fp64 oracle: exercises the next layer's RMSNorm produced inside the combine, in
-    temporal and pipelined execution."""
+    temporal and pipelined execution.  The chained output is compared end to end; routing is
+    bit-exact where the two sides see the same input -- layer 0 here, and every layer in the
+    teacher-forced pass, whose oracle starts from the GPU's own input to the layer (a chained
+    layer's input already differs from the oracle's by bf16 rounding, which a 1e-3 logit
+    margin does not cover)."""
     wl = synth.WORKLOADS["gptoss_36l"].with_(n_layers=3, kv_len=1024)
     inp, ref = H.make_stack_inputs_with_margin(wl, 12)
     d = H.dims(wl.shape)
     k = wl.shape.top_k
     out_t, tki, tkw, _ = _temporal(inp, d)
     H.assert_close("x_out (temporal)", out_t, ref["x_out"])
-    assert _routing_sets_per_layer(tki, 3, k) == [H.routing_sets(ref["idx"][l]) for l in range(3)]
+    assert _routing_sets_per_layer(tki, 3, k)[0] == H.routing_sets(ref["idx"][0])
     got = _pipelined(inp, d, 2, 32)
     assert torch.equal(got[0], out_t)
+    inp.reset_caches()
+    _teacher_forced_check(inp, list(range(wl.n_tokens)))
 
 
 def _teacher_forced_check(inp, seqs, n_stages=2, micro=None, min_checked=0.9):
