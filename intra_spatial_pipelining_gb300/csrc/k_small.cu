@@ -404,26 +404,36 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const DispatchProblem P, 
 }
 
 // ---------------------------------------------------------------------------------------
-// Combine: out[t] = bf16(h[t] + sum_j w[t][j] * Y[pair_pos[t k + j]]), j in pick order
+// Combine: out[t] = bf16(h[t] + sum_j w[t][j] * Y[pair_pos[t k + j]]), j in pick order.
+// With a K-split expert-down projection, Y[r] is the sum of its K segments, formed here in
+// segment order (the same fp32 operations the finishing pass would do), so that pass is not
+// launched.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, const KCtx ctx) {
+constexpr int kCombThreads = 512;
+template <int KP>  // picks per token, at most
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(const CombineProblem P, const KCtx ctx) {
     griddep_launch();
     griddep_wait();
     task_begin(ctx);
-    constexpr int kKeep = 8;  // 4-element vectors per thread kept for the fused RMSNorm
-    __shared__ float red[8];
+    constexpr int kKeep = 4;  // 4-element vectors per thread kept for the fused RMSNorm
+    __shared__ float red[kCombThreads / 32];
     const int tl = blockIdx.x;
     const int row = P.row0 + tl;
     const int n4 = P.H >> 2;
-    int pos[8];
-    float w[8];
-    for (int j = 0; j < P.k; ++j) {
-        pos[j] = P.pair_pos[tl * P.k + j];
-        w[j] = P.wts[tl * P.k + j];
-        if (pos[j] < 0 || pos[j] >= P.nrows * P.k) {
-            if (threadIdx.x == 0) report(ctx, ST_BOUNDS, (uint32_t)pos[j]);
-            pos[j] = 0;
-            w[j] = 0.f;
+    int pos[KP];
+    float w[KP];
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+        pos[j] = 0;
+        w[j] = 0.f;
+        if (j < P.k) {
+            pos[j] = P.pair_pos[tl * P.k + j];
+            w[j] = P.wts[tl * P.k + j];
+            if (pos[j] < 0 || pos[j] >= P.nrows * P.k) {
+                if (threadIdx.x == 0) report(ctx, ST_BOUNDS, (uint32_t)pos[j]);
+                pos[j] = 0;
+                w[j] = 0.f;
+            }
         }
     }
     const uint2* h = reinterpret_cast<const uint2*>(P.h + (size_t)row * P.H);
@@ -433,14 +443,48 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, co
 #pragma unroll
     for (int i = 0; i < kKeep; ++i) keep[i] = make_uint2(0, 0);
     int i = 0;
-    for (int v = threadIdx.x; v < n4; v += 256, ++i) {
+    for (int v = threadIdx.x; v < n4; v += kCombThreads, ++i) {
+        float4 y[KP];
+#pragma unroll
+        for (int j = 0; j < KP; ++j) y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (P.ksplit <= 1) {
+#pragma unroll
+            for (int j = 0; j < KP; ++j)
+                if (j < P.k) y[j] = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
+        } else {
+            // K segments s of pick j live at ((tile * ksplit + s) * R + row) * 128 + col
+            const size_t sstride = (size_t)P.R * 128;
+            const float* base = P.Y + (size_t)((4 * v) >> 7) * P.ksplit * sstride + ((4 * v) & 127);
+            for (int s0 = 0; s0 < P.ksplit; s0 += 2) {
+                float4 ld[KP][2];
+#pragma unroll
+                for (int j = 0; j < KP; ++j)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (j < P.k && s0 + u < P.ksplit)
+                            ld[j][u] = __ldcg(reinterpret_cast<const float4*>(
+                                base + (size_t)(s0 + u) * sstride + (size_t)pos[j] * 128));
+#pragma unroll
+                for (int j = 0; j < KP; ++j)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (j < P.k && s0 + u < P.ksplit) {
+                            y[j].x += ld[j][u].x;
+                            y[j].y += ld[j][u].y;
+                            y[j].z += ld[j][u].z;
+                            y[j].w += ld[j][u].w;
+                        }
+            }
+        }
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < P.k; ++j) {
-            const float4 y = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
-            acc[0] = fmaf(w[j], y.x, acc[0]);
-            acc[1] = fmaf(w[j], y.y, acc[1]);
-            acc[2] = fmaf(w[j], y.z, acc[2]);
-            acc[3] = fmaf(w[j], y.w, acc[3]);
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+            if (j < P.k) {
+                acc[0] = fmaf(w[j], y[j].x, acc[0]);
+                acc[1] = fmaf(w[j], y[j].y, acc[1]);
+                acc[2] = fmaf(w[j], y[j].z, acc[2]);
+                acc[3] = fmaf(w[j], y[j].w, acc[3]);
+            }
         }
         const uint2 hv = h[v];
         const float2 h01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.x));
@@ -468,13 +512,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineProblem P, co
         __syncthreads();
         float tot = 0.f;
 #pragma unroll
-        for (int wq = 0; wq < 8; ++wq) tot += red[wq];
+        for (int wq = 0; wq < kCombThreads / 32; ++wq) tot += red[wq];
         const float inv = rsqrtf(tot / (float)P.H + P.eps);
         const uint2* g = reinterpret_cast<const uint2*>(P.g_next);
         uint2* a = reinterpret_cast<uint2*>(P.a_next + (size_t)row * P.H);
 #pragma unroll
         for (int q = 0; q < kKeep; ++q) {
-            const int v = threadIdx.x + q * 256;
+            const int v = threadIdx.x + q * kCombThreads;
             if (v < n4) {
                 const uint2 gv = g[v];
                 const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&keep[q].x));
@@ -525,7 +569,10 @@ int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c) {
 
 int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c) {
     void* args[] = {(void*)&p, (void*)&c};
-    return L.launch((const void*)combine_kernel, dim3(p.nrows), dim3(256), 0, args);
+    if (p.k < 1 || p.k > 8 || (p.H & 3) || (p.a_next != nullptr && p.H > 8192))
+        return (int)cudaErrorInvalidValue;
+    const void* f = p.k <= 4 ? (const void*)combine_kernel<4> : (const void*)combine_kernel<8>;
+    return L.launch(f, dim3(p.nrows), dim3(kCombThreads), 0, args);
 }
 
 }  // namespace sgp

@@ -165,7 +165,10 @@ struct DispatchProblem {
 
 struct CombineProblem {
     const bf16* h;          // [T][H] batch-wide
-    const float* Y;         // [nrows * k][H]
+    // expert-down output: ksplit == 1: rows [nrows * k][H]; ksplit > 1: the projection's K
+    // segments, [H / 128][ksplit][R][128] (summed here in segment order)
+    const float* Y;
+    int ksplit, R;
     const float* wts;       // [nrows][k]
     const int* pair_pos;    // [nrows * k]
     bf16* out;              // [T][H] batch-wide

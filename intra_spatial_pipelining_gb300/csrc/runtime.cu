@@ -625,6 +625,8 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
         p.epi = epi;
         return enqueue_gemm_tc(L, p, c);
     }
+    // the expert-down K segments are summed by the combine (it reads each routed row once)
+    if (op == SGP_OP_EXPERT_DOWN) return enqueue_gemm_tc(L, p, c);
     // the flag check belongs to the first launch, the publish to the last
     KCtx c1 = c, c2 = c;
     c1.post_flag = nullptr;
@@ -720,7 +722,12 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
             return enqueue_dispatch(L, p, c);
         }
         case SGP_OP_COMBINE: {
-            CombineProblem p{e.ws.at<bf16>(Lay.h), e.ws.mu<float>(mu, Lay.ybuf),
+            // a K-split tensor-core expert-down projection leaves its segments in the partial
+            // buffer (no finishing pass); otherwise its rows are in ybuf
+            const int ks = e.tc_expert ? gemm_shape(d, SGP_OP_EXPERT_DOWN, e.T).ksplit : 1;
+            CombineProblem p{e.ws.at<bf16>(Lay.h),
+                             ks > 1 ? e.ws.mu<float>(mu, Lay.gemm_part) : e.ws.mu<float>(mu, Lay.ybuf),
+                             ks, b * d.top_k,
                              e.ws.mu<float>(mu, Lay.wts), e.ws.mu<int>(mu, Lay.pair_pos),
                              e.x_out, row0, b, d.top_k, d.hidden,
                              e.next ? (const bf16*)e.next->g_attn : nullptr,
@@ -886,7 +893,27 @@ static int temporal_common(const sgp_dims* d, const sgp_layer* layers, int n_lay
             return r;
         if ((r = cp(dump->pair_pos, w.mu<int>(0, Lay.pair_pos), R * 4))) return r;
         if ((r = cp(dump->z, w.mu<bf16>(0, Lay.zbuf), R * d->inter * 2))) return r;
-        if ((r = cp(dump->y, w.mu<float>(0, Lay.ybuf), R * H * 4))) return r;
+        const GemmShape gd = gemm_shape(*d, SGP_OP_EXPERT_DOWN, T);
+        if (dump->y && use_tc_expert(*d, T) && gd.ksplit > 1) {
+            // the combine summed the expert-down K segments itself; form y for the dump
+            FinishProblem f;
+            memset(&f, 0, sizeof(f));
+            f.partial = w.mu<float>(0, Lay.gemm_part);
+            f.ksplit = gd.ksplit;
+            f.m_tiles = gd.m_tiles;
+            f.R = (int)R;
+            f.rows = (int)R;
+            f.epi.mode = EPI_F32;
+            f.epi.n_out = (int)H;
+            f.epi.ld = (int)H;
+            f.epi.out_f32 = (float*)dump->y;
+            StreamLauncher L(s);
+            KCtx c = plain_ctx(w.status(), kDefaultTimeout, (uint32_t)SGP_OP_EXPERT_DOWN << 24);
+            const int e2 = enqueue_gemm_finish(L, f, c);
+            if (e2 != 0) return fail_cuda((cudaError_t)e2, "dump of y");
+        } else if ((r = cp(dump->y, w.mu<float>(0, Lay.ybuf), R * H * 4))) {
+            return r;
+        }
     }
     return SGP_OK;
 }
