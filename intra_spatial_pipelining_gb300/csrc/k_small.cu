@@ -60,25 +60,32 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const NormProblem P, const
 //       by 16 bytes so ldmatrix rows fall on distinct banks) and, from the first expert
 //       group, to global memory;
 //   (2) logits z = u W_r^T on warp-level bf16 tensor-core MMAs with fp32 accumulation
-//       (M = 16 tokens, N = 8 experts); the 16 warps split K and their partial tiles are
-//       added in warp order;
+//       (M = 16 tokens, N = 8 experts, two N tiles per CTA); the 16 warps split K and their
+//       partial tiles are added in warp order;
 //   (3) the last CTA of a token group selects each token's top-k (descending logit, ties to
 //       the lower index, a NaN logit ranks below every number) and the softmax over the
 //       selected logits, one warp per token.
 // ---------------------------------------------------------------------------------------
 constexpr int kRouterTok = 16;
 constexpr int kRouterWarps = 16;
+// experts per CTA: 16 (two 8-wide MMA tiles) where the rows fit in shared memory, else 8
 
 __host__ __device__ inline int router_row_bytes(int H) { return H * 2 + 16; }
 // u rows, router rows and g (the first two reused for the logit rows of the top-k), then the
 // MMA partials
-__host__ __device__ inline size_t router_rows_bytes(int H, int E) {
-    const size_t rows = (size_t)(kRouterTok + 8 + 1) * router_row_bytes(H);
+__host__ __device__ inline size_t router_rows_bytes(int H, int E, int NE) {
+    const size_t rows = (size_t)(kRouterTok + NE + 1) * router_row_bytes(H);
     const size_t logit_rows = (size_t)kRouterWarps * E * sizeof(float);
     return rows > logit_rows ? rows : logit_rows;
 }
-inline size_t router_smem_bytes(int H, int E) {
-    return router_rows_bytes(H, E) + (size_t)kRouterWarps * 16 * 8 * sizeof(float);
+inline size_t router_smem_bytes(int H, int E, int NE) {
+    return router_rows_bytes(H, E, NE) + (size_t)kRouterWarps * 16 * NE * sizeof(float);
+}
+// experts per CTA: 16 for many tokens (half the CTAs, half the repeated RMSNorm work) when
+// that fits the opt-in shared memory (with margin); 8 for few tokens (more CTAs in flight).
+// Both give the same logits: every expert's dot product is split over the warps alike.
+inline int router_experts_per_cta(int H, int E, int nrows) {
+    return nrows >= 128 && router_smem_bytes(H, E, 16) <= 220 * 1024 ? 16 : 8;
 }
 
 __device__ __forceinline__ void ldsm_x4_r(uint32_t addr, uint32_t (&r)[4]) {
@@ -104,26 +111,29 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                  : "memory");
 }
 
+template <int NE>
 __global__ void __launch_bounds__(kRouterWarps * 32, 1)
     router_kernel(const RouterProblem P, const KCtx ctx) {
+    constexpr int kRouterExp = NE;
     griddep_launch();
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int rb = router_row_bytes(P.H);
     uint8_t* u_s = smem_raw;                                   // [16][rb]
-    uint8_t* w_s = u_s + (size_t)kRouterTok * rb;              // [8][rb]
-    uint8_t* g_s = w_s + (size_t)8 * rb;                       // [rb]
-    float* red = reinterpret_cast<float*>(smem_raw + router_rows_bytes(P.H, P.E));  // [16][16][8]
+    uint8_t* w_s = u_s + (size_t)kRouterTok * rb;              // [kRouterExp][rb]
+    uint8_t* g_s = w_s + (size_t)kRouterExp * rb;              // [rb]
+    float* red = reinterpret_cast<float*>(smem_raw + router_rows_bytes(P.H, P.E, NE));  // [16][16][NE]
     __shared__ int sh_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tg = blockIdx.x;
     const int nv = P.H >> 3;
     const int ntok = min(kRouterTok, P.nrows - tg * kRouterTok);
-    const int e0 = blockIdx.y * 8;
+    const int e0 = blockIdx.y * kRouterExp;
     const uint4 z4 = make_uint4(0, 0, 0, 0);
 
-    // (0) router rows of experts e0 .. e0+7 (rows past E are zero) and g, by cp.async: layer
+    // (0) router rows of experts e0 .. e0+NE-1 (rows past E are zero) and g, by cp.async: layer
     // constants, so they are requested before the previous kernel has finished
-    if (warp < 8) {
+    static_assert(NE == 8 || NE == 16, "one or two 8-wide tiles");
+    if (warp < NE) {
         const int e = e0 + warp;
         uint8_t* dst = w_s + (size_t)warp * rb;
         if (e < P.E) {
@@ -132,9 +142,10 @@ __global__ void __launch_bounds__(kRouterWarps * 32, 1)
         } else {
             for (int v = lane; v < nv; v += 32) *reinterpret_cast<uint4*>(dst + v * 16) = z4;
         }
-    } else {
-        const uint4* src = reinterpret_cast<const uint4*>(P.g);
-        for (int v = threadIdx.x - 256; v < nv; v += 256) cp_async16(g_s + v * 16, src + v);
+    }
+    {
+        const uint4* gsrc = reinterpret_cast<const uint4*>(P.g);
+        for (int v = threadIdx.x; v < nv; v += kRouterWarps * 32) cp_async16(g_s + v * 16, gsrc + v);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     griddep_wait();
@@ -213,30 +224,39 @@ __global__ void __launch_bounds__(kRouterWarps * 32, 1)
     {
         const int KS = P.H >> 4;
         const int k0 = warp * KS / kRouterWarps, k1 = (warp + 1) * KS / kRouterWarps;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        constexpr int NTL = NE / 8;  // 8-wide expert tiles
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const uint32_t ua = smem_u32(u_s) + (uint32_t)((lane & 15) * rb + (lane >> 4) * 16);
         const uint32_t wa = smem_u32(w_s) + (uint32_t)((lane & 7) * rb + ((lane >> 3) & 1) * 16);
         for (int kk = k0; kk < k1; ++kk) {
             uint32_t a[4], b0, b1;
             ldsm_x4_r(ua + kk * 32, a);
-            ldsm_x2_r(wa + kk * 32, b0, b1);
-            mma_bf16_16816(acc, a, b0, b1);
+            ldsm_x2_r(wa + kk * 32, b0, b1);  // experts e0 .. e0+7
+            mma_bf16_16816(acc[0], a, b0, b1);
+            if constexpr (NTL == 2) {
+                uint32_t b2, b3;
+                ldsm_x2_r(wa + (uint32_t)(8 * rb) + kk * 32, b2, b3);  // experts e0+8 .. e0+15
+                mma_bf16_16816(acc[1], a, b2, b3);
+            }
         }
-        // partial tile: rows (tokens) lane/4 and lane/4 + 8, columns (experts) 2(lane%4), +1
-        float* rw = red + warp * 128;
+        // partial tiles: rows (tokens) lane/4 and lane/4 + 8, columns (experts) 2(lane%4), +1
+        float* rw = red + warp * (16 * kRouterExp);
         const int rr = lane >> 2, cc = 2 * (lane & 3);
-        rw[rr * 8 + cc] = acc[0];
-        rw[rr * 8 + cc + 1] = acc[1];
-        rw[(rr + 8) * 8 + cc] = acc[2];
-        rw[(rr + 8) * 8 + cc + 1] = acc[3];
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt) {
+            rw[rr * kRouterExp + nt * 8 + cc] = acc[nt][0];
+            rw[rr * kRouterExp + nt * 8 + cc + 1] = acc[nt][1];
+            rw[(rr + 8) * kRouterExp + nt * 8 + cc] = acc[nt][2];
+            rw[(rr + 8) * kRouterExp + nt * 8 + cc + 1] = acc[nt][3];
+        }
     }
     __syncthreads();
-    if (threadIdx.x < 128) {
-        const int r = threadIdx.x >> 3, c = threadIdx.x & 7, e = e0 + c;
+    if (threadIdx.x < 16 * kRouterExp) {
+        const int r = threadIdx.x / kRouterExp, c = threadIdx.x % kRouterExp, e = e0 + c;
         if (r < ntok && e < P.E) {
             float z = 0.f;
 #pragma unroll
-            for (int w = 0; w < kRouterWarps; ++w) z += red[w * 128 + r * 8 + c];
+            for (int w = 0; w < kRouterWarps; ++w) z += red[w * (16 * kRouterExp) + r * kRouterExp + c];
             P.logits[(size_t)(tg * kRouterTok + r) * P.E + e] = z + (P.bias ? P.bias[e] : 0.f);
         }
     }
@@ -410,12 +430,16 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const DispatchProblem P, 
 // launched.
 // ---------------------------------------------------------------------------------------
 constexpr int kCombThreads = 512;
-template <int KP>  // picks per token, at most
-__global__ void __launch_bounds__(kCombThreads) combine_kernel(const CombineProblem P, const KCtx ctx) {
+// KP: picks per token, at most.  WIDE: every pick's segment loads in flight together (few
+// tokens, latency-bound); otherwise one pick at a time in fewer registers, so that two CTAs
+// share an SM (many tokens).  Both perform the same fp32 operations in the same order.
+template <int KP, bool WIDE>
+__global__ void __launch_bounds__(kCombThreads, WIDE ? 1 : 2)
+    combine_kernel(const CombineProblem P, const KCtx ctx) {
     griddep_launch();
     griddep_wait();
     task_begin(ctx);
-    constexpr int kKeep = 4;  // 4-element vectors per thread kept for the fused RMSNorm
+    constexpr int kKeep = 2;  // 4-element vectors per thread kept for the fused RMSNorm (H <= 4096)
     __shared__ float red[kCombThreads / 32];
     const int tl = blockIdx.x;
     const int row = P.row0 + tl;
@@ -444,46 +468,74 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(const CombineProb
     for (int i = 0; i < kKeep; ++i) keep[i] = make_uint2(0, 0);
     int i = 0;
     for (int v = threadIdx.x; v < n4; v += kCombThreads, ++i) {
-        float4 y[KP];
-#pragma unroll
-        for (int j = 0; j < KP; ++j) y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (P.ksplit <= 1) {
-#pragma unroll
-            for (int j = 0; j < KP; ++j)
-                if (j < P.k) y[j] = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
-        } else {
-            // K segments s of pick j live at ((tile * ksplit + s) * R + row) * 128 + col
-            const size_t sstride = (size_t)P.R * 128;
-            const float* base = P.Y + (size_t)((4 * v) >> 7) * P.ksplit * sstride + ((4 * v) & 127);
-            for (int s0 = 0; s0 < P.ksplit; s0 += 2) {
-                float4 ld[KP][2];
-#pragma unroll
-                for (int j = 0; j < KP; ++j)
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        if (j < P.k && s0 + u < P.ksplit)
-                            ld[j][u] = __ldcg(reinterpret_cast<const float4*>(
-                                base + (size_t)(s0 + u) * sstride + (size_t)pos[j] * 128));
-#pragma unroll
-                for (int j = 0; j < KP; ++j)
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        if (j < P.k && s0 + u < P.ksplit) {
-                            y[j].x += ld[j][u].x;
-                            y[j].y += ld[j][u].y;
-                            y[j].z += ld[j][u].z;
-                            y[j].w += ld[j][u].w;
-                        }
-            }
-        }
+        // y_j = sum of pick j's K segments in segment order, then acc += w_j y_j in pick order
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const size_t sstride = (size_t)P.R * 128;
+        // K segments s of a row live at ((tile * ksplit + s) * R + row) * 128 + col
+        const float* base = P.Y + (size_t)((4 * v) >> 7) * P.ksplit * sstride + ((4 * v) & 127);
+        if constexpr (WIDE) {
+            float4 y[KP];
 #pragma unroll
-        for (int j = 0; j < KP; ++j) {
-            if (j < P.k) {
-                acc[0] = fmaf(w[j], y[j].x, acc[0]);
-                acc[1] = fmaf(w[j], y[j].y, acc[1]);
-                acc[2] = fmaf(w[j], y[j].z, acc[2]);
-                acc[3] = fmaf(w[j], y[j].w, acc[3]);
+            for (int j = 0; j < KP; ++j) y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (P.ksplit <= 1) {
+#pragma unroll
+                for (int j = 0; j < KP; ++j)
+                    if (j < P.k) y[j] = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
+            } else {
+                for (int s0 = 0; s0 < P.ksplit; s0 += 2) {
+                    float4 ld[KP][2];
+#pragma unroll
+                    for (int j = 0; j < KP; ++j)
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            if (j < P.k && s0 + u < P.ksplit)
+                                ld[j][u] = __ldcg(reinterpret_cast<const float4*>(
+                                    base + (size_t)(s0 + u) * sstride + (size_t)pos[j] * 128));
+#pragma unroll
+                    for (int j = 0; j < KP; ++j)
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            if (j < P.k && s0 + u < P.ksplit) {
+                                y[j].x += ld[j][u].x;
+                                y[j].y += ld[j][u].y;
+                                y[j].z += ld[j][u].z;
+                                y[j].w += ld[j][u].w;
+                            }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < KP; ++j) {
+                if (j < P.k) {
+                    acc[0] = fmaf(w[j], y[j].x, acc[0]);
+                    acc[1] = fmaf(w[j], y[j].y, acc[1]);
+                    acc[2] = fmaf(w[j], y[j].z, acc[2]);
+                    acc[3] = fmaf(w[j], y[j].w, acc[3]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < KP; ++j) {
+                if (j < P.k) {
+                    float4 yj;
+                    if (P.ksplit <= 1) {
+                        yj = *reinterpret_cast<const float4*>(P.Y + (size_t)pos[j] * P.H + 4 * v);
+                    } else {
+                        yj = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+                        for (int sg = 0; sg < P.ksplit; ++sg) {
+                            const float4 l = __ldcg(reinterpret_cast<const float4*>(
+                                base + (size_t)sg * sstride + (size_t)pos[j] * 128));
+                            yj.x += l.x;
+                            yj.y += l.y;
+                            yj.z += l.z;
+                            yj.w += l.w;
+                        }
+                    }
+                    acc[0] = fmaf(w[j], yj.x, acc[0]);
+                    acc[1] = fmaf(w[j], yj.y, acc[1]);
+                    acc[2] = fmaf(w[j], yj.z, acc[2]);
+                    acc[3] = fmaf(w[j], yj.w, acc[3]);
+                }
             }
         }
         const uint2 hv = h[v];
@@ -554,9 +606,11 @@ int enqueue_rmsnorm(Launcher& L, const NormProblem& p, const KCtx& c) {
 
 int enqueue_router(Launcher& L, const RouterProblem& p, const KCtx& c) {
     void* args[] = {(void*)&p, (void*)&c};
-    dim3 grid((p.nrows + kRouterTok - 1) / kRouterTok, (p.E + 7) / 8);
-    return L.launch((const void*)router_kernel, grid, dim3(kRouterWarps * 32),
-                    router_smem_bytes(p.H, p.E), args);
+    const int ne = router_experts_per_cta(p.H, p.E, p.nrows);
+    dim3 grid((p.nrows + kRouterTok - 1) / kRouterTok, (p.E + ne - 1) / ne);
+    return L.launch(ne == 16 ? (const void*)router_kernel<16> : (const void*)router_kernel<8>, grid,
+                    dim3(kRouterWarps * 32),
+                    router_smem_bytes(p.H, p.E, ne), args);
 }
 
 int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c) {
@@ -569,9 +623,11 @@ int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c) {
 
 int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c) {
     void* args[] = {(void*)&p, (void*)&c};
-    if (p.k < 1 || p.k > 8 || (p.H & 3) || (p.a_next != nullptr && p.H > 8192))
+    if (p.k < 1 || p.k > 8 || (p.H & 3) || (p.a_next != nullptr && p.H > 4 * 2 * kCombThreads))
         return (int)cudaErrorInvalidValue;
-    const void* f = p.k <= 4 ? (const void*)combine_kernel<4> : (const void*)combine_kernel<8>;
+    const bool wide = p.nrows <= 96;  // few tokens: load latency, not occupancy, is the limit
+    const void* f = p.k <= 4 ? (wide ? (const void*)combine_kernel<4, true> : (const void*)combine_kernel<4, false>)
+                             : (wide ? (const void*)combine_kernel<8, true> : (const void*)combine_kernel<8, false>);
     return L.launch(f, dim3(p.nrows), dim3(kCombThreads), 0, args);
 }
 
@@ -642,15 +698,15 @@ extern "C" int sgp_router_topk_noalloc(const sgp_dims* d, const void* h, const v
     memset(&c, 0, sizeof(c));
     c.status = status;
     c.timeout_ns = 2000000000ull;
-    const size_t smem = router_smem_bytes(d->hidden, d->n_experts);
+    const int ne = router_experts_per_cta(d->hidden, d->n_experts, n_tokens);
+    const void* fn = ne == 16 ? (const void*)router_kernel<16> : (const void*)router_kernel<8>;
+    const size_t smem = router_smem_bytes(d->hidden, d->n_experts, ne);
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute((const void*)router_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return SGP_ERR_CUDA;
     void* args[] = {(void*)&p, (void*)&c};
-    dim3 grid(groups, (d->n_experts + 7) / 8);
-    if (cudaLaunchKernel((const void*)router_kernel, grid, dim3(kRouterWarps * 32), args, smem, s) !=
-        cudaSuccess)
+    dim3 grid(groups, (d->n_experts + ne - 1) / ne);
+    if (cudaLaunchKernel(fn, grid, dim3(kRouterWarps * 32), args, smem, s) != cudaSuccess)
         return SGP_ERR_CUDA;
     return SGP_OK;
 }

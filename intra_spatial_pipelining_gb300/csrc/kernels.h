@@ -173,7 +173,7 @@ struct CombineProblem {
     const int* pair_pos;    // [nrows * k]
     bf16* out;              // [T][H] batch-wide
     int row0, nrows, k, H;
-    // optional: the next layer's a = RMSNorm(out; g_next) in the same pass (H <= 8192)
+    // optional: the next layer's a = RMSNorm(out; g_next) in the same pass (H <= 4096)
     const bf16* g_next;     // or NULL
     bf16* a_next;           // [T][H] batch-wide
     float eps;

@@ -475,8 +475,8 @@ struct RunEnv {
     bool keep_weights = false;
 };
 
-// The combine can produce the next layer's RMSNorm-1 while it holds the row (H <= 8192).
-bool can_fuse_norm(const sgp_dims& d) { return d.hidden <= 8192; }
+// The combine can produce the next layer's RMSNorm-1 while it holds the row (H <= 4096).
+bool can_fuse_norm(const sgp_dims& d) { return d.hidden <= 4096; }
 
 int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     const sgp_dims& d = *e.d;
