@@ -6,13 +6,14 @@
 // of work follows the pool size while every chunk's arithmetic does not.
 //
 // Every warp streams its chunks through a private ring of kASlots shared-memory stages of
-// kAPos = 64 positions (one 8 KB TMA operation for K and one for V, L2 evict-first): lane 0
-// refills a stage as soon as the warp has consumed it, so a warp never waits on another.
-// A warp's arithmetic on a stage takes about as long as the stage's load, so the ring is
-// spent on more warps rather than on deeper per-warp buffering: twelve warps with one
-// 64-position stage each stream faster on a partial pool than six with 128 positions (at
-// 512 sequences x KV 32768: 100 against 87 GB/s per SM on 56 SMs), and six with one stage
-// faster than three with two.
+// POS positions (one TMA operation for K and one for V, L2 evict-first): lane 0 refills a
+// stage as soon as the warp has consumed it, so a warp never waits on another.  A warp's
+// arithmetic on a stage takes about as long as the stage's load, so the ring is spent on
+// more warps rather than on deeper per-warp buffering: twelve warps with one 64-position
+// stage each stream faster on a partial pool than six with 128 positions (at 512 sequences
+// x KV 32768: 100 against 87 GB/s per SM on 56 SMs), six with 128 faster on the full GPU
+// when each warp gets only a few chunks (0.975 against 0.93 of HBM bandwidth at 64
+// sequences x KV 8192), and six with one stage faster than three with two.
 // Per stage the warp computes, on warp-level bf16 MMAs with fp32 accumulation,
 //     S^T = K q^T   (M = 16 positions, N = 8 query heads of the KV head, K = 64)
 //     O^T += V^T P^T (M = 16 dims, N = 8 heads, K = 16 positions),
@@ -34,15 +35,15 @@ namespace sgp {
 
 namespace {
 
-constexpr int kAWarps = 12;                  // streaming warps per CTA
+// Two configurations of the same kernel, chosen per shape (never per pool: the stage
+// length sets the order of the fp32 online softmax): NW streaming warps per CTA with one
+// stage of POS positions each, 192 KB of ring either way.
+//   12 x 64: twice the warps on half the arithmetic per stage -- faster per SM where the pool
+//            is small and there are many chunks (long caches);
+//    6 x 128: larger TMA boxes -- faster on the full GPU when chunks per warp are few.
 constexpr int kASlots = 1;                   // ring stages per warp
-constexpr int kAPos = kAttnStagePos;         // positions per stage (64)
-constexpr int kAPT = kAPos / 16;             // 16-position MMA tiles per stage
-constexpr int kAHalf = kAPos * 128;          // K (or V) bytes of a stage: 8 KB
-constexpr int kAStage = 2 * kAHalf;          // K then V
 constexpr int kAMaxRows = 512;               // sequences per launch (prefix table size)
 constexpr int kAPerLane = kAMaxRows / 32;    // sequences per lane of the prefix scan
-constexpr size_t kARing = (size_t)kAWarps * kASlots * kAStage;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -82,6 +83,7 @@ struct Cursor {
     int j, nst;          // stage within the chunk, stages of the chunk
 };
 
+template <int POS>
 __device__ __forceinline__ void cursor_at(Cursor& x, int i, const int* pre, const int* kvl,
                                           int nrows, const AttnProblem& P) {
     x.i = i;
@@ -101,7 +103,7 @@ __device__ __forceinline__ void cursor_at(Cursor& x, int i, const int* pre, cons
     x.p0 = first + x.c * P.chunk;
     x.p1 = min(L, x.p0 + P.chunk);
     x.j = 0;
-    x.nst = (x.p1 - x.p0 + kAPos - 1) / kAPos;
+    x.nst = (x.p1 - x.p0 + POS - 1) / POS;
 }
 
 template <int NT>
@@ -158,9 +160,15 @@ __device__ void merge_pair(const AttnProblem& P, int t, int kvh, int S_t, int la
     }
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kAWarps * 32, 1)
+template <int NT, int NW, int POS>
+__global__ void __launch_bounds__(NW * 32, 1)
     attn_decode_kernel(const __grid_constant__ AttnProblem P, const KCtx ctx) {
+    constexpr int kAWarps = NW;                    // streaming warps per CTA
+    constexpr int kAPos = POS;                     // positions per stage
+    constexpr int kAPT = kAPos / 16;               // 16-position MMA tiles per stage
+    constexpr int kAHalf = kAPos * 128;            // K (or V) bytes of a stage
+    constexpr int kAStage = 2 * kAHalf;            // K then V
+    constexpr size_t kARing = (size_t)kAWarps * kASlots * kAStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -231,7 +239,7 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
     const int g = lane >> 2, cq = lane & 3;
 
     Cursor cs, ld;
-    if (i0 < i1) cursor_at(cs, i0, pre, kvl, P.nrows, P);
+    if (i0 < i1) cursor_at<POS>(cs, i0, pre, kvl, P.nrows, P);
     else cs.i = i1;
     ld = cs;
     uint32_t n_iss = 0, n_con = 0;
@@ -246,7 +254,7 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
         }
         ++n_iss;
         if (++ld.j == ld.nst) {
-            if (ld.i + 1 < i1) cursor_at(ld, ld.i + 1, pre, kvl, P.nrows, P);
+            if (ld.i + 1 < i1) cursor_at<POS>(ld, ld.i + 1, pre, kvl, P.nrows, P);
             else ld.i = i1;
         }
     };
@@ -454,7 +462,7 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
             }
         }
         if (++cs.j == cs.nst) {
-            if (cs.i + 1 < i1) cursor_at(cs, cs.i + 1, pre, kvl, P.nrows, P);
+            if (cs.i + 1 < i1) cursor_at<POS>(cs, cs.i + 1, pre, kvl, P.nrows, P);
             else cs.i = i1;
         }
     }
@@ -469,12 +477,19 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
 }  // namespace
 
 int enqueue_attention(Launcher& L, const AttnProblem& p, const KCtx& c) {
-    if (p.nrows < 1 || p.nrows > kAMaxRows || p.G < 1 || p.G > 16 || p.chunk % kAPos)
+    if (p.nrows < 1 || p.nrows > kAMaxRows || p.G < 1 || p.G > 16 ||
+        (p.pos != 64 && p.pos != 128) || p.chunk % p.pos)
         return (int)cudaErrorInvalidValue;
-    dim3 grid(p.n_cta > 0 ? p.n_cta : 1), block(kAWarps * 32);
-    size_t smem = kARing + 1024 + kAWarps * kASlots * 8 + (2 * kAMaxRows + 1) * 4;
+    const int nw = p.pos == 64 ? 12 : 6;
+    dim3 grid(p.n_cta > 0 ? p.n_cta : 1), block(nw * 32);
+    const size_t smem = (size_t)nw * kASlots * 2 * p.pos * 128 + 1024 + nw * kASlots * 8 +
+                        (2 * kAMaxRows + 1) * 4;
     void* args[] = {(void*)&p, (void*)&c};
-    const void* f = p.G > 8 ? (const void*)attn_decode_kernel<2> : (const void*)attn_decode_kernel<1>;
+    const void* f;
+    if (p.pos == 64)
+        f = p.G > 8 ? (const void*)attn_decode_kernel<2, 12, 64> : (const void*)attn_decode_kernel<1, 12, 64>;
+    else
+        f = p.G > 8 ? (const void*)attn_decode_kernel<2, 6, 128> : (const void*)attn_decode_kernel<1, 6, 128>;
     return L.launch(f, grid, block, smem, args);
 }
 

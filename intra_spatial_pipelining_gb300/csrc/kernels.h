@@ -118,7 +118,7 @@ struct GemvProblem {
 };
 
 struct AttnProblem {
-    CUtensorMap tmK, tmV;   // caches as 2-D [seq * nkv * cap][64], box {64, 128}, SW128
+    CUtensorMap tmK, tmV;   // caches as 2-D [seq * nkv * cap][64], box {64, pos}, SW128
     const bf16* q;          // [T][nq * 64]
     const int* kv_len;      // [T]
     bf16* o;                // [T][nq * 64]
@@ -128,6 +128,7 @@ struct AttnProblem {
     int row0, nrows, nq, nkv, G, cap, window, chunk, S_max;
     float scale_log2;       // log2(e) / sqrt(d)
     int n_cta;              // persistent CTAs (one per SM of the pool)
+    int pos;                // positions per stage (64 or 128; the K / V box height)
 };
 
 struct NormProblem {
@@ -196,6 +197,9 @@ size_t gemm_tc_ring_bytes(int n_cap, int stages, int kps);
 size_t gemm_tc_smem_bytes(int n_cap, int stages, int kps);
 // attention chunk length (positions per split-KV work item); fixed, never SM-dependent
 constexpr int kAttnChunk = 1024;
-constexpr int kAttnStagePos = 64;  // KV positions per attention stage (the K / V TMA box height)
+// Positions per attention stage for a call: 64 (12 warps per CTA) when the full batch has at
+// least 8192 split-KV chunks, else 128 (6 warps).  A function of the shape alone, never of
+// the SM pool, since it fixes the order of the fp32 online softmax.
+inline int attn_stage_pos(long long n_chunks) { return n_chunks >= 8192 ? 64 : 128; }
 
 }  // namespace sgp

@@ -668,8 +668,13 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
             AttnProblem p;
             memset(&p, 0, sizeof(p));
             const uint64_t rows = (uint64_t)e.T * d.n_kv_heads * e.layer->kv_cap;
-            if ((r = make_tmap(&p.tmK, e.layer->k_cache, 64, rows, 64, kAttnStagePos)) != SGP_OK) return r;
-            if ((r = make_tmap(&p.tmV, e.layer->v_cache, 64, rows, 64, kAttnStagePos)) != SGP_OK) return r;
+            {
+                const int span0 = e.layer->window > 0 ? std::min(e.layer->window, e.layer->kv_cap)
+                                                      : e.layer->kv_cap;
+                p.pos = attn_stage_pos((long long)e.T * d.n_kv_heads * cdiv(span0, kAttnChunk));
+            }
+            if ((r = make_tmap(&p.tmK, e.layer->k_cache, 64, rows, 64, p.pos)) != SGP_OK) return r;
+            if ((r = make_tmap(&p.tmV, e.layer->v_cache, 64, rows, 64, p.pos)) != SGP_OK) return r;
             p.q = e.ws.at<bf16>(Lay.q);
             p.kv_len = e.kv_len;
             p.o = e.ws.at<bf16>(Lay.o);
