@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--virtual-comm", action="store_true",
+                    help="add the pages' virtual communication kernels (3 us + bytes / 900 GB/s "
+                         "for the attention all-reduce, MoE dispatch and MoE combine)")
     return ap.parse_args()
 
 
@@ -306,7 +309,8 @@ def run_sgp(args, rank, world, local_rank):
     caches = [synth.kv_cache(wl, l, seed, dev) for l in range(wl.n_layers)]
     layers = sgp.layer_array([sgp.make_layer(w, k, v, wl.layer_window(l))
                               for l, (w, (k, v)) in enumerate(zip(weights, caches))])
-    d = sgp.make_dims(s)
+    comm = (3.0, 900.0) if args.virtual_comm else (0.0, 0.0)
+    d = sgp.make_dims(s, comm_floor_us=comm[0], comm_gbps=comm[1])
     out = x.clone()
     info = sgp.sgp_device_info_get()
     N = info.sm_count
@@ -432,6 +436,8 @@ def run_sgp(args, rank, world, local_rank):
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                "ms_per_step": ms_e2e}
     n_launch = launches_per_run(make, n_stages, split, micro, opts_kw, layers, kv_len, x, out, T)
+    if args.virtual_comm:  # the communication kernels record no trace: three per layer and microbatch
+        n_launch += 3 * wl.n_layers * (T // micro)
     sgp.sgp_pipeline_destroy(pipe)
 
     # ---- roofline of the dominant kernel (full-attention decode), timed alone ----
@@ -480,6 +486,8 @@ def run_sgp(args, rank, world, local_rank):
                                 "cut": args.cut if n_stages == 2 else "A | B1-B4 | B5-B8",
                                 "sm_split": split,
                                 "microbatches": T // micro, "microbatch": micro,
+                                "virtual_comm": ("3 us + payload / 900 GB/s per collective"
+                                                 if args.virtual_comm else None),
                                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
         "iteration_us": iter_us,
         "tokens_per_s_per_user": 1e6 / iter_us,

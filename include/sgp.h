@@ -94,6 +94,15 @@ typedef struct sgp_dims {
     float rope_theta;     /* RoPE base for q and the new key at position kv_len-1
                              (half-split pairs i, i + d/2); 0 = no rotation.  Needs the
                              tensor-core QKV path (SGP_ERR_UNSUPPORTED otherwise)      */
+    /* Virtual communication of a multi-GPU deployment emulated on this GPU ("SubGPU
+     * Pipelining: Intra-GPU Fine-Grained Spatial Parallelism for LLM Inference", Section
+     * 5.3): when both are > 0, every layer and microbatch runs three loopback kernels that
+     * copy the payload of the attention all-reduce (after the output projection, b*H bf16),
+     * the MoE dispatch (after the dispatch, b*k*H bf16) and the MoE combine (before the
+     * combine, b*k*H bf16) into workspace scratch and last at least
+     * comm_floor_us + payload / comm_gbps.  Results are unchanged.  0, 0 = off.        */
+    float comm_floor_us;
+    float comm_gbps;
 } sgp_dims;
 
 /* One layer's weights and KV cache (all device pointers, caller-owned).

@@ -621,6 +621,46 @@ int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c) {
                     (size_t)(3 * R + p.E_local + 1) * sizeof(int), args);
 }
 
+// ---------------------------------------------------------------------------------------
+// Virtual communication (a collective of a multi-GPU deployment emulated on one GPU): the
+// local endpoint work -- the payload is read and written to scratch -- and a duration of at
+// least the model's floor, measured from the moment the payload is ready.  Every CTA copies
+// its share, then sleeps until its own floor has passed (bounded by the floor itself).
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) comm_kernel(const CommProblem P, const KCtx ctx) {
+    griddep_launch();
+    griddep_wait();
+    task_begin(ctx);
+    const uint64_t t0 = globaltimer();
+    const size_t n16 = P.bytes / 16;
+    const uint4* __restrict__ src = reinterpret_cast<const uint4*>(P.src);
+    uint4* __restrict__ dst = reinterpret_cast<uint4*>(P.dst);
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    constexpr int kU = 4;  // independent loads in flight per thread
+    for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n16; i0 += kU * stride) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (i0 + u * stride < n16) v[u] = __ldcg(src + i0 + u * stride);
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (i0 + u * stride < n16) dst[i0 + u * stride] = v[u];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        while (globaltimer() - t0 < P.floor_ns) __nanosleep(256);
+    __syncthreads();
+    task_end(ctx);
+}
+
+int enqueue_comm(Launcher& L, const CommProblem& p, const KCtx& c) {
+    if (((reinterpret_cast<uintptr_t>(p.src) | reinterpret_cast<uintptr_t>(p.dst)) & 15) ||
+        p.floor_ns > 1000000000ull)
+        return (int)cudaErrorInvalidValue;
+    void* args[] = {(void*)&p, (void*)&c};
+    return L.launch((const void*)comm_kernel, dim3(32), dim3(256), 0, args);
+}
+
 int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c) {
     void* args[] = {(void*)&p, (void*)&c};
     if (p.k < 1 || p.k > 8 || (p.H & 3) || (p.a_next != nullptr && p.H > 4 * 2 * kCombThreads))

@@ -180,10 +180,20 @@ struct CombineProblem {
     float eps;
 };
 
+// Virtual communication: copy `bytes` (a multiple of 16) from src to dst, lasting at least
+// floor_ns from the moment the payload is ready.
+struct CommProblem {
+    const void* src;
+    void* dst;
+    size_t bytes;
+    unsigned long long floor_ns;
+};
+
 // --------------------------------------------------------------------------------------
 // host enqueue functions (return cudaError_t as int)
 // --------------------------------------------------------------------------------------
 int enqueue_rmsnorm(Launcher& L, const NormProblem& p, const KCtx& c);
+int enqueue_comm(Launcher& L, const CommProblem& p, const KCtx& c);
 int enqueue_router(Launcher& L, const RouterProblem& p, const KCtx& c);
 int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c);
 int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c);

@@ -240,6 +240,8 @@ int check_dims(const sgp_dims* d) {
     if (d->path < 0 || d->path > 2) return fail_arg("path must be SGP_PATH_*");
     if (!(d->rope_theta >= 0.f)) return fail_arg("rope_theta must be >= 0");
     if (!(d->rms_eps > 0.f)) return fail_arg("rms_eps must be positive");
+    if (!(d->comm_floor_us >= 0.f && d->comm_floor_us <= 1e5f) || !(d->comm_gbps >= 0.f))
+        return fail_arg("comm_floor_us must be in [0, 1e5] and comm_gbps >= 0");
     if (d->hidden > 8192) return fail_arg("hidden above 8192 is not supported");
     return SGP_OK;
 }
@@ -328,7 +330,7 @@ struct Layout {
     size_t mu_base = 0;
     // offsets inside a microbatch block
     size_t part_ml = 0, part_acc = 0, logits = 0, idx = 0, wts = 0, offsets = 0, pair_pos = 0,
-           xperm = 0, zbuf = 0, ybuf = 0, gemm_part = 0;
+           xperm = 0, zbuf = 0, ybuf = 0, gemm_part = 0, comm = 0;
     int max_tiles = 0;
     size_t total = 0;
 };
@@ -386,6 +388,7 @@ Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags, int
     L.xperm = mtake((size_t)R * H * 2);
     L.zbuf = mtake((size_t)R * d.inter * 2);
     L.ybuf = mtake((size_t)R * H * 4);
+    L.comm = mtake((size_t)R * H * 2);  // virtual-communication scratch (largest payload)
     size_t gp = 0;
     for (int op : {SGP_OP_QKV, SGP_OP_OPROJ, SGP_OP_EXPERT_UP, SGP_OP_EXPERT_DOWN}) {
         GemmShape g = gemm_shape(d, op, T);
@@ -647,6 +650,31 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     return enqueue_gemm_finish(L, f, c2);
 }
 
+// Virtual communication (sgp_dims::comm_floor_us / comm_gbps): on when both are positive.
+bool comm_on(const sgp_dims& d) { return d.comm_floor_us > 0.f && d.comm_gbps > 0.f; }
+unsigned long long comm_floor_ns(const sgp_dims& d, size_t bytes) {
+    return (unsigned long long)((double)d.comm_floor_us * 1e3 + (double)bytes / (double)d.comm_gbps);
+}
+// An op followed (or preceded) by a communication kernel: the op's first launch checks the
+// handoff flag and the last one publishes it; the communication kernel has no trace slot.
+void split_for_comm(const KCtx& c, bool comm_last, KCtx& op_ctx, KCtx& comm_ctx) {
+    op_ctx = c;
+    comm_ctx = c;
+    comm_ctx.trace = nullptr;
+    if (comm_last) {
+        op_ctx.post_flag = nullptr;
+        op_ctx.post_cnt = nullptr;
+        op_ctx.fault &= ~FAULT_SKIP_PUBLISH;
+        comm_ctx.wait_flag = nullptr;
+        comm_ctx.fault &= FAULT_SKIP_PUBLISH;
+    } else {
+        comm_ctx.post_flag = nullptr;
+        comm_ctx.post_cnt = nullptr;
+        comm_ctx.fault = 0;
+        op_ctx.wait_flag = nullptr;
+    }
+}
+
 int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     const sgp_dims& d = *e.d;
     const Layout& Lay = *e.ws.L;
@@ -659,8 +687,19 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
                           d.hidden, d.rms_eps};
             return enqueue_rmsnorm(L, p, c);
         }
-        case SGP_OP_QKV:
         case SGP_OP_OPROJ:
+            if (comm_on(d)) {
+                // attention all-reduce of the projected rows (b x H bf16)
+                KCtx co, cc;
+                split_for_comm(c, true, co, cc);
+                if ((r = gemm_op(L, e, op, mu, co)) != 0) return r;
+                const size_t bytes = (size_t)b * d.hidden * 2;
+                CommProblem cp{e.ws.at<bf16>(Lay.h) + (size_t)row0 * d.hidden,
+                               e.ws.mu<bf16>(mu, Lay.comm), bytes, comm_floor_ns(d, bytes)};
+                return enqueue_comm(L, cp, cc);
+            }
+            return gemm_op(L, e, op, mu, c);
+        case SGP_OP_QKV:
         case SGP_OP_EXPERT_UP:
         case SGP_OP_EXPERT_DOWN:
             return gemm_op(L, e, op, mu, c);
@@ -724,6 +763,16 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
                               e.ws.mu<bf16>(mu, Lay.xperm), e.ws.mu<int>(mu, Lay.offsets),
                               e.ws.mu<int>(mu, Lay.pair_pos), row0, b, d.top_k, d.hidden,
                               d.n_experts, d.n_local_experts, d.slot_map};
+            if (comm_on(d)) {
+                // MoE dispatch: the routed rows (b k x H bf16)
+                KCtx co, cc;
+                split_for_comm(c, true, co, cc);
+                if ((r = enqueue_dispatch(L, p, co)) != 0) return r;
+                const size_t bytes = (size_t)b * d.top_k * d.hidden * 2;
+                CommProblem cp{e.ws.mu<bf16>(mu, Lay.xperm), e.ws.mu<bf16>(mu, Lay.comm), bytes,
+                               comm_floor_ns(d, bytes)};
+                return enqueue_comm(L, cp, cc);
+            }
             return enqueue_dispatch(L, p, c);
         }
         case SGP_OP_COMBINE: {
@@ -737,6 +786,15 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
                              e.x_out, row0, b, d.top_k, d.hidden,
                              e.next ? (const bf16*)e.next->g_attn : nullptr,
                              e.next ? e.ws.at<bf16>(Lay.a) : nullptr, d.rms_eps};
+            if (comm_on(d)) {
+                // MoE combine: the expert outputs return (b k x H, bf16-sized payload)
+                KCtx co, cc;
+                split_for_comm(c, false, co, cc);
+                const size_t bytes = (size_t)b * d.top_k * d.hidden * 2;
+                CommProblem cp{p.Y, e.ws.mu<bf16>(mu, Lay.comm), bytes, comm_floor_ns(d, bytes)};
+                if ((r = enqueue_comm(L, cp, cc)) != 0) return r;
+                return enqueue_combine(L, p, co);
+            }
             return enqueue_combine(L, p, c);
         }
         default:

@@ -34,7 +34,7 @@ class sgp_dims(C.Structure):
                 ("head_dim", C.c_int), ("n_experts", C.c_int), ("top_k", C.c_int),
                 ("n_local_experts", C.c_int), ("inter", C.c_int), ("rms_eps", C.c_float),
                 ("slot_map", C.c_int), ("path", C.c_int), ("gemv_max_tokens", C.c_int),
-                ("rope_theta", C.c_float)]
+                ("rope_theta", C.c_float), ("comm_floor_us", C.c_float), ("comm_gbps", C.c_float)]
 
 
 class sgp_layer(C.Structure):
@@ -155,11 +155,15 @@ def _stream(stream) -> Optional[int]:
 # --------------------------------------------------------------------------------------
 # structure builders
 # --------------------------------------------------------------------------------------
-def make_dims(shape, path: int = PATH_AUTO, gemv_max_tokens: int = 16) -> sgp_dims:
+def make_dims(shape, path: int = PATH_AUTO, gemv_max_tokens: int = 16,
+              comm_floor_us: float = 0.0, comm_gbps: float = 0.0) -> sgp_dims:
+    """Layer dimensions.  comm_floor_us / comm_gbps > 0 turn on the virtual communication
+    kernels (3 us and 900 GB/s are the pages' model of a B200 NVLink deployment)."""
     return sgp_dims(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
                     shape.n_experts, shape.top_k, shape.n_local_experts, shape.inter,
                     shape.rms_eps, 0 if shape.slot_map == "mod" else 1, path, gemv_max_tokens,
-                    float(getattr(shape, "rope_theta", 0.0)))
+                    float(getattr(shape, "rope_theta", 0.0)), float(comm_floor_us),
+                    float(comm_gbps))
 
 
 def make_layer(w: dict, k_cache, v_cache, window: int) -> sgp_layer:

@@ -327,3 +327,41 @@ def test_stage_times_and_balancer_pick_a_legal_split():
     i = [r[0] for r in rows].index(best)
     assert max(rows[i][1:]) == min(max(r[1:]) for r in rows)
     print("balance", best, rows)
+
+
+def _time_temporal(inp, d, reps=5):
+    wl = inp.wl
+    T = wl.n_tokens
+    ws = H.workspace(d, T, wl.cap)
+    out = torch.empty_like(inp.x)
+    layers = inp.sgp_layers()
+    sgp.sgp_stack_temporal(d, layers, inp.kv_len, inp.x, out, T, None, None, ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        sgp.sgp_stack_temporal(d, layers, inp.kv_len, inp.x, out, T, None, None, ws)
+    e1.record()
+    e1.synchronize()
+    assert sgp.sgp_status_from_workspace(ws) == sgp.SGP_OK
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def test_virtual_communication_kernels():
+    """The pages' emulation of a 32-GPU deployment on one GPU: after the output projection
+    (attention all-reduce), after the dispatch and before the combine a kernel moves the
+    payload and lasts at least 3 us + payload / 900 GB/s.  Results are unchanged, temporal
+    and pipelined alike, and a temporal layer takes at least the three floors longer."""
+    wl, inp = _stack_inputs(4, 1024, 8)
+    d0 = H.dims(wl.shape)
+    d1 = sgp.make_dims(wl.shape, comm_floor_us=3.0, comm_gbps=900.0)
+    ref = _temporal(inp, d0)
+    got = _temporal(inp, d1)
+    assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+    got_p = _pipelined(inp, d1, 2, 32)
+    assert torch.equal(got_p[0], ref[0]) and torch.equal(got_p[1], ref[1])
+    T, H_, k = wl.n_tokens, wl.shape.hidden, wl.shape.top_k
+    floors_us = 3 * 3.0 + (T * H_ * 2 + 2 * T * k * H_ * 2) / 900e3
+    t0, t1 = _time_temporal(inp, d0), _time_temporal(inp, d1)
+    print(f"temporal 4 layers: {t0:.1f} us, with virtual communication {t1:.1f} us "
+          f"(floors {floors_us * wl.n_layers:.1f} us)")
+    assert t1 >= t0 + 0.8 * floors_us * wl.n_layers
