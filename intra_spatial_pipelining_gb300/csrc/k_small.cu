@@ -2,6 +2,7 @@
 // dispatch (stable counting sort of the routed pairs by expert slot + row gather) and the
 // weighted combine with the residual.  All loads and stores are 16-byte vectors, every
 // reduction has a fixed order, and each token's result depends only on that token.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -345,10 +346,13 @@ __global__ void __launch_bounds__(kRouterWarps * 32, 1)
 
 // ---------------------------------------------------------------------------------------
 // Dispatch.  Every CTA redundantly computes the stable counting sort of the pairs
-// i = t*k + j by slot (order within a slot = pair order), then gathers 8 rows of u into the
-// slot-sorted activation matrix.  CTA 0 also publishes the slot offsets and pair rows.
+// i = t*k + j by slot (order within a slot = pair order), then gathers its share of the rows
+// of u into the slot-sorted activation matrix (few rows per CTA and many loads in flight:
+// the gather is latency-bound; at most kDispCtas CTAs, as each one repeats the sort).  CTA 0
+// also publishes the slot offsets and pair rows.
 // ---------------------------------------------------------------------------------------
-constexpr int kDispRows = 8;
+constexpr int kDispRowsMin = 2;
+constexpr int kDispCtas = 256;
 
 __global__ void __launch_bounds__(256) dispatch_kernel(const DispatchProblem P, const KCtx ctx) {
     griddep_launch();
@@ -397,9 +401,10 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const DispatchProblem P, 
         for (int s = threadIdx.x; s <= P.E_local; s += 256) P.offsets[s] = offs[s];
     __syncthreads();
     const int nv = P.H >> 3;
-    const int rbeg = blockIdx.x * kDispRows;
-    const int total = (min(R, rbeg + kDispRows) - rbeg) * nv;
-    constexpr int kU = 4;  // loads in flight per thread
+    const int rpc = (R + gridDim.x - 1) / gridDim.x;  // rows of this CTA's share
+    const int rbeg = blockIdx.x * rpc;
+    const int total = max(0, min(R, rbeg + rpc) - rbeg) * nv;
+    constexpr int kU = 8;  // loads in flight per thread
     for (int i0 = threadIdx.x; i0 < total; i0 += 256 * kU) {
         uint4 v[kU];
 #pragma unroll
@@ -616,7 +621,7 @@ int enqueue_router(Launcher& L, const RouterProblem& p, const KCtx& c) {
 int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c) {
     void* args[] = {(void*)&p, (void*)&c};
     const int R = p.nrows * p.k;
-    dim3 grid((R + kDispRows - 1) / kDispRows);
+    dim3 grid(std::max(1, std::min((R + kDispRowsMin - 1) / kDispRowsMin, kDispCtas)));
     return L.launch((const void*)dispatch_kernel, grid, dim3(256),
                     (size_t)(3 * R + p.E_local + 1) * sizeof(int), args);
 }
