@@ -264,9 +264,12 @@ int q_width(const sgp_dims& d) { return d.n_q_heads * d.head_dim; }
 // 152-SM part), at least 4 k-blocks per segment.
 // tiles counts (weight tile, 128-token pass) pairs of the full batch: with many tokens the
 // passes alone give every SM work and no K split is needed.
-int choose_ksplit(int tiles, int kb_total, int kps) {
+// units_target: the (tile, pass, K segment) units the split aims at, about 2 per SM of the
+// whole GPU (3 for the expert gate/up projection, whose many tiles balance better that way;
+// measured).  Fixed numbers, so the split never depends on the pool a call runs on.
+int choose_ksplit(int tiles, int kb_total, int kps, double units_target) {
     const int n_sb = cdiv(kb_total, kps);  // K segments are made of whole stage blocks
-    int ks = (int)std::lround(456.0 / tiles);
+    int ks = (int)std::lround(units_target / tiles);
     ks = std::max(1, std::min(ks, n_sb / 2));
     return std::max(1, ks);
 }
@@ -299,7 +302,7 @@ GemmShape gemm_shape(const sgp_dims& d, int op, int T) {
     // per stage keeps the ring deep (both choices follow the full batch, like the K split)
     g.kps = rows >= 128 ? 1 : 2;
     g.ksplit = choose_ksplit(g.n_groups * g.m_tiles * cdiv(std::max(1, rows), kGemmMaxN), g.K / 64,
-                             g.kps);
+                             g.kps, op == SGP_OP_EXPERT_UP ? 456.0 : 304.0);
     return g;
 }
 
