@@ -4,16 +4,16 @@
 // Decode gives few tokens per weight matrix (64 per layer, 16-64 per expert slot), so the
 // contraction is "swap-AB": the weight tile is the MMA's M = 128 operand and the tokens are
 // its N (16..256) operand.  Two kernels per projection:
-//   gemm_tc_kernel   one CTA per (group, 128-row weight tile, K segment): weights stream
-//                    HBM -> shared memory through a TMA ring (128-byte swizzle, L2
-//                    evict-first), one elected thread issues tcgen05.mma into a TMEM
-//                    accumulator, and the fp32 tile leaves with one TMA bulk store per pass
-//                    into a partial-sum buffer.  Nothing else: no scalar stores, no
-//                    cross-CTA protocol.
-//   gemm_finish_kernel  every thread owns 8 consecutive outputs of one token: it sums the
+//   gemm_tc_kernel   persistent, one work unit = (group, 128-row weight tile, K segment):
+//                    weights stream HBM -> shared memory through a TMA ring (128-byte
+//                    swizzle), one elected lane issues tcgen05.mma into a double-buffered
+//                    TMEM accumulator, and the tile leaves through shared memory -- with the
+//                    epilogue applied when the K split is 1, else as one TMA bulk store per
+//                    chunk into a partial-sum buffer.  No cross-CTA protocol.
+//   gemm_finish_kernel  every thread owns 4 consecutive outputs of one token: it sums the
 //                    K segments in segment order (fixed, so results never depend on the
-//                    grid or the token count) and applies the fused epilogue with 16-byte
-//                    loads and stores.
+//                    grid or the token count) and applies the epilogue with 16-byte loads.
+//                    (The expert-down projection has none: the combine sums its segments.)
 #include <algorithm>
 
 #include "kernels.h"
