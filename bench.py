@@ -175,13 +175,17 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []            # (host arrival time, line)
+        self.window = None         # host times bracketing the timed region
+
+    def mark(self, t_begin, t_end):
+        self.window = (t_begin, t_end)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()
         except OSError:
@@ -189,7 +193,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def stop(self):
         if self.proc is None:
@@ -201,7 +205,15 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        lines = self.lines
+        if self.window is not None:
+            # samples taken while the timed region ran (a line arrives up to one period late)
+            t0, t1 = self.window
+            inside = [l for t, l in lines if t0 <= t <= t1 + 0.06]
+            lines = inside if inside else [l for t, l in lines if t >= t0][:1]
+        else:
+            lines = [l for _, l in lines]
+        for line in lines:
             p = [x.strip() for x in line.split(",")]
             if len(p) < 9:
                 continue
@@ -316,6 +328,10 @@ def run_sgp(args, rank, world, local_rank):
     N = info.sm_count
     stream = torch.cuda.current_stream()
 
+    # clock samples are kept only for the timed region; nvidia-smi needs a moment to start
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+
     # ---- pipeline configuration ----
     n_stages = args.stages
     micro = args.micro or (T // max(1, wl.microbatches))
@@ -374,7 +390,7 @@ def run_sgp(args, rank, world, local_rank):
     def make(nst, spl, mb, o):
         return sgp.sgp_pipeline_create(d, spl, nst, mb, T, wl.cap, o)
 
-    def time_runs(p, steps, warmup):
+    def time_runs(p, steps, warmup, sampler=None):
         for _ in range(warmup):
             sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
         sgp.check(sgp.sgp_pipeline_sync(p), "warmup")
@@ -383,11 +399,14 @@ def run_sgp(args, rank, world, local_rank):
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        t_begin = time.monotonic()
         e0.record(stream)
         for _ in range(steps):
             sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
         e1.record(stream)
         torch.cuda.synchronize()
+        if sampler is not None:
+            sampler.mark(t_begin, time.monotonic())
         sgp.check(sgp.sgp_pipeline_sync(p), "timed runs")
         ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         if world > 1:
@@ -395,9 +414,7 @@ def run_sgp(args, rank, world, local_rank):
         return ms / steps
 
     pipe = make(n_stages, split, micro, opts)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    ms_pipe = time_runs(pipe, args.steps, args.warmup)
+    ms_pipe = time_runs(pipe, args.steps, args.warmup, clocks)
     clk = clocks.stop()
 
     ms_temp = None
