@@ -178,10 +178,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     griddep_launch();
-    griddep_wait();
-    task_begin(ctx);
 
     // ---- chunk counts and their prefix over the launch's sequences (warp 0) ----
+    // kv_len is an input of the call, never written by a kernel: this prologue may run while
+    // the previous kernel (the QKV projection's last launch) still runs.
     if (warp == 0) {
         int cnt[kAPerLane], sum = 0;
 #pragma unroll
@@ -227,6 +227,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
     }
     __syncthreads();
+    // q and the appended KV row come from the previous kernel
+    griddep_wait();
+    task_begin(ctx);
 
     const int total = pre[P.nrows];
     const long long W = (long long)gridDim.x * kAWarps;
@@ -490,7 +493,7 @@ int enqueue_attention(Launcher& L, const AttnProblem& p, const KCtx& c) {
         f = p.G > 8 ? (const void*)attn_decode_kernel<2, 12, 64> : (const void*)attn_decode_kernel<1, 12, 64>;
     else
         f = p.G > 8 ? (const void*)attn_decode_kernel<2, 6, 128> : (const void*)attn_decode_kernel<1, 6, 128>;
-    return L.launch(f, grid, block, smem, args);
+    return L.launch(f, grid, block, smem, args, true);
 }
 
 }  // namespace sgp
