@@ -5,15 +5,22 @@
 // positions); warp w of the grid owns a contiguous, equal share of that list, so the split
 // of work follows the pool size while every chunk's arithmetic does not.
 //
-// Every warp streams its chunks through a private ring of kASlots shared-memory stages of
-// POS positions (one TMA operation for K and one for V, L2 evict-first): lane 0 refills a
-// stage as soon as the warp has consumed it, so a warp never waits on another.  A warp's
-// arithmetic on a stage takes about as long as the stage's load, so the ring is spent on
-// more warps rather than on deeper per-warp buffering: twelve warps with one 64-position
-// stage each stream faster on a partial pool than six with 128 positions (at 512 sequences
-// x KV 32768: 100 against 87 GB/s per SM on 56 SMs), six with 128 faster on the full GPU
-// when each warp gets only a few chunks (0.975 against 0.93 of HBM bandwidth at 64
-// sequences x KV 8192), and six with one stage faster than three with two.
+// Every warp streams its chunks through a private shared-memory stage of POS positions: a K
+// half and a V half, one TMA operation each (L2 evict-first), refilled by lane 0; a warp never
+// waits on another.  Two refill schedules, the same arithmetic:
+//   split (P.kv_split): each half has its own mbarrier; the K half takes the next stage's keys
+//     as soon as the scores are computed, so that load overlaps the softmax and the V
+//     product, and the V half is refilled once that product is done, overlapping the next
+//     scores.  Faster alone on the GPU (both configurations) and in a partial pool with
+//     128-position stages;
+//   joint: one mbarrier, both halves refilled after the V product.  Gentler on the HBM a
+//     neighbouring stage shares: with 64-position stages on a partial pool, the split
+//     schedule made the attention faster alone but the two-stage pipeline slower.
+// A warp's arithmetic on a stage takes about as long as the stage's load, so shared memory is
+// spent on more warps rather than on deeper per-warp buffering: twelve warps with one
+// 64-position stage each stream faster on a partial pool than six with 128 positions, six
+// with 128 faster on the full GPU when each warp gets only a few chunks, and six with one
+// stage faster than three with two.
 // Per stage the warp computes, on warp-level bf16 MMAs with fp32 accumulation,
 //     S^T = K q^T   (M = 16 positions, N = 8 query heads of the KV head, K = 64)
 //     O^T += V^T P^T (M = 16 dims, N = 8 heads, K = 16 positions),
@@ -41,7 +48,6 @@ namespace {
 //   12 x 64: twice the warps on half the arithmetic per stage -- faster per SM where the pool
 //            is small and there are many chunks (long caches);
 //    6 x 128: larger TMA boxes -- faster on the full GPU when chunks per warp are few.
-constexpr int kASlots = 1;                   // ring stages per warp
 constexpr int kAMaxRows = 512;               // sequences per launch (prefix table size)
 constexpr int kAPerLane = kAMaxRows / 32;    // sequences per lane of the prefix scan
 
@@ -160,7 +166,7 @@ __device__ void merge_pair(const AttnProblem& P, int t, int kvh, int S_t, int la
     }
 }
 
-template <int NT, int NW, int POS>
+template <int NT, int NW, int POS, bool SPLIT>
 __global__ void __launch_bounds__(NW * 32, 1)
     attn_decode_kernel(const __grid_constant__ AttnProblem P, const KCtx ctx) {
     constexpr int kAWarps = NW;                    // streaming warps per CTA
@@ -168,12 +174,12 @@ __global__ void __launch_bounds__(NW * 32, 1)
     constexpr int kAPT = kAPos / 16;               // 16-position MMA tiles per stage
     constexpr int kAHalf = kAPos * 128;            // K (or V) bytes of a stage
     constexpr int kAStage = 2 * kAHalf;            // K then V
-    constexpr size_t kARing = (size_t)kAWarps * kASlots * kAStage;
+    constexpr size_t kARing = (size_t)kAWarps * kAStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kARing);  // [warp][slot]
-    int* pre = reinterpret_cast<int*>(full + kAWarps * kASlots);  // [kAMaxRows + 1]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kARing);  // [warp][K, V]
+    int* pre = reinterpret_cast<int*>(full + kAWarps * 2);        // [kAMaxRows + 1]
     int* kvl = pre + kAMaxRows + 1;                                 // [kAMaxRows]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -219,7 +225,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
             run += cnt[k];
         }
         if (lane == 31) pre[P.nrows] = incl;
-        if (lane < kASlots * kAWarps) mbar_init(&full[lane], 1);
+        if (lane < 2 * kAWarps) mbar_init(&full[lane], 1);
         fence_barrier_init();
         if (lane == 0) {
             prefetch_tensormap(&P.tmK);
@@ -236,8 +242,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
     const long long gw = (long long)blockIdx.x * kAWarps + warp;
     const int i0 = (int)(gw * total / W), i1 = (int)((gw + 1) * total / W);
 
-    uint8_t* ring = smem + (size_t)warp * kASlots * kAStage;
-    uint64_t* wfull = full + warp * kASlots;
+    uint8_t* ring = smem + (size_t)warp * kAStage;
+    uint64_t* barK = full + warp * 2;
+    uint64_t* barV = barK + 1;
     const uint64_t pol = policy_evict_first();
     const int g = lane >> 2, cq = lane & 3;
 
@@ -245,23 +252,37 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (i0 < i1) cursor_at<POS>(cs, i0, pre, kvl, P.nrows, P);
     else cs.i = i1;
     ld = cs;
-    uint32_t n_iss = 0, n_con = 0;
-    auto issue = [&]() {  // next stage of `ld` -> slot n_iss % kASlots, then advance `ld`
+    // K and V halves of stage n arrive on barK / barV phase n & 1; `ld` is the next stage
+    // whose K half is to be issued, v_row the cache row of the stage whose V half is pending
+    // (joint schedule: both halves on barK, issued together by issue_k)
+    uint32_t n_k = 0, n_v = 0;  // K / V halves issued (n_v stays 0 when joint)
+    uint32_t n_kc = 0, n_con = 0;  // K halves consumed, stages consumed
+    int v_row = 0;
+    auto issue_k = [&]() {  // K half (joint: the whole stage) of stage `ld`, then advance `ld`
+        const int row = ((P.row0 + ld.t) * P.nkv + ld.kvh) * P.cap + ld.p0 + ld.j * kAPos;
         if (lane == 0) {
-            uint8_t* dst = ring + (n_iss % kASlots) * kAStage;
-            uint64_t* bar = &wfull[n_iss % kASlots];
-            const int row = ((P.row0 + ld.t) * P.nkv + ld.kvh) * P.cap + ld.p0 + ld.j * kAPos;
-            mbar_arrive_expect_tx(bar, kAStage);
-            tma_load_2d(dst, &P.tmK, bar, 0, row, pol);
-            tma_load_2d(dst + kAHalf, &P.tmV, bar, 0, row, pol);
+            mbar_arrive_expect_tx(barK, SPLIT ? kAHalf : kAStage);
+            tma_load_2d(ring, &P.tmK, barK, 0, row, pol);
+            if constexpr (!SPLIT) tma_load_2d(ring + kAHalf, &P.tmV, barK, 0, row, pol);
         }
-        ++n_iss;
+        v_row = row;
+        ++n_k;
         if (++ld.j == ld.nst) {
             if (ld.i + 1 < i1) cursor_at<POS>(ld, ld.i + 1, pre, kvl, P.nrows, P);
             else ld.i = i1;
         }
     };
-    while (ld.i < i1 && n_iss < (uint32_t)kASlots) issue();
+    auto issue_v = [&]() {  // V half of the stage whose K half was issued last
+        if (lane == 0) {
+            mbar_arrive_expect_tx(barV, kAHalf);
+            tma_load_2d(ring + kAHalf, &P.tmV, barV, 0, v_row, pol);
+        }
+        ++n_v;
+    };
+    if (ld.i < i1) {
+        issue_k();
+        if constexpr (SPLIT) issue_v();
+    }
 
     uint32_t qf[NT][4][2];
     int q_t = -1, q_h = -1;
@@ -296,22 +317,25 @@ __global__ void __launch_bounds__(NW * 32, 1)
                     oacc[md][nt][0] = oacc[md][nt][1] = oacc[md][nt][2] = oacc[md][nt][3] = 0.f;
             }
         }
-        const int slot = n_con % kASlots;
-        const bool ok = mbar_wait(&wfull[slot], (n_con / kASlots) & 1u, ctx.timeout_ns);
-        if (__any_sync(0xffffffffu, !ok)) {
+        const bool okk = mbar_wait(barK, n_con & 1u, ctx.timeout_ns);
+        if (__any_sync(0xffffffffu, !okk)) {
             if (lane == 0) report(ctx, ST_TIMEOUT, 10);
             failed = true;
             break;
         }
-        uint8_t* sk = ring + slot * kAStage;
-        const uint32_t ka = smem_u32(sk), va = ka + kAHalf;
+        if constexpr (SPLIT) ++n_kc;
+        const uint32_t ka = smem_u32(ring), va = ka + kAHalf;
         const int valid = min(kAPos, cs.p1 - (cs.p0 + cs.j * kAPos));
-        if (valid < kAPos) {
-            // positions past the chunk: zero V (the cache there is arbitrary, P is 0 there)
-            uint4* v4 = reinterpret_cast<uint4*>(sk + kAHalf);
-            for (int e = valid * 8 + lane; e < kAPos * 8; e += 32) v4[e] = make_uint4(0, 0, 0, 0);
-            __syncwarp();
-        }
+        // positions past the chunk: zero V (the cache there is arbitrary, P is 0 there);
+        // joint: V has landed with K
+        auto zero_v_tail = [&]() {
+            if (valid < kAPos) {
+                uint4* v4 = reinterpret_cast<uint4*>(ring + kAHalf);
+                for (int e = valid * 8 + lane; e < kAPos * 8; e += 32) v4[e] = make_uint4(0, 0, 0, 0);
+                __syncwarp();
+            }
+        };
+        if constexpr (!SPLIT) zero_v_tail();
 
         // ---- S^T = K q^T: 8 position tiles x NT head tiles ----
         float s[kAPT][NT][4];
@@ -379,6 +403,19 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 oacc[md][nt][3] *= c1;
             }
         }
+        if constexpr (SPLIT) {
+            // ---- K half consumed: the next stage's keys load during the V product ----
+            fence_proxy_async();
+            __syncwarp();
+            if (ld.i < i1) issue_k();
+            const bool okv = mbar_wait(barV, n_con & 1u, ctx.timeout_ns);
+            if (__any_sync(0xffffffffu, !okv)) {
+                if (lane == 0) report(ctx, ST_TIMEOUT, 11);
+                failed = true;
+                break;
+            }
+            zero_v_tail();
+        }
         // ---- O^T += V^T P^T: 8 position steps of 16 x 4 dim tiles x NT head tiles ----
 #pragma unroll
         for (int ks = 0; ks < kAPT; ++ks) {
@@ -397,11 +434,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
                 for (int nt = 0; nt < NT; ++nt) mma16816(oacc[md][nt], a, b0[nt], b1[nt]);
             }
         }
-        // ---- release the stage: this warp refills it ----
+        // ---- V half consumed (split: the next stage's values load during its scores;
+        //      joint: the whole stage is refilled) ----
         fence_proxy_async();
         __syncwarp();
         ++n_con;
-        if (ld.i < i1) issue();
+        if constexpr (SPLIT) {
+            if (n_v < n_k) issue_v();
+        } else if (ld.i < i1) {
+            issue_k();
+        }
 
         if (cs.j == cs.nst - 1) {
             // ---- end of chunk: row sums over the position lanes, then partial or output ----
@@ -470,9 +512,11 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
     }
     if (failed) {
-        // drain this warp's loads still in flight (bounded)
-        for (uint32_t q = n_con; q < n_iss; ++q)
-            (void)mbar_wait(&wfull[q % kASlots], (q / kASlots) & 1u, 10000000ull);
+        // drain this warp's loads still in flight (bounded): at most one per half, the
+        // stage the warp was waiting on or the one after it
+        for (uint32_t q = SPLIT ? n_kc : n_con; q < n_k; ++q)
+            (void)mbar_wait(barK, q & 1u, 10000000ull);
+        for (uint32_t q = n_con; q < n_v; ++q) (void)mbar_wait(barV, q & 1u, 10000000ull);
     }
     task_end(ctx);
 }
@@ -485,14 +529,16 @@ int enqueue_attention(Launcher& L, const AttnProblem& p, const KCtx& c) {
         return (int)cudaErrorInvalidValue;
     const int nw = p.pos == 64 ? 12 : 6;
     dim3 grid(p.n_cta > 0 ? p.n_cta : 1), block(nw * 32);
-    const size_t smem = (size_t)nw * kASlots * 2 * p.pos * 128 + 1024 + nw * kASlots * 8 +
+    const size_t smem = (size_t)nw * 2 * p.pos * 128 + 1024 + nw * 2 * 8 +
                         (2 * kAMaxRows + 1) * 4;
     void* args[] = {(void*)&p, (void*)&c};
-    const void* f;
-    if (p.pos == 64)
-        f = p.G > 8 ? (const void*)attn_decode_kernel<2, 12, 64> : (const void*)attn_decode_kernel<1, 12, 64>;
-    else
-        f = p.G > 8 ? (const void*)attn_decode_kernel<2, 6, 128> : (const void*)attn_decode_kernel<1, 6, 128>;
+    // [pos == 64][G > 8][kv_split]
+    static const void* const kern[2][2][2] = {
+        {{(const void*)attn_decode_kernel<1, 6, 128, false>, (const void*)attn_decode_kernel<1, 6, 128, true>},
+         {(const void*)attn_decode_kernel<2, 6, 128, false>, (const void*)attn_decode_kernel<2, 6, 128, true>}},
+        {{(const void*)attn_decode_kernel<1, 12, 64, false>, (const void*)attn_decode_kernel<1, 12, 64, true>},
+         {(const void*)attn_decode_kernel<2, 12, 64, false>, (const void*)attn_decode_kernel<2, 12, 64, true>}}};
+    const void* f = kern[p.pos == 64][p.G > 8][p.kv_split != 0];
     return L.launch(f, grid, block, smem, args, true);
 }
 

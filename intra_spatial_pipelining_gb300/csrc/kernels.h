@@ -129,6 +129,10 @@ struct AttnProblem {
     float scale_log2;       // log2(e) / sqrt(d)
     int n_cta;              // persistent CTAs (one per SM of the pool)
     int pos;                // positions per stage (64 or 128; the K / V box height)
+    // 1: the K and V halves of a stage are waited on and refilled separately (K after the
+    // scores, V after the V product); 0: together, after the V product.  Load schedule only:
+    // the results are identical either way.
+    int kv_split;
 };
 
 struct NormProblem {

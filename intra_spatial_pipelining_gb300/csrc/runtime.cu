@@ -737,6 +737,9 @@ int enqueue_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
             if (p.S_max > Lay.S_max) return fail_arg("kv_cap exceeds the workspace's max_kv_len");
             p.scale_log2 = 1.4426950408889634f / sqrtf((float)d.head_dim);
             p.n_cta = e.pool_sms;
+            // split refills: alone on the GPU, or with 128-position stages; with 64-position
+            // stages on a partial pool the joint schedule leaves more HBM to the other stage
+            p.kv_split = (p.pos == 128 || e.pool_sms >= device_sms()) ? 1 : 0;
             return enqueue_attention(L, p, c);
         }
         case SGP_OP_ROUTER: {
