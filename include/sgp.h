@@ -266,8 +266,11 @@ typedef struct sgp_pipeline_opts {
     int programmatic_launch;    /* programmatic dependent launch between consecutive kernels
                                    of a task (a kernel's launch and prologue overlap the
                                    previous kernel's tail; results are identical):
-                                   0 = default: only into the projection kernels and their
-                                   finishing passes (the weight stream starts early);
+                                   0 = default: only into the kernels whose prologue does
+                                   not read the predecessor's output: the projection
+                                   kernels and their finishing passes (the weight stream
+                                   starts early) and the attention (it builds its chunk
+                                   table from kv_len first);
                                    1 = into every kernel; -1 = off                            */
     int trace;                  /* 1: every kernel records its first-CTA start and last-CTA
                                    end (%globaltimer ns); read with sgp_pipeline_trace      */
