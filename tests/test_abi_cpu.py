@@ -81,3 +81,102 @@ def test_split_enumerator_matches_the_model(lib):
         assert all(pmin <= p <= n_sm - pmin and p % q == 0 for p in got)
     # the page's 148-SM, 2-SM-quantum grid has 73 two-stage allocations
     assert len(sgp.sgp_enumerate_splits(148, 2, 2)) == S.count_allocations_closed(148, 2, 2)
+
+
+def _gptoss_dims():
+    from intra_spatial_pipelining_gb300 import synth
+    return sgp.make_dims(synth.SHAPE_GPTOSS)
+
+
+def test_pipeline_create_rejects_bad_arguments_before_any_device_work(lib):
+    """sgp_pipeline_create validates its arguments first: every bad argument returns
+    SGP_ERR_INVALID_ARG, leaves *out NULL and records a message (no CUDA call is made)."""
+    d = _gptoss_dims()
+    split = (ctypes.c_int * 2)(40, 112)
+    opts = sgp.make_opts()
+
+    def create(dims, n_stages=2, micro=32, max_tokens=64, max_kv=8192, out=True):
+        h = ctypes.c_void_p(12345)
+        r = lib.sgp_pipeline_create(dims, split, n_stages, micro, max_tokens, max_kv,
+                                    ctypes.byref(opts), ctypes.byref(h) if out else None)
+        return r, h.value
+
+    bad_dims = _gptoss_dims()
+    bad_dims.head_dim = 128
+    cases = [
+        dict(dims=ctypes.byref(bad_dims)),                       # head_dim != 64
+        dict(dims=None),                                          # dims NULL
+        dict(dims=ctypes.byref(d), n_stages=0),
+        dict(dims=ctypes.byref(d), n_stages=4),
+        dict(dims=ctypes.byref(d), micro=24),                     # does not divide 64
+        dict(dims=ctypes.byref(d), micro=0),
+        dict(dims=ctypes.byref(d), micro=512, max_tokens=1024),   # more than 512 sequences
+        dict(dims=ctypes.byref(d), max_kv=0),
+    ]
+    for c in cases:
+        r, h = create(**c)
+        assert r == sgp.SGP_ERR_INVALID_ARG, c
+        assert h is None, c                                       # *out was reset to NULL
+        assert lib.sgp_last_error().decode()
+    r, _ = create(ctypes.byref(d), out=False)
+    assert r == sgp.SGP_ERR_INVALID_ARG
+
+
+def test_dims_checks_cover_every_documented_limit(lib):
+    """check_dims, reached through sgp_workspace_bytes (0 = rejected)."""
+    good = _gptoss_dims()
+    assert lib.sgp_workspace_bytes(ctypes.byref(good), 64, 8192) > 0
+    edits = [("hidden", 2880 + 32), ("hidden", 8192 + 64), ("inter", 100), ("n_kv_heads", 0),
+             ("n_q_heads", 60), ("n_q_heads", 8 * 17), ("top_k", 0), ("top_k", 9),
+             ("n_experts", 2), ("n_experts", 2048), ("n_local_experts", 0),
+             ("n_local_experts", 129), ("slot_map", 2), ("path", 3), ("rope_theta", -1.0),
+             ("rms_eps", 0.0), ("comm_floor_us", -1.0), ("comm_floor_us", 2e5),
+             ("comm_gbps", -1.0)]
+    for field, value in edits:
+        d = _gptoss_dims()
+        setattr(d, field, value)
+        assert lib.sgp_workspace_bytes(ctypes.byref(d), 64, 8192) == 0, (field, value)
+    assert lib.sgp_workspace_bytes(ctypes.byref(good), 0, 8192) == 0
+    assert lib.sgp_workspace_bytes(ctypes.byref(good), 64, 0) == 0
+
+
+def test_layer_calls_reject_bad_arguments_before_any_device_work(lib):
+    """sgp_layer_op / sgp_layer_temporal: op index, token count, NULL pointers and alignment
+    are checked before the library touches the device."""
+    d = _gptoss_dims()
+    layer = sgp.sgp_layer()
+    buf = ctypes.create_string_buffer(4096 + 256)
+    base = (ctypes.addressof(buf) + 255) & ~255
+    ok_ptr = ctypes.c_void_p(base)
+    odd_ptr = ctypes.c_void_p(base + 8)
+    E = sgp.SGP_ERR_INVALID_ARG
+    op = lambda o, T, kv, x, y, ws: lib.sgp_layer_op(ctypes.byref(d), ctypes.byref(layer), o,
+                                                       kv, x, y, T, ws, 1 << 30, None)
+    assert op(-1, 64, ok_ptr, ok_ptr, ok_ptr, ok_ptr) == E
+    assert op(9, 64, ok_ptr, ok_ptr, ok_ptr, ok_ptr) == E
+    assert op(0, 0, ok_ptr, ok_ptr, ok_ptr, ok_ptr) == E
+    assert op(0, 513, ok_ptr, ok_ptr, ok_ptr, ok_ptr) == E
+    assert op(0, 64, None, ok_ptr, ok_ptr, ok_ptr) == E
+    assert op(0, 64, ok_ptr, None, ok_ptr, ok_ptr) == E
+    assert op(0, 64, ok_ptr, ok_ptr, ok_ptr, None) == E
+    assert op(0, 64, ok_ptr, odd_ptr, ok_ptr, ok_ptr) == E       # x not 16-byte aligned
+    assert op(0, 64, ok_ptr, ok_ptr, ok_ptr, odd_ptr) == E       # workspace not 256-byte aligned
+    # a layer with NULL weights is refused by the layer check
+    assert op(0, 64, ok_ptr, ok_ptr, ok_ptr, ok_ptr) == E
+    tmp = lambda T, layer_ptr, kv: lib.sgp_layer_temporal(
+        ctypes.byref(d), layer_ptr, kv, ok_ptr, ok_ptr, T, None, None, ok_ptr, 1 << 30,
+        None, None)
+    assert tmp(64, None, ok_ptr) == E                            # no layers
+    assert tmp(64, ctypes.byref(layer), None) == E               # kv_len NULL
+    assert tmp(0, ctypes.byref(layer), ok_ptr) == E
+    assert tmp(64, ctypes.byref(layer), ok_ptr) == E             # NULL weights
+
+
+def test_pipeline_calls_on_a_null_handle(lib):
+    E = sgp.SGP_ERR_INVALID_ARG
+    n = ctypes.c_int(-1)
+    assert lib.sgp_pipeline_sync(None) == E
+    assert lib.sgp_pipeline_tasks(None, ctypes.byref(n), None, 0) == E
+    assert lib.sgp_pipeline_trace(None, None, 0, ctypes.byref(n)) == E
+    assert lib.sgp_pipeline_run(None, None, 1, None, None, None, 64, None, None, None) == E
+    lib.sgp_pipeline_destroy(None)  # no-op
