@@ -74,7 +74,7 @@ def test_tiny_pipeline_bit_identical():
     assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
 
 
-@pytest.mark.parametrize("n_stages,micro", [(1, 64), (2, 32), (2, 16), (3, 16)])
+@pytest.mark.parametrize("n_stages,micro", [(1, 64), (2, 32), (2, 16), (2, 8), (3, 16)])
 def test_gptoss_stack_pipeline_bit_identical(n_stages, micro):
     wl, inp = _stack_inputs(4, 1024, 8)
     d = H.dims(wl.shape)
