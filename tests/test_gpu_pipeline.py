@@ -45,10 +45,10 @@ def _temporal(inp, d):
     return out, tki, tkw, caches
 
 
-def _pipelined(inp, d, n_stages, micro, opts=None, reps=2):
+def _pipelined(inp, d, n_stages, micro, opts=None, reps=2, split=None):
     wl = inp.wl
     T = wl.n_tokens
-    p = sgp.sgp_pipeline_create(d, _splits(n_stages), n_stages, micro, T, wl.cap, opts)
+    p = sgp.sgp_pipeline_create(d, split or _splits(n_stages), n_stages, micro, T, wl.cap, opts)
     try:
         out = torch.empty_like(inp.x)
         tki = torch.zeros(wl.n_layers, T, wl.shape.top_k, dtype=torch.int32, device="cuda")
@@ -84,6 +84,25 @@ def test_gptoss_stack_pipeline_bit_identical(n_stages, micro):
     assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2]), "routing differs"
     for (k0, v0), (k1, v1) in zip(ref[3], inp.caches):
         assert torch.equal(k0, k1) and torch.equal(v0, v1), "KV append differs"
+
+
+def test_pipeline_bit_identical_across_sm_splits():
+    """The SM split decides where and when the work runs, never what it computes: the smallest,
+    a middle and the largest legal stage-A pool (attention on as few as 8-16 SMs, or on almost
+    all of them) give the temporal output, routing and KV appends bit for bit."""
+    wl, inp = _stack_inputs(4, 1024, 8)
+    d = H.dims(wl.shape)
+    ref = _temporal(inp, d)
+    info = sgp.sgp_device_info_get()
+    a = max(1, info.sm_alignment)
+    legal = sgp.sgp_enumerate_splits(info.sm_count, a, max(a, info.sm_min_partition))
+    assert legal
+    for pa in sorted({legal[0], legal[len(legal) // 2], legal[-1]}):
+        got = _pipelined(inp, d, 2, 16, split=[pa, info.sm_count - pa])
+        assert torch.equal(got[0], ref[0]), f"x_out differs at stage-A pool {pa}"
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2]), pa
+        for (k0, v0), (k1, v1) in zip(ref[3], inp.caches):
+            assert torch.equal(k0, k1) and torch.equal(v0, v1), pa
 
 
 def _routing_sets_per_layer(tki, L, k, rows=None):
