@@ -426,3 +426,86 @@ def test_layer_rope_rotates_q_and_new_key_only():
         assert np.array_equal(rot["q"][i], q_ref)
         assert np.array_equal(rot["v_new"][i], plain["v_new"][i])
     assert np.array_equal(rot["q"][0], plain["q"][0])   # L = 1: position 0, no rotation
+
+
+def test_rope_frequencies_written_out_by_hand():
+    """RoFormer's schedule theta_i = theta^(-2(i-1)/d), i = 1..d/2, written out by hand:
+    d = 4, theta = 100 gives angular rates {1, 0.1}; d = 8, theta = 10000 gives
+    {1, 0.1, 0.01, 0.001}.  Pair i is (x_i, x_{i+d/2}) (half-split).  A schedule
+    theta^(-i/d) or a transposed pairing fails here."""
+    x = np.array([1.0, 2.0, 3.0, 4.0])
+    c1, s1, c01, s01 = math.cos(1.0), math.sin(1.0), math.cos(0.1), math.sin(0.1)
+    want = [1 * c1 - 3 * s1, 2 * c01 - 4 * s01, 1 * s1 + 3 * c1, 2 * s01 + 4 * c01]
+    assert np.allclose(O.rope(x, 1, 100.0), want, rtol=0, atol=1e-15)
+    # position 2 doubles every angle
+    c2, s2, c02, s02 = math.cos(2.0), math.sin(2.0), math.cos(0.2), math.sin(0.2)
+    want = [1 * c2 - 3 * s2, 2 * c02 - 4 * s02, 1 * s2 + 3 * c2, 2 * s02 + 4 * c02]
+    assert np.allclose(O.rope(x, 2, 100.0), want, rtol=0, atol=1e-15)
+    # d = 8: unit vectors in the first half pick out (cos, sin) of each rate
+    for i, rate in enumerate((1.0, 0.1, 0.01, 0.001)):
+        e = np.zeros(8)
+        e[i] = 1.0
+        y = O.rope(e, 1, 10000.0)
+        assert math.isclose(y[i], math.cos(rate), rel_tol=0, abs_tol=1e-15)
+        assert math.isclose(y[i + 4], math.sin(rate), rel_tol=0, abs_tol=1e-15)
+        assert np.count_nonzero(y) == 2
+
+
+# ---------------------------------------------------------------------------
+# the stack: layer l's output feeds layer l+1, each layer with its own cache
+# ---------------------------------------------------------------------------
+def test_stack_equals_layers_chained_by_hand():
+    """Three layers with windows [2, 0, 4], a separate cache per layer and the token
+    subset [2, 0] (out of order).  The reference chains the pinned one-layer oracle by hand,
+    token by token, each layer on its own copy of its own cache.  A wrong cache per layer,
+    a wrong window, or a row scattered to the wrong token changes the result."""
+    wl = synth.Workload("t", TINY, n_tokens=3, n_layers=3, kv_len=6, kv_sigma=1.0, w_sigma=0.3)
+    seed = 31
+    weights = [{n: (O.f64(v) if v is not None else None)
+                for n, v in synth.layer_weights(wl, l, seed).items()} for l in range(3)]
+    caches = []
+    for l in range(3):
+        k, v = synth.kv_cache(wl, l, seed)
+        caches.append((O.f64(k).copy(), O.f64(v).copy()))
+    x = O.f64(synth.x_in(wl, seed))
+    kvl = np.array([6, 4, 5])
+    windows = [2, 0, 4]
+    tokens = [2, 0]
+    ref_caches = [(k.copy(), v.copy()) for k, v in caches]
+    untouched = [(k.copy(), v.copy()) for k, v in caches]
+    r = O.stack(TINY, weights, windows, x, kvl, caches, tokens=tokens)
+
+    for i, t in enumerate(tokens):
+        cur = x.copy()
+        for l in range(3):
+            one = O.layer(TINY, weights[l], cur, kvl, ref_caches[l][0], ref_caches[l][1],
+                          windows[l], tokens=[t])
+            cur = cur.copy()
+            cur[t] = one["x_next"][0]
+            assert np.array_equal(r["idx"][l][i], one["idx"][0])
+            assert np.array_equal(r["w"][l][i], one["w"][0])
+            assert np.array_equal(r["logits"][l][i], one["logits"][0])
+        assert np.array_equal(r["x_out"][i], cur[t])
+    # every layer's cache received its own appended rows, and only the listed tokens'
+    for l in range(3):
+        assert np.array_equal(caches[l][0], ref_caches[l][0])
+        assert np.array_equal(caches[l][1], ref_caches[l][1])
+        assert np.array_equal(caches[l][0][1], untouched[l][0][1])
+        for t in tokens:
+            assert not np.array_equal(caches[l][0][t, :, kvl[t] - 1], untouched[l][0][t, :, kvl[t] - 1])
+    # the layers differ from each other, so a shared cache or weight set would be visible
+    assert not np.array_equal(r["idx"][0], r["idx"][1]) or not np.array_equal(r["w"][0], r["w"][1])
+
+
+def test_steady_state_period_is_the_growth_rate_of_the_makespan():
+    """Each extra microbatch adds the slowest stage's time to the Eq. 4-5 makespan of a
+    chain pipeline: the steady-state period is max_d tau_d."""
+    rnd = random.Random(5)
+    for _ in range(20):
+        K = rnd.randint(2, 4)
+        tau_st = [rnd.uniform(0.2, 3.0) for _ in range(K)]
+        spans = []
+        for m in (6, 7):
+            tasks = S.build_tasks(1, m, K)
+            spans.append(S.makespan(tasks, [tau_st[t["seg"] - 1] for t in tasks])[0])
+        assert math.isclose(spans[1] - spans[0], S.steady_state_period(tau_st), rel_tol=1e-12)
