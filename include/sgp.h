@@ -74,9 +74,10 @@ enum {
     SGP_PATH_TC = 2     /* always the tcgen05 tensor-core GEMM                                  */
 };
 
-/* Layer dimensions.  Up to 512 sequences per call.  Supported: head_dim == 64; hidden, inter and n_q_heads*head_dim
- * multiples of 64; n_q_heads a multiple of n_kv_heads with n_q_heads/n_kv_heads <= 16;
- * top_k <= 8; n_experts <= 1024; n_local_experts <= n_experts. */
+/* Layer dimensions.  Up to 512 sequences per call.  Supported: head_dim == 64; hidden, inter
+ * and n_q_heads*head_dim multiples of 64; hidden <= 4096 (the router keeps rows of H in shared
+ * memory); n_q_heads a multiple of n_kv_heads with n_q_heads/n_kv_heads <= 16; top_k <= 8;
+ * n_experts <= 1024; n_local_experts <= n_experts. */
 typedef struct sgp_dims {
     int hidden;           /* H                                                       */
     int n_q_heads;        /* query heads                                             */
@@ -221,22 +222,26 @@ int sgp_status_from_workspace(const void* workspace, sgp_stream_t stream);
  * selected logits) for one layer, and it allocates nothing.  The paper has no counterpart;
  * it is an interface convenience.
  *
- * Its scratch (fp32 logits, arrival counters, a status word) is a fixed array inside the
- * library: at most 262,144 logits, i.e. n_tokens * n_experts <= 262144 (for example 256
- * tokens x 1024 experts), about 1 MiB, which every GPU that loads the library keeps until
- * the process exits.  The first call on a device looks up that array's device address (with
- * the device current) and caches it; make that first call before any stream capture.
- * Every call shares the array: the counters are cleared on `stream` at the start of each
- * call, the logits keep the last call's values, and calls that overlap on the GPU (two
- * streams, or two host threads) race -- serialise them.
+ * Its scratch (fp32 logits and arrival counters) is a fixed array inside the library: at most
+ * 262,144 logits, i.e. n_tokens * n_experts <= 262144 (for example 256 tokens x 1024 experts),
+ * about 1 MiB, which every GPU that loads the library keeps until the process exits.  The
+ * first call on a device does a one-time set-up with that device current: it looks up the
+ * array's device address and prepares both router kernel variants (their shared-memory
+ * limit), and it caches both; make that first call before any stream capture.  Every call
+ * shares the array: the counters are cleared on `stream` at the start of each call, the
+ * logits keep the last call's values, and calls that overlap on the GPU (two streams, or two
+ * host threads) race -- serialise them.
  *
  *   h          device bf16 [n_tokens][H]   residual stream after the attention block
  *   g_mlp      device bf16 [H];  w_router device bf16 [E][H];  router_bias device fp32 [E] or NULL
  *   u_out      device bf16 [n_tokens][H]   RMSNorm(h; g_mlp), as the layer computes it
  *   topk_idx   device int32 [n_tokens][k]; topk_w device fp32 [n_tokens][k]
  * Results equal those sgp_layer_temporal produces for the same h.  Returns SGP_OK,
- * SGP_ERR_INVALID_ARG (NULL or unaligned pointer, unsupported dims, or a size beyond the
- * fixed scratch; nothing is launched) or SGP_ERR_CUDA. */
+ * SGP_ERR_INVALID_ARG (NULL or unaligned pointer, unsupported dims (hidden above 4096
+ * included), or a size beyond the fixed scratch; nothing is launched) or SGP_ERR_CUDA.  The
+ * return code is the whole error report: the router kernel has no device-side error path (it
+ * waits on nothing and indexes only within the sizes checked here), so no status is deferred
+ * to the device. */
 int sgp_router_topk_noalloc(const sgp_dims* dims, const void* h, const void* g_mlp,
                             const void* w_router, const float* router_bias, int n_tokens,
                             void* u_out, int32_t* topk_idx, float* topk_w, sgp_stream_t stream);
@@ -298,15 +303,20 @@ int sgp_pipeline_create(const sgp_dims* dims, const int* sm_split, int n_stages,
  * waits for its data predecessor (the previous segment of microbatch mu) and for the task
  * before it on stage s in the global dispatch order (Section 3.2).  The DAG is a CUDA graph
  * (built on the first run with these arguments, then replayed); it starts after the work
- * already queued on `stream` and `stream` waits for it.  No host round trip inside a run.
+ * already queued on `stream` and `stream` waits for it.  Runs of one pipeline may use
+ * different streams: each run is also ordered after the pipeline's previous run (an event
+ * wait), since they share its flags and scratch.  The call does not wait for the GPU and
+ * makes no host round trip inside a run.
  * Arguments as sgp_stack_temporal; layers is a host array read during this call only.
- * Returns SGP_OK, SGP_ERR_INVALID_ARG, SGP_ERR_CUDA, or a device status left by a previous
- * run that was never synchronised. */
+ * Returns SGP_OK, SGP_ERR_INVALID_ARG, SGP_ERR_CUDA, or the device status left by an earlier
+ * run that has already completed (read from a host copy, without waiting; a run still in
+ * flight reports through sgp_pipeline_sync or a later run). */
 int sgp_pipeline_run(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
                      const int32_t* kv_len, const void* x_in, void* x_out, int n_tokens,
                      int32_t* topk_idx, float* topk_w, sgp_stream_t stream);
 
-/* Waits for the last run and returns its device status (then clears it). */
+/* Waits for the last run (its completion event) and returns the device status recorded since
+ * the status was last read (then clears it). */
 int sgp_pipeline_sync(sgp_pipeline* p);
 
 /* Times each stage's tasks of one run alone on its own SM pool (no other stage active),

@@ -596,12 +596,12 @@ __global__ void __launch_bounds__(kCombThreads, WIDE ? 1 : 2)
 
 // ---------------------------------------------------------------------------------------
 // Router without device allocation (see sgp_router_topk_noalloc in sgp.h).  The scratch the
-// router needs -- fp32 logits, per-token-group arrival counters and a status word -- lives
-// in this fixed array; every GPU that loads the library holds it until the process exits.
+// router needs -- fp32 logits and per-token-group arrival counters -- lives in this fixed
+// array; every GPU that loads the library holds it until the process exits.
 // ---------------------------------------------------------------------------------------
 constexpr size_t kNoallocLogits = 256 * 1024;                    // fp32 logits (1 MiB)
 constexpr size_t kNoallocCounters = 256;                         // u32 token-group counters
-constexpr size_t kNoallocBytes = kNoallocLogits * 4 + kNoallocCounters * 4 + 64;
+constexpr size_t kNoallocBytes = kNoallocLogits * 4 + kNoallocCounters * 4;
 static __device__ __align__(256) unsigned char g_router_scratch[kNoallocBytes];
 
 int enqueue_rmsnorm(Launcher& L, const NormProblem& p, const KCtx& c) {
@@ -678,11 +678,41 @@ int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c) {
 
 }  // namespace sgp
 
-// Host side of the allocation-free router.  The device address of g_router_scratch is
-// fetched once per device (with that device current) and cached.
+// Host side of the allocation-free router.  Once per device (with that device current) the
+// set-up looks up the device address of g_router_scratch and prepares both router kernel
+// instances for the largest dynamic shared memory the device allows, so that no later call
+// touches a kernel attribute; the per-instance limits decide which sizes are refused.
 namespace {
+struct NoallocDev {
+    bool ready = false;
+    void* scratch = nullptr;
+    size_t smem_limit[2] = {0, 0};  // router_kernel<8>, router_kernel<16>
+};
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[128];
+NoallocDev g_noalloc[128];
+
+int noalloc_setup(int dev, NoallocDev& s) {
+    using namespace sgp;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_router_scratch) != cudaSuccess || p == nullptr)
+        return SGP_ERR_CUDA;
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return SGP_ERR_CUDA;
+    const void* fns[2] = {(const void*)router_kernel<8>, (const void*)router_kernel<16>};
+    for (int i = 0; i < 2; ++i) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, fns[i]) != cudaSuccess) return SGP_ERR_CUDA;
+        const int dyn = optin - (int)fa.sharedSizeBytes;
+        if (dyn <= 0 ||
+            cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess)
+            return SGP_ERR_CUDA;
+        s.smem_limit[i] = (size_t)dyn;
+    }
+    s.scratch = p;
+    s.ready = true;
+    return SGP_OK;
+}
 }  // namespace
 
 extern "C" int sgp_router_topk_noalloc(const sgp_dims* d, const void* h, const void* g_mlp,
@@ -692,7 +722,7 @@ extern "C" int sgp_router_topk_noalloc(const sgp_dims* d, const void* h, const v
     using namespace sgp;
     if (!d || !h || !g_mlp || !w_router || !u_out || !topk_idx || !topk_w)
         return SGP_ERR_INVALID_ARG;
-    if (d->hidden <= 0 || d->hidden % 64 || d->hidden > 8192 || d->top_k < 1 || d->top_k > 8 ||
+    if (d->hidden <= 0 || d->hidden % 64 || d->hidden > 4096 || d->top_k < 1 || d->top_k > 8 ||
         d->n_experts < d->top_k || d->n_experts > 1024 || !(d->rms_eps > 0.f))
         return SGP_ERR_INVALID_ARG;
     const void* ptrs[] = {h, g_mlp, w_router, u_out};
@@ -705,23 +735,23 @@ extern "C" int sgp_router_topk_noalloc(const sgp_dims* d, const void* h, const v
         return SGP_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return SGP_ERR_CUDA;
-    void* base = nullptr;
+    NoallocDev st;
     {
         std::lock_guard<std::mutex> lk(g_noalloc_mu);
-        if (g_noalloc_ptr[dev] == nullptr) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_router_scratch) != cudaSuccess || p == nullptr)
-                return SGP_ERR_CUDA;
-            g_noalloc_ptr[dev] = p;
+        if (!g_noalloc[dev].ready) {
+            const int r = noalloc_setup(dev, g_noalloc[dev]);
+            if (r != SGP_OK) return r;
         }
-        base = g_noalloc_ptr[dev];
+        st = g_noalloc[dev];
     }
-    float* logits = reinterpret_cast<float*>(base);
+    const int ne = router_experts_per_cta(d->hidden, d->n_experts, n_tokens);
+    const size_t smem = router_smem_bytes(d->hidden, d->n_experts, ne);
+    if (smem > st.smem_limit[ne == 16 ? 1 : 0]) return SGP_ERR_INVALID_ARG;  // nothing launched
+    float* logits = reinterpret_cast<float*>(st.scratch);
     uint32_t* cnt = reinterpret_cast<uint32_t*>(logits + kNoallocLogits);
-    uint32_t* status = cnt + kNoallocCounters;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // counters (and the status word) must start at zero; the logits need no clearing
-    if (cudaMemsetAsync(cnt, 0, kNoallocCounters * 4 + 64, s) != cudaSuccess) return SGP_ERR_CUDA;
+    // the arrival counters must start at zero; the logits need no clearing
+    if (cudaMemsetAsync(cnt, 0, kNoallocCounters * 4, s) != cudaSuccess) return SGP_ERR_CUDA;
     RouterProblem p;
     memset(&p, 0, sizeof(p));
     p.h = reinterpret_cast<const bf16*>(h);
@@ -739,16 +769,12 @@ extern "C" int sgp_router_topk_noalloc(const sgp_dims* d, const void* h, const v
     p.E = d->n_experts;
     p.k = d->top_k;
     p.eps = d->rms_eps;
+    // the router kernel has no device-side error path (no waits, no data-dependent indexing
+    // beyond the sizes checked above), so it gets no status word
     KCtx c;
     memset(&c, 0, sizeof(c));
-    c.status = status;
     c.timeout_ns = 2000000000ull;
-    const int ne = router_experts_per_cta(d->hidden, d->n_experts, n_tokens);
     const void* fn = ne == 16 ? (const void*)router_kernel<16> : (const void*)router_kernel<8>;
-    const size_t smem = router_smem_bytes(d->hidden, d->n_experts, ne);
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return SGP_ERR_CUDA;
     void* args[] = {(void*)&p, (void*)&c};
     dim3 grid(groups, (d->n_experts + ne - 1) / ne);
     if (cudaLaunchKernel(fn, grid, dim3(kRouterWarps * 32), args, smem, s) != cudaSuccess)

@@ -242,7 +242,8 @@ int check_dims(const sgp_dims* d) {
     if (!(d->rms_eps > 0.f)) return fail_arg("rms_eps must be positive");
     if (!(d->comm_floor_us >= 0.f && d->comm_floor_us <= 1e5f) || !(d->comm_gbps >= 0.f))
         return fail_arg("comm_floor_us must be in [0, 1e5] and comm_gbps >= 0");
-    if (d->hidden > 8192) return fail_arg("hidden above 8192 is not supported");
+    // the router keeps 25 rows of H bf16 in shared memory (about 205 KB at H = 4096)
+    if (d->hidden > 4096) return fail_arg("hidden above 4096 is not supported");
     return SGP_OK;
 }
 
@@ -1074,6 +1075,11 @@ struct sgp_pipeline {
     std::vector<PTask> tasks;
     cudaStream_t last_stream = nullptr;
     int trace_pairs = 0;  // launch-trace pairs the cached graph writes
+    // completion of the last run (recorded on its stream after its status copy) and a pinned
+    // host copy of the device status word as that run left it
+    cudaEvent_t done = nullptr;
+    uint32_t* host_status = nullptr;
+    bool launched = false;
 };
 
 namespace {
@@ -1382,6 +1388,13 @@ extern "C" int sgp_pipeline_create(const sgp_dims* d, const int* sm_split, int n
         sgp_pipeline_destroy(p);
         return r;
     }
+    cudaError_t ce = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
+    if (ce == cudaSuccess) ce = cudaHostAlloc((void**)&p->host_status, 16, cudaHostAllocDefault);
+    if (ce != cudaSuccess) {
+        sgp_pipeline_destroy(p);
+        return fail_cuda(ce, "pipeline completion event / status copy");
+    }
+    memset(p->host_status, 0, 16);
     *out = p;
     return SGP_OK;
 }
@@ -1389,6 +1402,7 @@ extern "C" int sgp_pipeline_create(const sgp_dims* d, const int* sm_split, int n
 static int read_status(sgp_pipeline* p) {
     uint32_t st[4] = {0, 0, 0, 0};
     CK(cudaMemcpy(st, p->ws + p->lay.status, sizeof(st), cudaMemcpyDeviceToHost));
+    if (p->host_status) p->host_status[0] = 0;
     if (st[0]) {
         CK(cudaMemset(p->ws + p->lay.status, 0, sizeof(st)));
         char buf[96];
@@ -1425,12 +1439,18 @@ extern "C" int sgp_pipeline_run(sgp_pipeline* p, const sgp_layer* layers, int n_
     if ((r = pipeline_prepare(p, layers, n_layers, kv_len, x_in, x_out, n_tokens)) != SGP_OK)
         return r;
     cudaStream_t s = (cudaStream_t)stream;
-    // report a device error of an earlier, never-synchronised run
-    if (p->last_stream != nullptr || p->exec != nullptr) {
-        uint32_t st0 = 0;
-        CK(cudaMemcpyAsync(&st0, p->ws + p->lay.status, 4, cudaMemcpyDeviceToHost, s));
-        CK(cudaStreamSynchronize(s));
-        if (st0) return read_status(p);
+    if (p->launched) {
+        // a device error of an earlier run that has completed: read from the pinned copy
+        // that run left, without waiting for anything
+        const cudaError_t q = cudaEventQuery(p->done);
+        if (q == cudaSuccess) {
+            if (p->host_status[0]) return read_status(p);
+        } else if (q != cudaErrorNotReady) {
+            return fail_cuda(q, "cudaEventQuery");
+        }
+        // the previous run (whatever stream it used) completes before this one starts: it
+        // shares the pipeline's flags and scratch
+        if (s != p->last_stream) CK(cudaStreamWaitEvent(s, p->done, 0));
     }
     std::vector<uint8_t> key;
     auto add = [&](const void* v, size_t n) {
@@ -1471,14 +1491,16 @@ extern "C" int sgp_pipeline_run(sgp_pipeline* p, const sgp_layer* layers, int n_
         p->tasks = tasks;
     }
     CK(cudaGraphLaunch(p->exec, s));
+    CK(cudaMemcpyAsync(p->host_status, p->ws + p->lay.status, 16, cudaMemcpyDeviceToHost, s));
+    CK(cudaEventRecord(p->done, s));
+    p->launched = true;
     p->last_stream = s;
     return SGP_OK;
 }
 
 extern "C" int sgp_pipeline_sync(sgp_pipeline* p) {
     if (!p) return fail_arg("pipeline is NULL");
-    if (p->last_stream) CK(cudaStreamSynchronize(p->last_stream));
-    CK(cudaDeviceSynchronize());
+    if (p->launched) CK(cudaEventSynchronize(p->done));
     return read_status(p);
 }
 
@@ -1489,6 +1511,7 @@ extern "C" int sgp_pipeline_stage_times(sgp_pipeline* p, const sgp_layer* layers
     if ((r = pipeline_prepare(p, layers, n_layers, kv_len, x_in, x_out, n_tokens)) != SGP_OK)
         return r;
     if (!t_us || reps < 1) return fail_arg("t_us / reps");
+    if (p->launched) CK(cudaEventSynchronize(p->done));  // the last run shares the scratch
     const int m = n_tokens / p->micro;
     std::vector<PTask> tasks = build_tasks(*p, layers, n_layers, m);
     if ((r = ensure_ws(p, n_tokens, (int)tasks.size())) != SGP_OK) return r;
@@ -1556,7 +1579,7 @@ extern "C" int sgp_pipeline_trace(sgp_pipeline* p, uint64_t* t_ns, int max_pairs
     if (!p->exec) return fail_arg("no run yet");
     *n_pairs = p->trace_pairs;
     if (!t_ns || max_pairs <= 0) return SGP_OK;
-    if (p->last_stream) CK(cudaStreamSynchronize(p->last_stream));
+    if (p->launched) CK(cudaEventSynchronize(p->done));
     const int n = std::min(max_pairs, p->trace_pairs);
     std::vector<unsigned long long> h((size_t)n * 2);
     CK(cudaMemcpy(h.data(), p->ws + p->lay.trace, h.size() * 8, cudaMemcpyDeviceToHost));
@@ -1569,9 +1592,11 @@ extern "C" int sgp_pipeline_trace(sgp_pipeline* p, uint64_t* t_ns, int max_pairs
 
 extern "C" void sgp_pipeline_destroy(sgp_pipeline* p) {
     if (!p) return;
-    if (p->last_stream) cudaStreamSynchronize(p->last_stream);
+    if (p->launched) cudaEventSynchronize(p->done);
     if (p->exec) cudaGraphExecDestroy(p->exec);
     if (p->ws) cudaFree(p->ws);
+    if (p->done) cudaEventDestroy(p->done);
+    if (p->host_status) cudaFreeHost(p->host_status);
     Driver& d = drv();
     for (int i = p->n_gctx - 1; i >= 0; --i)
         if (p->gctx[i] && d.greenDestroy) d.greenDestroy(p->gctx[i]);

@@ -126,7 +126,7 @@ def test_dims_checks_cover_every_documented_limit(lib):
     """check_dims, reached through sgp_workspace_bytes (0 = rejected)."""
     good = _gptoss_dims()
     assert lib.sgp_workspace_bytes(ctypes.byref(good), 64, 8192) > 0
-    edits = [("hidden", 2880 + 32), ("hidden", 8192 + 64), ("inter", 100), ("n_kv_heads", 0),
+    edits = [("hidden", 2880 + 32), ("hidden", 4096 + 64), ("inter", 100), ("n_kv_heads", 0),
              ("n_q_heads", 60), ("n_q_heads", 8 * 17), ("top_k", 0), ("top_k", 9),
              ("n_experts", 2), ("n_experts", 2048), ("n_local_experts", 0),
              ("n_local_experts", 129), ("slot_map", 2), ("path", 3), ("rope_theta", -1.0),
@@ -180,3 +180,28 @@ def test_pipeline_calls_on_a_null_handle(lib):
     assert lib.sgp_pipeline_trace(None, None, 0, ctypes.byref(n)) == E
     assert lib.sgp_pipeline_run(None, None, 1, None, None, None, 64, None, None, None) == E
     lib.sgp_pipeline_destroy(None)  # no-op
+
+
+def test_noalloc_router_refuses_bad_arguments_before_any_device_work(lib):
+    """The allocation-free router checks pointers, dims (hidden above 4096 included: its
+    rows would not fit in shared memory) and the fixed scratch size before any CUDA call."""
+    d = _gptoss_dims()
+    buf = ctypes.create_string_buffer(4096 + 256)
+    base = (ctypes.addressof(buf) + 255) & ~255
+    ok, odd = ctypes.c_void_p(base), ctypes.c_void_p(base + 8)
+    E = sgp.SGP_ERR_INVALID_ARG
+
+    def call(dims, T=64, h=ok, u=ok, idx=ok, w=ok):
+        return lib.sgp_router_topk_noalloc(ctypes.byref(dims), h, ok, ok, None, T, u, idx, w,
+                                           None)
+    assert call(d, h=None) == E
+    assert call(d, idx=None) == E
+    assert call(d, h=odd) == E
+    assert call(d, u=odd) == E
+    assert call(d, T=0) == E
+    big = _gptoss_dims()
+    big.hidden = 4096 + 64
+    assert call(big) == E
+    wide = _gptoss_dims()
+    wide.n_experts = 1024
+    assert call(wide, T=257) == E                 # 257 x 1024 logits exceed the scratch

@@ -61,6 +61,16 @@ def _check_layer(inp, ref, res, T):
     for t in range(T):
         for j in range(s.top_k):
             assert off[slots[t, j]] <= pos[t, j] < off[slots[t, j] + 1]
+    # dispatch is a stable counting sort of the pairs i = t k + j by slot: the slot sizes are
+    # the counts, the positions are a permutation of the rows, and inside a slot the rows
+    # follow the pair order (t, j)
+    counts = np.bincount(slots.reshape(-1), minlength=s.n_local_experts)
+    assert off[0] == 0 and np.array_equal(np.diff(off), counts)
+    flat_pos, flat_slot = pos.reshape(-1), slots.reshape(-1)
+    assert np.array_equal(np.sort(flat_pos), np.arange(T * s.top_k))
+    for sl in range(s.n_local_experts):
+        rows = flat_pos[flat_slot == sl]                  # in pair order i = t k + j
+        assert np.array_equal(rows, np.arange(off[sl], off[sl + 1])), sl
     # SwiGLU rows and expert-down rows vs the oracle's per-pick values (matched by expert)
     zr = np.zeros((T * s.top_k, s.inter))
     yr = np.zeros((T * s.top_k, s.hidden))

@@ -300,6 +300,47 @@ def test_macro_cut_bit_identical():
     assert torch.equal(got[0], ref[0])
 
 
+@pytest.mark.parametrize("opt", ["weight_reuse", "serpentine_experts"])
+def test_weight_reuse_and_serpentine_orders_are_bit_identical(opt):
+    """Weight-reuse scheduling (evict-last weight loads for every microbatch but the last) and
+    the serpentine expert walk (odd microbatches visit the expert slots in reverse order)
+    change when and in which order weights are read, never what is summed: the pipelined
+    output, routing and KV appends equal the temporal ones bit for bit."""
+    wl, inp = _stack_inputs(4, 1024, 8)
+    d = H.dims(wl.shape)
+    ref = _temporal(inp, d)
+    full = [1] * sgp.N_OPS
+    full[2] = 0
+    for micro, cut in ((32, None), (16, None), (16, [full, [1] * sgp.N_OPS])):
+        got = _pipelined(inp, d, 2, micro, sgp.make_opts(stage_of_op=cut, **{opt: 1}))
+        assert torch.equal(got[0], ref[0]), (opt, micro)
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2]), (opt, micro)
+        for (k0, v0), (k1, v1) in zip(ref[3], inp.caches):
+            assert torch.equal(k0, k1) and torch.equal(v0, v1), (opt, micro)
+
+
+def test_runs_on_different_streams_are_ordered():
+    """Runs of one pipeline share its flags and scratch; a run issued on another stream waits
+    for the previous run (an event), so alternating streams still give the temporal output."""
+    wl, inp = _stack_inputs(2, 1024, 14)
+    d = H.dims(wl.shape)
+    ref = _temporal(inp, d)
+    T = wl.n_tokens
+    p = sgp.sgp_pipeline_create(d, _splits(2), 2, 16, T, wl.cap)
+    try:
+        out = torch.empty_like(inp.x)
+        s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+        inp.reset_caches()
+        torch.cuda.synchronize()
+        for s in (s1, s2, s1, s2):
+            sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, T, stream=s)
+        assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref[0])
+    finally:
+        sgp.sgp_pipeline_destroy(p)
+
+
 def test_handoff_check_reports_missing_publish():
     wl, inp = _stack_inputs(2, 256, 11, n_tokens=16)
     d = H.dims(wl.shape)
@@ -310,6 +351,13 @@ def test_handoff_check_reports_missing_publish():
         sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, 16)
         assert sgp.sgp_pipeline_sync(p) == sgp.SGP_ERR_HANDOFF
         assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK     # status cleared after reading
+        # without a sync, the next run reports a completed run's error (read without waiting)
+        sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, 16)
+        torch.cuda.synchronize()
+        with pytest.raises(sgp.SgpError) as e:
+            sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, 16)
+        assert e.value.code == sgp.SGP_ERR_HANDOFF
+        assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK
     finally:
         sgp.sgp_pipeline_destroy(p)
 
