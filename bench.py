@@ -35,7 +35,9 @@ if ROOT not in sys.path:
 
 METRIC = "36-layer decode iteration µs, tokens/s/GPU; DRAM GB/s as % of HBM peak"
 UNIT = "tokens/s"
-ATTN_SRC = os.path.join(ROOT, "intra_spatial_pipelining_gb300", "csrc", "k_attention.cu")
+CSRC = os.path.join(ROOT, "intra_spatial_pipelining_gb300", "csrc")
+# the attention kernel's sources: its own file and the device helpers it includes
+ATTN_SRCS = [os.path.join(CSRC, f) for f in ("k_attention.cu", "common.cuh", "kernels.h")]
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_decode_kernel_gptoss_36l.md")
 
 
@@ -157,7 +159,7 @@ def read_traffic():
         txt = open(TRAFFIC_SUMMARY).read()
     except OSError:
         return None
-    src_hash = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
+    src_hash = attn_source_hash()
     h = t = None
     for line in txt.splitlines():
         if line.startswith("kernel_source_sha256_16:"):
@@ -165,6 +167,43 @@ def read_traffic():
         if line.startswith("dram_bytes_per_full_layer_launch:"):
             t = float(line.split(":", 1)[1].strip())
     return t if (h == src_hash and t) else None
+
+
+def attn_source_hash() -> str:
+    """sha256 (first 16 hex digits) of the attention kernel's source files, concatenated."""
+    h = hashlib.sha256()
+    for f in ATTN_SRCS:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def blas_threads():
+    """Threads of the BLAS thread pool numpy uses (OpenBLAS reports it), or None."""
+    import ctypes
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    try:
+        paths = {ln.split()[-1] for ln in open("/proc/self/maps") if "openblas" in ln.lower()}
+    except OSError:
+        return None
+    for path in sorted(paths):
+        try:
+            h = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                    "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+            f = getattr(h, sym, None)
+            if f is not None:
+                f.restype = ctypes.c_int
+                return int(f())
+    return None
 
 
 class ClockSampler:
@@ -237,7 +276,7 @@ class OracleSample:
     layer.  Inputs are drawn once; run() times only the oracle and scales to the metric:
     tokens/s = 1 / (time per token through all layers)."""
 
-    def __init__(self, wl, seed, n_tok=1, layer_pair=(0, 1)):
+    def __init__(self, wl, seed, n_tok=8, layer_pair=(0, 1)):
         import numpy as np
 
         from intra_spatial_pipelining_gb300 import synth
@@ -252,7 +291,9 @@ class OracleSample:
             kc = np.stack([O.f64(k) for k, _ in caches])
             vc = np.stack([O.f64(v) for _, v in caches])
             self.layers.append((l, w, kc, vc))
-        self.threads = os.cpu_count()
+        import numpy as np
+        np.ones(64) @ np.ones(64)              # load the BLAS before asking for its threads
+        self.threads = blas_threads() or os.cpu_count()
 
     def run(self):
         x = self.x
@@ -265,9 +306,19 @@ class OracleSample:
         per_token_all = secs / self.n_tok * self.wl.n_layers / len(self.layer_pair)
         return 1.0 / per_token_all, secs
 
-    def describe(self, secs):
-        return (f"{self.n_tok} sequence(s) through 1 sliding + 1 full layer per step "
-                f"({secs:.1f} s, fp64 numpy, BLAS default threads), scaled to "
+    def run_for(self, min_secs):
+        """Repeats run() until at least min_secs of oracle time; returns (tokens/s, secs, n)."""
+        vals, secs = [], 0.0
+        while secs < min_secs or not vals:
+            v, t = self.run()
+            vals.append(v)
+            secs += t
+        return statistics.mean(vals), secs, len(vals)
+
+    def describe(self, secs, reps=1):
+        return (f"{self.n_tok} sequences through 1 sliding + 1 full layer, {reps} run(s), "
+                f"{secs:.1f} s of oracle time (fp64 numpy; a single-threaded per-token loop "
+                f"around BLAS calls, BLAS pool of {self.threads} threads), scaled to "
                 f"{self.wl.n_layers} layers")
 
 
@@ -275,7 +326,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     wl = workload(args)
-    smp = OracleSample(wl, args.seed)
+    smp = OracleSample(wl, args.seed, n_tok=4)
     for _ in range(args.warmup):
         smp.run()
     vals, secs = [], 0.0
@@ -290,7 +341,7 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": describe(wl, {"arm": "fp64 CPU oracle"}),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
-                             "sample": smp.describe(secs / args.steps)},
+                             "sample": smp.describe(secs, args.steps)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -452,7 +503,8 @@ def run_sgp(args, rank, world, local_rank):
                "h2d_bytes_per_step": hx.numel() * hx.element_size(),
                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
                "ms_per_step": ms_e2e}
-    n_launch = launches_per_run(make, n_stages, split, micro, opts_kw, layers, kv_len, x, out, T)
+    n_launch, gaps = launches_per_run(make, n_stages, split, micro, opts_kw, layers, kv_len, x,
+                                      out, T)
     if args.virtual_comm:  # the communication kernels record no trace: three per layer and microbatch
         n_launch += 3 * wl.n_layers * (T // micro)
     sgp.sgp_pipeline_destroy(pipe)
@@ -491,9 +543,9 @@ def run_sgp(args, rank, world, local_rank):
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         smp = OracleSample(wl, args.seed)
-        v, secs = smp.run()
+        v, secs, n = smp.run_for(10.0)
         cpu = {"value": v, "unit": UNIT, "cores": smp.threads, "kind": "oracle",
-               "sample": smp.describe(secs)}
+               "sample": smp.describe(secs, n)}
     iter_us = ms_pipe * 1e3
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -524,6 +576,11 @@ def run_sgp(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * n_launch,
+        "handoff_gap_us": None if gaps is None or len(gaps) == 0 else {
+            "median": float(statistics.median(gaps)), "p95": float(sorted(gaps)[int(0.95 * (len(gaps) - 1))]),
+            "max": float(max(gaps)), "edges": len(gaps),
+            "what": "cross-stage task start minus its data producer's end (graph edge between "
+                    "green contexts), from the device launch trace of one run"},
         "clocks": clk,
         "algorithmic_bytes_per_step": total_bytes,
     }
@@ -532,16 +589,20 @@ def run_sgp(args, rank, world, local_rank):
 
 def launches_per_run(make, n_stages, split, micro, opts_kw, layers, kv_len, x, out, T):
     """Kernels one pipelined run launches, counted from the device launch trace of a run of
-    the same configuration (every kernel records its start; fused ops record nothing)."""
+    the same configuration (every kernel records its start; fused ops record nothing), and
+    the cross-stage handoff gaps of that run (us)."""
     from intra_spatial_pipelining_gb300 import sgp
     p = make(n_stages, split, micro, sgp.make_opts(trace=1, **opts_kw))
     try:
         sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
         sgp.check(sgp.sgp_pipeline_sync(p), "traced run")
+        sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)     # a warm replay
+        sgp.check(sgp.sgp_pipeline_sync(p), "traced run")
         tr = sgp.sgp_pipeline_trace(p)
+        gaps = sgp.handoff_gaps_us(p).tolist() if n_stages > 1 else None
     finally:
         sgp.sgp_pipeline_destroy(p)
-    return int((tr[:, 1] > 0).sum())
+    return int((tr[:, 1] > 0).sum()), gaps
 
 
 def main():

@@ -336,6 +336,26 @@ int sgp_pipeline_stage_times(sgp_pipeline* p, const sgp_layer* layers, int n_lay
  * t_ns may be NULL to query n_pairs.  Returns SGP_OK, SGP_ERR_INVALID_ARG or SGP_ERR_CUDA. */
 int sgp_pipeline_trace(sgp_pipeline* p, uint64_t* t_ns, int max_pairs, int* n_pairs);
 
+/* SMs of every launch of the last run (pipeline created with opts.trace = 1): every CTA of a
+ * kernel sets bit %smid (the hardware SM index, below 256) of that launch's mask.  Waits for
+ * the run, then writes n_entries = n_layers * m * SGP_N_OPS * 2 masks of 8 uint32 words
+ * (256 bits) to `masks` (host, at most max_entries), indexed like sgp_pipeline_trace's pairs.
+ * An all-zero mask means no such launch.  Checks the SM partition: the kernels of different
+ * stages must run on disjoint sets of SMs, each no larger than its pool ("SubGPU Pipelining:
+ * Intra-GPU Fine-Grained Spatial Parallelism for LLM Inference", Section 3.1: disjoint SM
+ * pools).  masks may be NULL to query n_entries.
+ * Returns SGP_OK, SGP_ERR_INVALID_ARG or SGP_ERR_CUDA. */
+int sgp_pipeline_trace_sms(sgp_pipeline* p, uint32_t* masks, int max_entries, int* n_entries);
+
+/* Measured span of every task of the last run (pipeline created with opts.trace = 1): the
+ * earliest CTA start of the task's first kernel and the latest CTA end of its last kernel,
+ * on the GPU's global timer (ns), as {start_ns, end_ns} pairs in task order (the order of
+ * sgp_pipeline_tasks).  Waits for the run.  A cross-stage handoff costs the gap between a
+ * task's start and the end of its data predecessor (same paper, Section 3.2, Eq. 4 takes it
+ * as zero).  spans may be NULL to query n_tasks.
+ * Returns SGP_OK, SGP_ERR_INVALID_ARG or SGP_ERR_CUDA. */
+int sgp_pipeline_task_spans(sgp_pipeline* p, uint64_t* spans, int max_tasks, int* n_tasks);
+
 /* Number of tasks of the last run's DAG and, when stamps != NULL, per-task
  * {stage, layer_first, micro, pred_data, pred_stage} as int32[5] rows (host memory). */
 int sgp_pipeline_tasks(sgp_pipeline* p, int* n_tasks, int32_t* rows, int max_rows);

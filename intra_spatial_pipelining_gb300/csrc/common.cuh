@@ -30,6 +30,9 @@ struct KCtx {
     // Optional launch trace [2]: [0] = ~(earliest CTA start), [1] = latest CTA end, both
     // %globaltimer ns, accumulated with atomicMax from a zeroed pair (NULL: off).
     unsigned long long* trace;
+    // Optional SM record [8] (256 bits): every CTA sets bit %smid of the SM it ran on
+    // (atomicOr into a zeroed mask; NULL: off).  Recorded together with the trace.
+    uint32_t* smmask;
 };
 
 enum : uint32_t { FAULT_SKIP_PUBLISH = 1u, FAULT_DROP_TMA = 2u };
@@ -81,6 +84,11 @@ __device__ __forceinline__ void task_end(const KCtx& c) {
     __syncthreads();
     if (threadIdx.x == 0 && c.trace != nullptr)
         atomicMax(&c.trace[1], (unsigned long long)globaltimer());
+    if (threadIdx.x == 0 && c.smmask != nullptr) {
+        uint32_t sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        if (sm < 256) atomicOr(&c.smmask[sm >> 5], 1u << (sm & 31));
+    }
     if (threadIdx.x == 0 && c.post_flag != nullptr) {
         __threadfence();
         uint32_t nblk = gridDim.x * gridDim.y * gridDim.z;

@@ -327,7 +327,7 @@ int attn_smax(int max_kv) { return std::max(1, cdiv(max_kv, kAttnChunk)); }
 struct Layout {
     int T = 0, m = 1, b = 0, S_max = 1, n_flags = 0;
     size_t status = 0, zero_beg = 0, zero_end = 0;
-    size_t attn_cnt = 0, router_cnt = 0, flags = 0, flag_cnt = 0, trace = 0;
+    size_t attn_cnt = 0, router_cnt = 0, flags = 0, flag_cnt = 0, trace = 0, smmask = 0;
     int n_trace = 0;  // trace pairs (0: tracing off)
     size_t a = 0, q = 0, o = 0, h = 0, u = 0;
     size_t per_mu = 0;  // bytes of one microbatch's scratch block
@@ -368,7 +368,10 @@ Layout make_layout(const sgp_dims& d, int T, int m, int max_kv, int n_flags, int
     L.flags = take((size_t)std::max(1, n_flags) * 4);
     L.flag_cnt = take((size_t)std::max(1, n_flags) * 4);
     L.n_trace = n_trace;
-    if (n_trace > 0) L.trace = take((size_t)n_trace * 16);
+    if (n_trace > 0) {
+        L.trace = take((size_t)n_trace * 16);
+        L.smmask = take((size_t)n_trace * 32);  // 8 x u32 per launch
+    }
     L.zero_end = off;
     L.a = take((size_t)T * H * 2);
     L.q = take((size_t)T * qw * 2);
@@ -641,6 +644,7 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     c2.wait_flag = nullptr;
     c2.fault = 0;
     if (c.trace) c2.trace = c.trace + 2;  // the finishing kernel has the op's second slot
+    if (c.smmask) c2.smmask = c.smmask + 8;
     if ((r = enqueue_gemm_tc(L, p, c1)) != 0) return r;
     FinishProblem f;
     memset(&f, 0, sizeof(f));
@@ -665,6 +669,7 @@ void split_for_comm(const KCtx& c, bool comm_last, KCtx& op_ctx, KCtx& comm_ctx)
     op_ctx = c;
     comm_ctx = c;
     comm_ctx.trace = nullptr;
+    comm_ctx.smmask = nullptr;
     if (comm_last) {
         op_ctx.post_flag = nullptr;
         op_ctx.post_cnt = nullptr;
@@ -1212,9 +1217,11 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
                     c.fault |= FAULT_SKIP_PUBLISH;
             }
             if ((p->opts.fault_inject & 2u) && i == 0 && op == SGP_OP_QKV) c.fault |= FAULT_DROP_TMA;
-            if (p->lay.n_trace > 0)
-                c.trace = w.at<unsigned long long>(p->lay.trace) +
-                          4 * (((size_t)l * p->lay.m + t.mu) * SGP_N_OPS + op);
+            if (p->lay.n_trace > 0) {
+                const size_t ent = ((size_t)l * p->lay.m + t.mu) * SGP_N_OPS + op;
+                c.trace = w.at<unsigned long long>(p->lay.trace) + 4 * ent;
+                c.smmask = w.at<uint32_t>(p->lay.smmask) + 16 * ent;
+            }
             RunEnv e{&d, &layers[l], kv_len, (const bf16*)(l == 0 ? x_in : x_out), (bf16*)x_out, T,
                      w, tki ? tki + (size_t)l * T * d.top_k : nullptr,
                      tkw ? tkw + (size_t)l * T * d.top_k : nullptr, tcd, tce,
@@ -1586,6 +1593,54 @@ extern "C" int sgp_pipeline_trace(sgp_pipeline* p, uint64_t* t_ns, int max_pairs
     for (int i = 0; i < n; ++i) {
         t_ns[2 * i] = h[2 * i] ? ~h[2 * i] : 0;  // stored complemented (max of ~t = min t)
         t_ns[2 * i + 1] = h[2 * i + 1];
+    }
+    return SGP_OK;
+}
+
+extern "C" int sgp_pipeline_trace_sms(sgp_pipeline* p, uint32_t* masks, int max_entries,
+                                      int* n_entries) {
+    if (!p || !n_entries) return fail_arg("NULL");
+    if (!p->opts.trace) return fail_arg("pipeline was created without opts.trace");
+    if (!p->exec) return fail_arg("no run yet");
+    *n_entries = p->trace_pairs;
+    if (!masks || max_entries <= 0) return SGP_OK;
+    if (p->launched) CK(cudaEventSynchronize(p->done));
+    const int n = std::min(max_entries, p->trace_pairs);
+    CK(cudaMemcpy(masks, p->ws + p->lay.smmask, (size_t)n * 32, cudaMemcpyDeviceToHost));
+    return SGP_OK;
+}
+
+extern "C" int sgp_pipeline_task_spans(sgp_pipeline* p, uint64_t* spans, int max_tasks,
+                                       int* n_tasks) {
+    if (!p || !n_tasks) return fail_arg("NULL");
+    if (!p->opts.trace) return fail_arg("pipeline was created without opts.trace");
+    if (!p->exec) return fail_arg("no run yet");
+    *n_tasks = (int)p->tasks.size();
+    if (!spans || max_tasks <= 0) return SGP_OK;
+    if (p->launched) CK(cudaEventSynchronize(p->done));
+    std::vector<unsigned long long> h((size_t)p->trace_pairs * 2);
+    CK(cudaMemcpy(h.data(), p->ws + p->lay.trace, h.size() * 8, cudaMemcpyDeviceToHost));
+    const int m = p->lay.m;
+    for (int i = 0; i < (int)p->tasks.size() && i < max_tasks; ++i) {
+        const PTask& t = p->tasks[i];
+        uint64_t first = 0, last = 0;
+        int l = t.l0, op = t.op0;
+        while (true) {
+            for (int part = 0; part < 2; ++part) {
+                const size_t e = ((((size_t)l * m + t.mu) * SGP_N_OPS + op) * 2 + part) * 2;
+                if (e + 1 >= h.size() || h[e + 1] == 0) continue;  // no such launch
+                const uint64_t st = ~h[e], en = h[e + 1];
+                if (first == 0 || st < first) first = st;
+                if (en > last) last = en;
+            }
+            if (l == t.l1 && op == t.op1) break;
+            if (++op == SGP_N_OPS) {
+                op = 0;
+                ++l;
+            }
+        }
+        spans[2 * i] = first;
+        spans[2 * i + 1] = last;
     }
     return SGP_OK;
 }

@@ -99,6 +99,10 @@ _SIGS = {
                                      C.c_int]),
     "sgp_pipeline_trace": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_int,
                                      C.POINTER(C.c_int)]),
+    "sgp_pipeline_trace_sms": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint32), C.c_int,
+                                         C.POINTER(C.c_int)]),
+    "sgp_pipeline_task_spans": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint64), C.c_int,
+                                          C.POINTER(C.c_int)]),
     "sgp_pipeline_destroy": (None, [C.c_void_p]),
     "sgp_enumerate_splits": (C.c_int, [C.c_int, C.c_int, C.c_int, C.POINTER(C.c_int), C.c_int]),
     "sgp_pipeline_balance": (C.c_int, [C.POINTER(sgp_dims), C.POINTER(sgp_layer), C.c_int,
@@ -307,6 +311,48 @@ def sgp_pipeline_trace(p):
     check(lib().sgp_pipeline_trace(p, out.ctypes.data_as(C.POINTER(C.c_uint64)), n.value,
                                    C.byref(n)), "sgp_pipeline_trace")
     return out[:n.value].astype(np.int64)
+
+
+def sgp_pipeline_trace_sms(p):
+    """SM masks of the last run's launches as a uint32 array [n_entries][8] (bit %smid set
+    for every SM a CTA of that launch ran on), indexed like sgp_pipeline_trace."""
+    import numpy as np
+    n = C.c_int()
+    check(lib().sgp_pipeline_trace_sms(p, None, 0, C.byref(n)), "sgp_pipeline_trace_sms")
+    out = np.zeros((max(1, n.value), 8), dtype=np.uint32)
+    check(lib().sgp_pipeline_trace_sms(p, out.ctypes.data_as(C.POINTER(C.c_uint32)), n.value,
+                                       C.byref(n)), "sgp_pipeline_trace_sms")
+    return out[:n.value]
+
+
+def sgp_pipeline_task_spans(p):
+    """Measured (start_ns, end_ns) of every task of the last run, in task order, as an int64
+    array [n_tasks][2]."""
+    import numpy as np
+    n = C.c_int()
+    check(lib().sgp_pipeline_task_spans(p, None, 0, C.byref(n)), "sgp_pipeline_task_spans")
+    out = np.zeros((max(1, n.value), 2), dtype=np.uint64)
+    check(lib().sgp_pipeline_task_spans(p, out.ctypes.data_as(C.POINTER(C.c_uint64)), n.value,
+                                        C.byref(n)), "sgp_pipeline_task_spans")
+    return out[:n.value].astype(np.int64)
+
+
+def handoff_gaps_us(p):
+    """Cross-stage handoff latencies of the last run (traced pipeline): for every task whose
+    data predecessor ran on another stage and finished after the task's stage predecessor
+    (so the handoff was what the task waited for), its start minus that data predecessor's
+    end, in us."""
+    import numpy as np
+    spans = sgp_pipeline_task_spans(p)
+    tasks = sgp_pipeline_tasks(p)
+    gaps = []
+    for i, (st, _, _, pd, ps) in enumerate(tasks):
+        if pd < 0 or tasks[pd][0] == st:
+            continue
+        if ps >= 0 and spans[ps, 1] > spans[pd, 1]:
+            continue
+        gaps.append((spans[i, 0] - spans[pd, 1]) * 1e-3)
+    return np.array(gaps, dtype=np.float64)
 
 
 def sgp_pipeline_destroy(p) -> None:

@@ -260,6 +260,8 @@ def test_measured_task_spans_respect_dag_and_eq4():
             assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK
         tr = sgp.sgp_pipeline_trace(p).reshape(L, m, sgp.N_OPS, 2, 2)
         tasks = sgp.sgp_pipeline_tasks(p)
+        lib_spans = sgp.sgp_pipeline_task_spans(p)
+        gaps = sgp.handoff_gaps_us(p)
     finally:
         sgp.sgp_pipeline_destroy(p)
     ops = {0: range(0, 3), 1: range(3, sgp.N_OPS)}  # default cut
@@ -269,10 +271,14 @@ def test_measured_task_spans_respect_dag_and_eq4():
         k = k[k[:, 1] > 0]
         assert len(k) > 0
         span.append((int(k[:, 0].min()), int(k[:, 1].max())))
+    assert [tuple(r) for r in lib_spans.tolist()] == span     # the library's own task spans
     for i, (st, l, mu, pd, ps) in enumerate(tasks):
         for j in (pd, ps):
             if j >= 0:
                 assert span[i][0] >= span[j][1], (i, j, span[i], span[j])
+    assert len(gaps) > 0 and np.all(gaps >= 0)
+    print(f"cross-stage handoff: median {np.median(gaps):.2f} us, max {gaps.max():.2f} us "
+          f"over {len(gaps)} edges")
     key = {(t[0], t[1], t[2]): i for i, t in enumerate(tasks)}
     model = S.build_tasks(L, m, 2)
     tau = []
@@ -285,6 +291,49 @@ def test_measured_task_spans_respect_dag_and_eq4():
     print(f"Eq. 4-5 makespan of measured durations {t_model:.1f} us, measured {t_meas:.1f} us")
     assert t_model <= t_meas + 1e-6
     assert abs(S.longest_path(model, tau) - t_model) < 1e-6
+
+
+def _sm_set(masks):
+    bits = set()
+    for row in np.asarray(masks).reshape(-1, 8):
+        for w in range(8):
+            v = int(row[w])
+            while v:
+                b = v & -v
+                bits.add(32 * w + b.bit_length() - 1)
+                v ^= b
+    return bits
+
+
+def test_stage_kernels_run_on_disjoint_sm_pools():
+    """Every CTA records the SM it ran on (%smid).  The kernels of stage A and of stage B use
+    disjoint SM sets, each no larger than its pool: a green context that silently fell back to
+    the whole GPU would fail here.  Temporal kernels spread over more SMs than either pool."""
+    wl, inp = _stack_inputs(2, 1024, 15)
+    d = H.dims(wl.shape)
+    T, L, micro = wl.n_tokens, wl.n_layers, 16
+    m = T // micro
+    split = _splits(2)
+    info = sgp.sgp_device_info_get()
+    sets = {}
+    for name, nst, spl, mb in (("pipe", 2, split, micro), ("temporal", 1, [info.sm_count], T)):
+        p = sgp.sgp_pipeline_create(d, spl, nst, mb, T, wl.cap, sgp.make_opts(trace=1))
+        try:
+            out = torch.empty_like(inp.x)
+            inp.reset_caches()
+            sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, T)
+            assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK
+            sets[name] = sgp.sgp_pipeline_trace_sms(p).reshape(L, -1, sgp.N_OPS, 2, 8)
+        finally:
+            sgp.sgp_pipeline_destroy(p)
+    a = _sm_set(sets["pipe"][:, :, 0:3])
+    b = _sm_set(sets["pipe"][:, :, 3:])
+    t = _sm_set(sets["temporal"])
+    print(f"stage A on {len(a)} SMs (pool {split[0]}), stage B on {len(b)} (pool {split[1]}), "
+          f"temporal on {len(t)}")
+    assert a and b and not (a & b)
+    assert len(a) <= split[0] and len(b) <= split[1]
+    assert len(t) > max(split)
 
 
 def test_macro_cut_bit_identical():
