@@ -394,17 +394,17 @@ def run_sgp(args, rank, world, local_rank):
         opts_kw = {"stage_of_op": [full, [1] * sgp.N_OPS]}
         opts = sgp.make_opts(**opts_kw)
     balance_rows = None
+    balance_shared_rows = None
     sweep_rows = None
     balancer_pick = None
-    if n_stages == 1:
-        split = [N]
-    elif args.split in ("auto", "sweep") and n_stages == 2:
-        best, balance_rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro,
-                                                      wl.cap, quantum=8, reps=3, opts=opts)
-        balancer_pick = best
+    balancer_shared_pick = None
+    full_runs = {}
+    refine = None
 
-        def full_run_ms(pa):
-            p = sgp.sgp_pipeline_create(d, [pa, N - pa], 2, micro, T, wl.cap, opts)
+    def full_run_ms(spl):
+        key = tuple(spl)
+        if key not in full_runs:
+            p = sgp.sgp_pipeline_create(d, list(spl), len(spl), micro, T, wl.cap, opts)
             sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
             sgp.check(sgp.sgp_pipeline_sync(p), "pipeline")
             t0 = torch.cuda.Event(enable_timing=True)
@@ -416,25 +416,57 @@ def run_sgp(args, rank, world, local_rank):
             t1.synchronize()
             sgp.check(sgp.sgp_pipeline_sync(p), "pipeline")
             sgp.sgp_pipeline_destroy(p)
-            return t0.elapsed_time(t1) / 3
+            full_runs[key] = t0.elapsed_time(t1) / 3
+        return full_runs[key]
 
+    if n_stages == 1:
+        split = [N]
+    elif args.split in ("auto", "sweep") and n_stages == 2:
+        # the t_A / t_B balancer, with each stage timed alone and with both stages running
+        # at once (sharing HBM and L2 as in a pipelined run)
+        best, balance_rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro,
+                                                      wl.cap, quantum=8, reps=3, opts=opts)
+        balancer_pick = best
+        shared_opts = sgp.make_opts(stage_times_shared=1, **opts_kw)
+        balancer_shared_pick, balance_shared_rows = sgp.sgp_pipeline_balance(
+            d, layers, kv_len, x, out, T, micro, wl.cap, quantum=8, reps=3, opts=shared_opts)
         if args.split == "sweep":
-            # every legal split as a full pipelined run: the balancer's pick against the best
-            sweep_rows = [(r[0], full_run_ms(r[0])) for r in balance_rows]
+            # every legal split as a full pipelined run: the balancer's picks against the best
+            sweep_rows = [(r[0], full_run_ms([r[0], N - r[0]])) for r in balance_rows]
             best = min(sweep_rows, key=lambda r: r[1])[0]
         else:
-            # check the model's pick against full pipelined runs of the best few candidates
-            ranked = sorted(balance_rows, key=lambda r: max(r[1], r[2]))[:4]
-            best_t = None
-            for pa, _, _ in ranked:
-                ms = full_run_ms(pa)
-                if best_t is None or ms < best_t:
-                    best_t, best = ms, pa
+            # check each model's best few candidates with full pipelined runs
+            cands = []
+            for rows in (balance_shared_rows, balance_rows):
+                for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:3]:
+                    if r[0] not in cands:
+                        cands.append(r[0])
+            best = min(cands, key=lambda pa: full_run_ms([pa, N - pa]))
         split = [best, N - best]
     elif args.split == "auto":
+        # 3 stages: pairwise-line refinement (Algorithm 2) on measured full runs, from a uniform
+        # seed and from a service-proportional one (SMs in proportion to each stage's work)
         a = max(1, info.sm_alignment)
+        pmin = max(a, info.sm_min_partition)
         p0 = max(a, (N // 3 // a) * a)
-        split = [p0, p0, N - 2 * p0]
+        uni = [p0, p0, N - 2 * p0]
+        pp = sgp.sgp_pipeline_create(d, uni, 3, micro, T, wl.cap, opts)
+        try:
+            t_uni = sgp.sgp_pipeline_stage_times(pp, layers, kv_len, x, out, T, 3, reps=3)
+        finally:
+            sgp.sgp_pipeline_destroy(pp)
+        work = [t * p for t, p in zip(t_uni, uni)]
+        prop = [max(pmin, int(round(N * w / sum(work) / a)) * a) for w in work]
+        prop[-1] = N - sum(prop[:-1])
+        seeds = [uni] + ([prop] if prop != uni and min(prop) >= pmin else [])
+        refine = {"seeds": [], "stage_times_uniform_us": t_uni}
+        best_t = None
+        for sd in seeds:
+            spl, t_us, n_ev = sgp.sgp_pipeline_refine(d, layers, kv_len, x, out, T, sd, micro,
+                                                      wl.cap, quantum=a, reps=3, opts=opts)
+            refine["seeds"].append({"seed": sd, "refined": spl, "us": t_us, "evaluations": n_ev})
+            if best_t is None or t_us < best_t:
+                best_t, split = t_us, spl
     else:
         split = [int(v) for v in args.split.split(",")]
 
@@ -568,6 +600,12 @@ def run_sgp(args, rank, world, local_rank):
             "pipeline_speedup": ms_temp / ms_pipe},
         "balance": None if balance_rows is None else [
             {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in balance_rows],
+        "balance_shared": None if balance_shared_rows is None else [
+            {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in balance_shared_rows],
+        "balancer_picks": None if balancer_pick is None else {
+            "alone": balancer_pick, "shared": balancer_shared_pick, "chosen": split[0],
+            "full_run_us": {str(k[0]): v * 1e3 for k, v in sorted(full_runs.items())}},
+        "refine_3_stage": refine,
         "split_sweep": None if sweep_rows is None else {
             "balancer_pick": balancer_pick,
             "sweep_best": min(sweep_rows, key=lambda r: r[1])[0],

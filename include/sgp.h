@@ -284,6 +284,21 @@ typedef struct sgp_pipeline_opts {
                                    microbatch rereads them), the last microbatch's with
                                    evict-first; 0 = default (off: every weight load is
                                    evict-first; the hint measured no faster here)           */
+    int l2_prefetch_mb;         /* L2 prefetch of the next projection's weights, issued beside
+                                   the chain (a prefetch kernel that no launch waits for) once
+                                   a projection's main kernel completes, so that HBM moves
+                                   them while the kernels in between leave it idle: QKV ->
+                                   output projection, output projection -> expert gate/up,
+                                   expert gate/up -> expert down, expert down -> the next
+                                   layer's QKV.  Dense matrices are prefetched whole, expert
+                                   matrices up to this many MB; 0 = default (off: measured
+                                   slower on the 36-layer slice).  Only timing changes;
+                                   results are bit-identical                                  */
+    int stage_times_shared;     /* sgp_pipeline_stage_times and the balancer: 0 = default, each
+                                   stage timed alone on the GPU; 1 = all stages replay their
+                                   tasks at the same time, so each is timed while the others
+                                   share HBM and L2 with it (the contention a pipelined run
+                                   sees)                                                      */
 } sgp_pipeline_opts;
 
 /* Creates a pipeline for up to max_tokens sequences with KV length <= max_kv_len.
@@ -319,10 +334,11 @@ int sgp_pipeline_run(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
  * the status was last read (then clears it). */
 int sgp_pipeline_sync(sgp_pipeline* p);
 
-/* Times each stage's tasks of one run alone on its own SM pool (no other stage active),
- * CUDA events, median of `reps` replays; writes n_stages values (microseconds) to t_us.
- * Data dependencies between stages are dropped, so outputs are meaningless; the caller's
- * buffers are written as by a run.  Synchronous. */
+/* Times each stage's tasks of one run on its own SM pool, CUDA events, median of `reps`
+ * replays; writes n_stages values (microseconds) to t_us.  Alone on the GPU by default; with
+ * opts.stage_times_shared all stages replay at the same time.  Data dependencies between
+ * stages are dropped, so outputs are meaningless; the caller's buffers are written as by a
+ * run.  Synchronous. */
 int sgp_pipeline_stage_times(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
                              const int32_t* kv_len, const void* x_in, void* x_out,
                              int n_tokens, int reps, float* t_us);
@@ -380,6 +396,46 @@ int sgp_pipeline_balance(const sgp_dims* dims, const sgp_layer* layers, int n_la
                          int microbatch, int max_kv_len, int quantum, int reps,
                          const sgp_pipeline_opts* opts, int* best_split_out, int* splits,
                          float* t_us, int max_out, int* n_out);
+
+/* ---- SM-allocation refinement for any stage count ---------------------------------- */
+
+/* Objective of an SM allocation p[0..n_stages-1] (each entry a stage's SMs): lower is better;
+ * a negative (or NaN) value marks an allocation that cannot be evaluated (treated as
+ * infinitely bad).  ctx is passed through. */
+typedef double (*sgp_alloc_objective)(const int* p, int n_stages, void* ctx);
+
+/* Pairwise-line SM-allocation refinement ("SubGPU Pipelining: Intra-GPU Fine-Grained
+ * Spatial Parallelism for LLM Inference", Section 4.2, Algorithm 2).  A move hands z * quantum
+ * SMs from a donor stage to a receiver stage; the total stays fixed.  Each pass evaluates
+ * every legal one-quantum move, takes the best (the first in (donor, receiver) order on
+ * ties); if it beats the current value, a line search along that pair doubles the step
+ * while the objective keeps improving and halves it otherwise; the allocation then moves to
+ * the best point found.  The search stops when no legal move improves or after pass_limit
+ * passes (<= 0: no limit).  A legal allocation has every entry >= max(p_min, quantum).
+ * Objective values are memoised per allocation.
+ *   p_inout  host int[n_stages]: the initial allocation (legal), replaced by the refined one
+ *   t_out    host, or NULL: the refined allocation's objective
+ * Host only, no device work of its own.  Returns the number of distinct allocations
+ * evaluated (>= 1), or SGP_ERR_INVALID_ARG (2 <= n_stages <= 8). */
+int sgp_refine_allocation(int n_stages, int* p_inout, int quantum, int p_min, int pass_limit,
+                          sgp_alloc_objective f, void* ctx, double* t_out);
+
+/* Pairwise-line refinement (sgp_refine_allocation) of a pipeline's SM allocation against
+ * measured time: the objective of an allocation is the median of `reps` full pipelined runs
+ * of the given layers (after one warm-up run), each a fresh pipeline with that split, the
+ * same microbatch and opts.  The quantum is raised to the device's green-context alignment
+ * and the minimum pool to its minimum partition.  Splits the device cannot form count as
+ * infeasible.  For any stage count (2 or 3 here; Section 4.2 uses it for D >= 3).
+ *   split_inout  host int[n_stages]: a legal starting allocation, replaced by the refined one
+ *   t_us_out     host or NULL: the refined allocation's measured time (us)
+ *   n_evals      host or NULL: distinct allocations measured
+ * Synchronous.  Returns SGP_OK, SGP_ERR_INVALID_ARG, SGP_ERR_UNSUPPORTED, SGP_ERR_CUDA or a
+ * device status of a measured run. */
+int sgp_pipeline_refine(const sgp_dims* dims, const sgp_layer* layers, int n_layers,
+                        const int32_t* kv_len, const void* x_in, void* x_out, int n_tokens,
+                        int n_stages, int microbatch, int max_kv_len, int quantum, int reps,
+                        int pass_limit, const sgp_pipeline_opts* opts, int* split_inout,
+                        float* t_us_out, int* n_evals);
 
 #ifdef __cplusplus
 }

@@ -658,6 +658,46 @@ __global__ void __launch_bounds__(256) comm_kernel(const CommProblem P, const KC
     task_end(ctx);
 }
 
+// ---------------------------------------------------------------------------------------
+// L2 prefetch of the weights of a coming projection, run beside the chain while the kernels
+// before that projection leave HBM idle (a finishing pass, the router and dispatch, the
+// combine).  Consecutive chunks go to different CTAs, so the bulk prefetches are issued by
+// the TMA units of many SMs at once.
+// ---------------------------------------------------------------------------------------
+constexpr uint32_t kPrefetchChunk = 32768;
+
+__global__ void __launch_bounds__(32) prefetch_kernel(const PrefetchProblem P, const KCtx ctx) {
+    griddep_launch();
+    griddep_wait();
+    task_begin(ctx);
+    const uint64_t pol = policy_evict_last();
+    const size_t n0 = (P.bytes[0] + kPrefetchChunk - 1) / kPrefetchChunk;
+    const size_t n1 = (P.bytes[1] + kPrefetchChunk - 1) / kPrefetchChunk;
+    for (size_t c = (size_t)threadIdx.x * gridDim.x + blockIdx.x; c < n0 + n1;
+         c += (size_t)gridDim.x * blockDim.x) {
+        const bool first = c < n0;
+        const size_t off = (first ? c : c - n0) * kPrefetchChunk;
+        const size_t left = (first ? P.bytes[0] : P.bytes[1]) - off;
+        const uint32_t nb = (uint32_t)(left < kPrefetchChunk ? left : kPrefetchChunk);
+        const char* src = static_cast<const char*>(first ? P.base[0] : P.base[1]) + off;
+        asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+                     "r"(nb), "l"(pol)
+                     : "memory");
+    }
+    task_end(ctx);
+}
+
+int enqueue_prefetch(Launcher& L, const PrefetchProblem& p, const KCtx& c) {
+    for (int r = 0; r < 2; ++r)
+        if ((reinterpret_cast<uintptr_t>(p.base[r]) & 15) || (p.bytes[r] & 15) ||
+            (p.bytes[r] && !p.base[r]))
+            return (int)cudaErrorInvalidValue;
+    if (p.bytes[0] + p.bytes[1] == 0) return 0;
+    void* args[] = {(void*)&p, (void*)&c};
+    return L.launch_side((const void*)prefetch_kernel, dim3(std::max(1, p.grid)), dim3(32), 0,
+                         args);
+}
+
 int enqueue_comm(Launcher& L, const CommProblem& p, const KCtx& c) {
     if (((reinterpret_cast<uintptr_t>(p.src) | reinterpret_cast<uintptr_t>(p.dst)) & 15) ||
         p.floor_ns > 1000000000ull)

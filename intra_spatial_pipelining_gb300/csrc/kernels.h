@@ -21,6 +21,13 @@ struct Launcher {
     // touches memory the predecessor writes after griddep_wait)
     virtual int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args,
                        bool overlap_ok = false) = 0;
+    // A launch beside the chain: it starts once the chain's last launch so far has completed,
+    // and nothing in the chain waits for it.  For work whose effect is only on timing (an L2
+    // prefetch); a launcher without side branches drops it.
+    virtual int launch_side(const void* func, dim3 grid, dim3 block, size_t smem, void** args) {
+        (void)func, (void)grid, (void)block, (void)smem, (void)args;
+        return 0;
+    }
 };
 
 // --------------------------------------------------------------------------------------
@@ -184,6 +191,14 @@ struct CombineProblem {
     float eps;
 };
 
+// L2 prefetch of up to two byte ranges (16-byte aligned, multiples of 16 bytes), with an
+// evict-last hint so that the lines stay until the projection that reads them.
+struct PrefetchProblem {
+    const void* base[2];
+    size_t bytes[2];
+    int grid;               // CTAs (one warp each), spread over the pool's SMs
+};
+
 // Virtual communication: copy `bytes` (a multiple of 16) from src to dst, lasting at least
 // floor_ns from the moment the payload is ready.
 struct CommProblem {
@@ -198,6 +213,7 @@ struct CommProblem {
 // --------------------------------------------------------------------------------------
 int enqueue_rmsnorm(Launcher& L, const NormProblem& p, const KCtx& c);
 int enqueue_comm(Launcher& L, const CommProblem& p, const KCtx& c);
+int enqueue_prefetch(Launcher& L, const PrefetchProblem& p, const KCtx& c);
 int enqueue_router(Launcher& L, const RouterProblem& p, const KCtx& c);
 int enqueue_dispatch(Launcher& L, const DispatchProblem& p, const KCtx& c);
 int enqueue_combine(Launcher& L, const CombineProblem& p, const KCtx& c);

@@ -180,6 +180,20 @@ struct GraphLauncher : Launcher {
         : g(graph), ctx(c), pdl(programmatic) {}
     int launch(const void* func, dim3 grid, dim3 block, size_t smem, void** args,
                bool overlap_ok = false) override {
+        const bool prog = (pdl == 1 || (pdl == 2 && overlap_ok)) && chained && deps.size() == 1;
+        CUgraphNode n;
+        const int e = add(func, grid, block, smem, args, deps, prog, &n);
+        if (e) return e;
+        deps.assign(1, n);
+        chained = true;
+        return 0;
+    }
+    int launch_side(const void* func, dim3 grid, dim3 block, size_t smem, void** args) override {
+        CUgraphNode n;
+        return add(func, grid, block, smem, args, deps, false, &n);
+    }
+    int add(const void* func, dim3 grid, dim3 block, size_t smem, void** args,
+            const std::vector<CUgraphNode>& on, bool prog, CUgraphNode* out) {
         int e = ensure_smem_attr(func, smem);
         if (e) return e;
         cudaKernel_t k;
@@ -199,20 +213,16 @@ struct GraphLauncher : Launcher {
         np.kernel.blockDimZ = block.z;
         np.kernel.sharedMemBytes = (unsigned)smem;
         np.kernel.kernelParams = args;
-        CUgraphNode n;
         CUgraphEdgeData ed;
         memset(&ed, 0, sizeof(ed));
         ed.from_port = CU_GRAPH_KERNEL_NODE_PORT_PROGRAMMATIC;
         ed.type = CU_GRAPH_DEPENDENCY_TYPE_PROGRAMMATIC;
-        const bool prog = (pdl == 1 || (pdl == 2 && overlap_ok)) && chained && deps.size() == 1;
-        CUresult r = drv().graphAddNode(&n, g, deps.empty() ? nullptr : deps.data(),
-                                        prog ? &ed : nullptr, deps.size(), &np);
+        CUresult r = drv().graphAddNode(out, g, on.empty() ? nullptr : on.data(),
+                                        prog ? &ed : nullptr, on.size(), &np);
         if (r != CUDA_SUCCESS) {
             g_err = "cuGraphAddNode: CUresult " + std::to_string((int)r);
             return (int)cudaErrorUnknown;
         }
-        deps.assign(1, n);
-        chained = true;
         return 0;
     }
 };
@@ -483,10 +493,61 @@ struct RunEnv {
     bool norm_fused = false;
     // weight loads of this microbatch keep the lines in L2 for the next microbatch
     bool keep_weights = false;
+    // L2 prefetch of the next projection's weights beside the chain: cap in MB for the
+    // expert matrices (the dense ones are prefetched whole); < 0: off
+    int prefetch_mb = -1;
+    int mu = 0;
+    const sgp_layer* next_layer = nullptr;  // the layer after this one (its QKV weights)
 };
 
 // The combine can produce the next layer's RMSNorm-1 while it holds the row (H <= 4096).
 bool can_fuse_norm(const sgp_dims& d) { return d.hidden <= 4096; }
+
+// After a projection's main kernel: prefetch into L2 the weights of the projection after
+// it, beside the chain, so that the HBM idle time of the kernels in between (a finishing
+// pass, the attention of a sliding layer, the router and dispatch, the combine) moves them.
+// QKV -> output projection, output projection -> expert gate/up, expert gate/up -> expert
+// down, expert down -> the next layer's QKV.  Only the timing changes.
+int side_prefetch(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
+    if (e.prefetch_mb < 0) return 0;
+    const sgp_dims& d = *e.d;
+    PrefetchProblem pf;
+    memset(&pf, 0, sizeof(pf));
+    pf.grid = e.pool_sms;
+    const size_t cap = (size_t)e.prefetch_mb << 20;
+    // a serpentine microbatch walks the expert slots from the last one: take the tail
+    const bool tail = e.serpentine && (mu & 1);
+    auto take = [&](const void* base, size_t total, size_t limit) {
+        const size_t nb = std::min(total, limit) & ~size_t(15);
+        pf.base[0] = tail ? static_cast<const char*>(base) + (total - nb) : base;
+        pf.bytes[0] = nb;
+    };
+    switch (op) {
+        case SGP_OP_QKV:
+            take(e.layer->w_o, (size_t)d.hidden * q_width(d) * 2, SIZE_MAX);
+            pf.base[0] = e.layer->w_o;  // dense: no serpentine order
+            break;
+        case SGP_OP_OPROJ:
+            take(e.layer->w_gate_up, (size_t)d.n_local_experts * 2 * d.inter * d.hidden * 2, cap);
+            break;
+        case SGP_OP_EXPERT_UP:
+            take(e.layer->w_down, (size_t)d.n_local_experts * d.hidden * d.inter * 2, cap);
+            break;
+        default:  // SGP_OP_EXPERT_DOWN
+            if (!e.next_layer) return 0;
+            take(e.next_layer->w_qkv, (size_t)qkv_rows(d) * d.hidden * 2, SIZE_MAX);
+            pf.base[0] = e.next_layer->w_qkv;
+            break;
+    }
+    KCtx pc = c;
+    pc.wait_flag = nullptr;
+    pc.post_flag = nullptr;
+    pc.post_cnt = nullptr;
+    pc.trace = nullptr;
+    pc.smmask = nullptr;
+    pc.fault = 0;
+    return enqueue_prefetch(L, pf, pc);
+}
 
 int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     const sgp_dims& d = *e.d;
@@ -550,6 +611,7 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
             break;
     }
     const int* goff = grouped ? e.ws.mu<int>(mu, e.ws.L->offsets) : nullptr;
+    int r0;
     if (!tc) {
         GemvProblem p;
         memset(&p, 0, sizeof(p));
@@ -565,7 +627,8 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
         p.row0 = grouped ? 0 : row0;
         p.nrows = grouped ? 0 : b;
         p.epi = epi;
-        return enqueue_gemv(L, p, c);
+        if ((r0 = enqueue_gemv(L, p, c)) != 0) return r0;
+        return side_prefetch(L, e, op, mu, c);
     }
     GemmProblem p;
     memset(&p, 0, sizeof(p));
@@ -633,10 +696,14 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
         p.fused_epi = 1;
         p.out_row0 = grouped ? 0 : row0;
         p.epi = epi;
-        return enqueue_gemm_tc(L, p, c);
+        if ((r0 = enqueue_gemm_tc(L, p, c)) != 0) return r0;
+        return side_prefetch(L, e, op, mu, c);
     }
     // the expert-down K segments are summed by the combine (it reads each routed row once)
-    if (op == SGP_OP_EXPERT_DOWN) return enqueue_gemm_tc(L, p, c);
+    if (op == SGP_OP_EXPERT_DOWN) {
+        if ((r0 = enqueue_gemm_tc(L, p, c)) != 0) return r0;
+        return side_prefetch(L, e, op, mu, c);
+    }
     // the flag check belongs to the first launch, the publish to the last
     KCtx c1 = c, c2 = c;
     c1.post_flag = nullptr;
@@ -646,6 +713,7 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     if (c.trace) c2.trace = c.trace + 2;  // the finishing kernel has the op's second slot
     if (c.smmask) c2.smmask = c.smmask + 8;
     if ((r = enqueue_gemm_tc(L, p, c1)) != 0) return r;
+    if ((r = side_prefetch(L, e, op, mu, c1)) != 0) return r;
     FinishProblem f;
     memset(&f, 0, sizeof(f));
     f.partial = p.partial;
@@ -1230,6 +1298,9 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
             e.next = fused[l + 1] ? &layers[l + 1] : nullptr;
             e.norm_fused = fused[l] != 0;
             e.keep_weights = p->opts.weight_reuse > 0 && t.mu + 1 < p->lay.m;
+            e.prefetch_mb = p->opts.l2_prefetch_mb > 0 ? p->opts.l2_prefetch_mb : -1;
+            e.mu = t.mu;
+            e.next_layer = l + 1 < n_layers ? &layers[l + 1] : nullptr;
             if (op == SGP_OP_RMSNORM_ATTN && e.norm_fused) {  // nothing to launch
                 if (++op == SGP_N_OPS) {
                     op = 0;
@@ -1511,6 +1582,62 @@ extern "C" int sgp_pipeline_sync(sgp_pipeline* p) {
     return read_status(p);
 }
 
+namespace {
+// Times each stage's tasks on its own pool (data edges between stages dropped), median of
+// `reps` replays after one warm-up.  shared: all stages replay at the same time, each on its
+// own stream, so every stage is timed while the others load HBM and L2 as in a pipelined
+// run; otherwise one stage at a time, alone on the GPU.
+int time_stages(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_layer* layers,
+                const int32_t* kv_len, const void* x_in, void* x_out, int T, int reps,
+                bool shared, float* t_us) {
+    const int n = p->n_stages;
+    std::vector<cudaGraphExec_t> ex(n, nullptr);
+    std::vector<cudaStream_t> st(n, nullptr);
+    std::vector<cudaEvent_t> e0(n, nullptr), e1(n, nullptr);
+    std::vector<std::vector<float>> ts(n);
+    int r = SGP_OK;
+    cudaError_t ce = cudaSuccess;
+    for (int i = 0; i < n && r == SGP_OK && ce == cudaSuccess; ++i) {
+        cudaGraph_t g;
+        if ((r = build_graph(p, tasks, layers, kv_len, x_in, x_out, T, nullptr, nullptr, i, &g)) !=
+            SGP_OK)
+            break;
+        ce = cudaGraphInstantiate(&ex[i], g, 0);
+        cudaGraphDestroy(g);
+        if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking);
+        if (ce == cudaSuccess) ce = cudaEventCreate(&e0[i]);
+        if (ce == cudaSuccess) ce = cudaEventCreate(&e1[i]);
+    }
+    for (int it = 0; it < reps + 1 && r == SGP_OK && ce == cudaSuccess; ++it) {
+        for (int i = 0; i < n && ce == cudaSuccess; ++i) {
+            ce = cudaEventRecord(e0[i], st[i]);
+            if (ce == cudaSuccess) ce = cudaGraphLaunch(ex[i], st[i]);
+            if (ce == cudaSuccess) ce = cudaEventRecord(e1[i], st[i]);
+            if (ce == cudaSuccess && !shared) ce = cudaEventSynchronize(e1[i]);
+        }
+        for (int i = 0; i < n && ce == cudaSuccess; ++i) {
+            ce = cudaEventSynchronize(e1[i]);
+            float ms = 0.f;
+            if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms, e0[i], e1[i]);
+            if (ce == cudaSuccess && it > 0) ts[i].push_back(ms * 1000.f);
+        }
+    }
+    for (int i = 0; i < n; ++i) {
+        if (ex[i]) cudaGraphExecDestroy(ex[i]);
+        if (e0[i]) cudaEventDestroy(e0[i]);
+        if (e1[i]) cudaEventDestroy(e1[i]);
+        if (st[i]) cudaStreamDestroy(st[i]);
+    }
+    if (r != SGP_OK) return r;
+    if (ce != cudaSuccess) return fail_cuda(ce, "stage timing");
+    for (int i = 0; i < n; ++i) {
+        std::sort(ts[i].begin(), ts[i].end());
+        t_us[i] = ts[i][ts[i].size() / 2];
+    }
+    return SGP_OK;
+}
+}  // namespace
+
 extern "C" int sgp_pipeline_stage_times(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
                                         const int32_t* kv_len, const void* x_in, void* x_out,
                                         int n_tokens, int reps, float* t_us) {
@@ -1531,37 +1658,9 @@ extern "C" int sgp_pipeline_stage_times(sgp_pipeline* p, const sgp_layer* layers
         }
         if ((r = ensure_ws(p, n_tokens, (int)tasks.size())) != SGP_OK) return r;
     }
-    cudaStream_t s;
-    CK(cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking));
-    cudaEvent_t e0, e1;
-    CK(cudaEventCreate(&e0));
-    CK(cudaEventCreate(&e1));
-    for (int st = 0; st < p->n_stages; ++st) {
-        cudaGraph_t g;
-        if ((r = build_graph(p, tasks, layers, kv_len, x_in, x_out, n_tokens, nullptr, nullptr, st,
-                             &g)) != SGP_OK)
-            return r;
-        cudaGraphExec_t ex;
-        cudaError_t ce = cudaGraphInstantiate(&ex, g, 0);
-        cudaGraphDestroy(g);
-        if (ce != cudaSuccess) return fail_cuda(ce, "cudaGraphInstantiate");
-        std::vector<float> ts;
-        for (int i = 0; i < reps + 1; ++i) {
-            CK(cudaEventRecord(e0, s));
-            CK(cudaGraphLaunch(ex, s));
-            CK(cudaEventRecord(e1, s));
-            CK(cudaEventSynchronize(e1));
-            float ms = 0.f;
-            CK(cudaEventElapsedTime(&ms, e0, e1));
-            if (i > 0) ts.push_back(ms * 1000.f);
-        }
-        cudaGraphExecDestroy(ex);
-        std::sort(ts.begin(), ts.end());
-        t_us[st] = ts[ts.size() / 2];
-    }
-    cudaEventDestroy(e0);
-    cudaEventDestroy(e1);
-    cudaStreamDestroy(s);
+    r = time_stages(p, tasks, layers, kv_len, x_in, x_out, n_tokens, reps,
+                    p->opts.stage_times_shared != 0, t_us);
+    if (r != SGP_OK) return r;
     return read_status(p);
 }
 
@@ -1656,6 +1755,170 @@ extern "C" void sgp_pipeline_destroy(sgp_pipeline* p) {
     for (int i = p->n_gctx - 1; i >= 0; --i)
         if (p->gctx[i] && d.greenDestroy) d.greenDestroy(p->gctx[i]);
     delete p;
+}
+
+// =======================================================================================
+// C ABI: pairwise-line SM-allocation refinement ("SubGPU Pipelining", Section 4.2,
+// Algorithm 2).  A move p^{d->r}[z] hands z quanta of SMs from donor stage d to receiver
+// stage r.  Each pass takes the best one-quantum move; if it improves the objective, a
+// doubling/halving line search extends it along the same (d, r) pair.  Objective values
+// are memoised per allocation.
+// =======================================================================================
+namespace {
+struct AllocSearch {
+    int n;
+    int g, p_min;
+    sgp_alloc_objective f;
+    void* ctx;
+    std::vector<std::pair<std::vector<int>, double>> memo;
+    int evals = 0;
+    bool feasible(const std::vector<int>& p) const {
+        for (int v : p)
+            if (v < p_min || v < g) return false;
+        return true;
+    }
+    // objective, memoised; an allocation the objective cannot evaluate (< 0) is +inf
+    double eval(const std::vector<int>& p) {
+        for (const auto& e : memo)
+            if (e.first == p) return e.second;
+        double t = f(p.data(), n, ctx);
+        ++evals;
+        if (!(t >= 0.0)) t = INFINITY;
+        memo.emplace_back(p, t);
+        return t;
+    }
+    std::vector<int> moved(const std::vector<int>& p, int d, int r, int z) const {
+        std::vector<int> q = p;
+        q[d] -= z * g;
+        q[r] += z * g;
+        return q;
+    }
+};
+}  // namespace
+
+extern "C" int sgp_refine_allocation(int n_stages, int* p_inout, int quantum, int p_min,
+                                     int pass_limit, sgp_alloc_objective f, void* ctx,
+                                     double* t_out) {
+    if (n_stages < 2 || n_stages > 8 || !p_inout || quantum < 1 || p_min < 0 || !f)
+        return fail_arg("n_stages, p, quantum, p_min or objective");
+    AllocSearch S{n_stages, quantum, p_min, f, ctx, {}, 0};
+    std::vector<int> p(p_inout, p_inout + n_stages);
+    if (!S.feasible(p)) return fail_arg("initial allocation below p_min or the quantum");
+    double t = S.eval(p);
+    for (int pass = 1; pass_limit <= 0 || pass <= pass_limit; ++pass) {
+        int bd = -1, br = -1;
+        double t_line = INFINITY;
+        for (int d = 0; d < n_stages; ++d)
+            for (int r = 0; r < n_stages; ++r) {
+                if (d == r) continue;
+                const std::vector<int> q = S.moved(p, d, r, 1);
+                if (!S.feasible(q)) continue;
+                const double v = S.eval(q);
+                if (bd < 0 || v < t_line) {  // first minimum in (d, r) order
+                    bd = d;
+                    br = r;
+                    t_line = v;
+                }
+            }
+        if (bd < 0 || !(t_line < t)) break;  // no legal move, or none improves
+        int z = 1, h = 1;
+        while (h > 0) {
+            const std::vector<int> q = S.moved(p, bd, br, z + h);
+            double v;
+            if (S.feasible(q) && (v = S.eval(q)) < t_line) {
+                z += h;
+                t_line = v;
+                h *= 2;
+            } else {
+                h /= 2;
+            }
+        }
+        p = S.moved(p, bd, br, z);
+        t = t_line;
+    }
+    for (int i = 0; i < n_stages; ++i) p_inout[i] = p[i];
+    if (t_out) *t_out = t;
+    return S.evals;
+}
+
+namespace {
+struct RefineCtx {
+    const sgp_dims* d;
+    const sgp_layer* layers;
+    int n_layers;
+    const int32_t* kv_len;
+    const void* x_in;
+    void* x_out;
+    int T, micro, max_kv, reps;
+    const sgp_pipeline_opts* opts;
+    int err = SGP_OK;  // first error other than an allocation the device cannot form
+};
+
+// objective: the median time (us) of `reps` full pipelined runs with SM allocation p
+double refine_objective(const int* split, int n, void* vctx) {
+    RefineCtx& c = *static_cast<RefineCtx*>(vctx);
+    if (c.err != SGP_OK) return -1.0;
+    sgp_pipeline* p = nullptr;
+    int r = sgp_pipeline_create(c.d, split, n, c.micro, c.T, c.max_kv, c.opts, &p);
+    if (r != SGP_OK) return -1.0;  // a split the device cannot form is infeasible
+    cudaStream_t s = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    std::vector<float> ts;
+    cudaError_t ce = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (ce == cudaSuccess) ce = cudaEventCreate(&e0);
+    if (ce == cudaSuccess) ce = cudaEventCreate(&e1);
+    for (int i = 0; i < c.reps + 1 && ce == cudaSuccess && r == SGP_OK; ++i) {
+        ce = cudaEventRecord(e0, s);
+        if (ce != cudaSuccess) break;
+        r = sgp_pipeline_run(p, c.layers, c.n_layers, c.kv_len, c.x_in, c.x_out, c.T, nullptr,
+                             nullptr, s);
+        if (r != SGP_OK) break;
+        ce = cudaEventRecord(e1, s);
+        if (ce == cudaSuccess) ce = cudaEventSynchronize(e1);
+        float ms = 0.f;
+        if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms, e0, e1);
+        if (ce == cudaSuccess && i > 0) ts.push_back(ms * 1000.f);
+    }
+    if (r == SGP_OK && ce == cudaSuccess) r = sgp_pipeline_sync(p);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    if (s) cudaStreamDestroy(s);
+    sgp_pipeline_destroy(p);
+    if (ce != cudaSuccess) r = fail_cuda(ce, "refinement run");
+    if (r != SGP_OK) {
+        c.err = r;
+        return -1.0;
+    }
+    std::sort(ts.begin(), ts.end());
+    return ts[ts.size() / 2];
+}
+}  // namespace
+
+extern "C" int sgp_pipeline_refine(const sgp_dims* d, const sgp_layer* layers, int n_layers,
+                                   const int32_t* kv_len, const void* x_in, void* x_out,
+                                   int n_tokens, int n_stages, int microbatch, int max_kv_len,
+                                   int quantum, int reps, int pass_limit,
+                                   const sgp_pipeline_opts* opts, int* split_inout,
+                                   float* t_us_out, int* n_evals) {
+    if (!split_inout || reps < 1 || n_stages < 2 || n_stages > 3)
+        return fail_arg("split, reps or n_stages (2 or 3)");
+    sgp_device_info info;
+    int r;
+    if ((r = sgp_device_info_get(&info)) != SGP_OK) return r;
+    if (!info.green_ctx_supported) return SGP_ERR_UNSUPPORTED;
+    const int q = std::max(quantum, std::max(1, info.sm_alignment));
+    const int pmin = std::max(q, info.sm_min_partition);
+    RefineCtx c{d, layers, n_layers, kv_len, x_in, x_out, n_tokens, microbatch, max_kv_len, reps,
+                opts};
+    double t = 0.0;
+    const int ev = sgp_refine_allocation(n_stages, split_inout, q, pmin, pass_limit,
+                                         refine_objective, &c, &t);
+    if (ev < 0) return ev;
+    if (c.err != SGP_OK) return c.err;
+    if (!std::isfinite(t)) return fail_arg("no allocation could be run");
+    if (t_us_out) *t_us_out = (float)t;
+    if (n_evals) *n_evals = ev;
+    return SGP_OK;
 }
 
 extern "C" int sgp_pipeline_balance(const sgp_dims* d, const sgp_layer* layers, int n_layers,

@@ -61,7 +61,8 @@ class sgp_pipeline_opts(C.Structure):
                 ("serpentine_experts", C.c_int), ("wait_timeout_ns", C.c_uint64),
                 ("fault_inject", C.c_uint32), ("fault_task", C.c_int),
                 ("programmatic_launch", C.c_int), ("trace", C.c_int),
-                ("weight_reuse", C.c_int)]
+                ("weight_reuse", C.c_int), ("l2_prefetch_mb", C.c_int),
+                ("stage_times_shared", C.c_int)]
 
 
 _lib = None
@@ -111,6 +112,16 @@ _SIGS = {
                                        C.POINTER(C.c_int), C.POINTER(C.c_int),
                                        C.POINTER(C.c_float), C.c_int, C.POINTER(C.c_int)]),
 }
+
+_SIGS["sgp_pipeline_refine"] = (C.c_int, [C.POINTER(sgp_dims), C.POINTER(sgp_layer), C.c_int,
+                                          C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
+                                          C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
+                                          C.POINTER(sgp_pipeline_opts), C.POINTER(C.c_int),
+                                          C.POINTER(C.c_float), C.POINTER(C.c_int)])
+ALLOC_OBJECTIVE = C.CFUNCTYPE(C.c_double, C.POINTER(C.c_int), C.c_int, C.c_void_p)
+_SIGS["sgp_refine_allocation"] = (C.c_int, [C.c_int, C.POINTER(C.c_int), C.c_int, C.c_int,
+                                            C.c_int, ALLOC_OBJECTIVE, C.c_void_p,
+                                            C.POINTER(C.c_double)])
 
 ABI_FUNCTIONS = tuple(_SIGS)
 
@@ -187,7 +198,8 @@ def layer_array(layers: Sequence[sgp_layer]):
 def make_opts(stage_of_op=None, use_green_contexts: int = 0, green_ctx_flags: int = 0,
               serpentine_experts: int = 0, wait_timeout_ns: int = 0, fault_inject: int = 0,
               fault_task: int = 0, programmatic_launch: int = 0,
-              trace: int = 0, weight_reuse: int = 0) -> sgp_pipeline_opts:
+              trace: int = 0, weight_reuse: int = 0, l2_prefetch_mb: int = 0,
+              stage_times_shared: int = 0) -> sgp_pipeline_opts:
     o = sgp_pipeline_opts()
     if stage_of_op is not None:
         o.custom_cut = 1
@@ -203,6 +215,8 @@ def make_opts(stage_of_op=None, use_green_contexts: int = 0, green_ctx_flags: in
     o.programmatic_launch = programmatic_launch
     o.trace = trace
     o.weight_reuse = weight_reuse
+    o.l2_prefetch_mb = l2_prefetch_mb
+    o.stage_times_shared = stage_times_shared
     return o
 
 
@@ -353,6 +367,46 @@ def handoff_gaps_us(p):
             continue
         gaps.append((spans[i, 0] - spans[pd, 1]) * 1e-3)
     return np.array(gaps, dtype=np.float64)
+
+
+def sgp_refine_allocation(p0: Sequence[int], quantum: int, p_min: int, objective,
+                          pass_limit: int = 0):
+    """Pairwise-line refinement of the allocation p0 under objective(p: tuple) -> float
+    (lower is better; negative = cannot evaluate).  Returns (allocation, value, evaluations)."""
+    n = len(p0)
+    p = (C.c_int * n)(*p0)
+    err = []
+
+    def _f(pp, nn, _ctx):
+        try:
+            return float(objective(tuple(pp[i] for i in range(nn))))
+        except Exception as e:          # an exception must not unwind through C
+            err.append(e)
+            return -1.0
+    cb = ALLOC_OBJECTIVE(_f)
+    t = C.c_double()
+    r = lib().sgp_refine_allocation(n, p, quantum, p_min, pass_limit, cb, None, C.byref(t))
+    if err:
+        raise err[0]
+    if r < 0:
+        raise SgpError(r, "sgp_refine_allocation")
+    return tuple(p), t.value, r
+
+
+def sgp_pipeline_refine(dims, layers, kv_len, x_in, x_out, n_tokens: int, split: Sequence[int],
+                        microbatch: int, max_kv_len: int, quantum: int = 8, reps: int = 3,
+                        pass_limit: int = 0, opts: Optional[sgp_pipeline_opts] = None):
+    """Measured pairwise-line refinement of `split`; returns (split, us, evaluations)."""
+    arr = layers if isinstance(layers, C.Array) else layer_array(layers)
+    n = len(split)
+    sp = (C.c_int * n)(*split)
+    t = C.c_float()
+    ev = C.c_int()
+    check(lib().sgp_pipeline_refine(C.byref(dims), arr, len(arr), _p(kv_len), _p(x_in),
+                                    _p(x_out), n_tokens, n, microbatch, max_kv_len, quantum, reps,
+                                    pass_limit, C.byref(opts) if opts is not None else None, sp,
+                                    C.byref(t), C.byref(ev)), "sgp_pipeline_refine")
+    return list(sp), t.value, ev.value
 
 
 def sgp_pipeline_destroy(p) -> None:

@@ -17,6 +17,9 @@ Inference":
   * Section 4.2, Eq. 7 and the illustrative counts that follow it: the number
     of cut-and-binding choices of an operator chain and of SM allocations in
     quanta.
+  * Section 4.2, Algorithm 2: pairwise-line SM-allocation refinement (the best
+    one-quantum transfer between two stages, then a doubling/halving line search
+    along that donor-receiver pair, repeated until no transfer improves).
 """
 from __future__ import annotations
 
@@ -130,3 +133,44 @@ def count_allocations(n_sm: int, n_stages: int, quantum: int) -> int:
 def count_allocations_closed(n_sm: int, n_stages: int, quantum: int) -> int:
     """Stars and bars: compositions of n_sm/quantum into n_stages positive parts."""
     return comb(n_sm // quantum - 1, n_stages - 1)
+
+
+# ---------------------------------------------------------------------------
+# Section 4.2, Algorithm 2: pairwise-line SM-allocation refinement
+# ---------------------------------------------------------------------------
+def transfer(p, d: int, r: int, z: int, g: int):
+    """p^{d->r}[z]: z*g SMs move from donor stage d to receiver stage r."""
+    q = list(p)
+    q[d] -= z * g
+    q[r] += z * g
+    return tuple(q)
+
+
+def pairwise_line(f, feasible, p, g: int, passes=None):
+    """Algorithm 2 in the pages' steps.  f(p) is the objective (lower is better),
+    feasible(p) the membership test of P, p the initial allocation, g the SM quantum and
+    passes the pass limit L (None = until no improving move).  Returns the refined
+    allocation and its objective value."""
+    p = tuple(p)
+    t = f(p)
+    n = len(p)
+    k = 0
+    while passes is None or k < passes:
+        k += 1
+        M = [(d, r) for d in range(n) for r in range(n) if d != r and feasible(transfer(p, d, r, 1, g))]
+        if not M:
+            return p, t
+        d, r = min(M, key=lambda dr: f(transfer(p, dr[0], dr[1], 1, g)))
+        z, h = 1, 1
+        t_line = f(transfer(p, d, r, 1, g))
+        if t_line >= t:
+            return p, t
+        while h > 0:
+            z2 = z + h
+            q = transfer(p, d, r, z2, g)
+            if feasible(q) and f(q) < t_line:
+                z, t_line, h = z2, f(q), 2 * h
+            else:
+                h //= 2
+        p, t = transfer(p, d, r, z, g), t_line
+    return p, t

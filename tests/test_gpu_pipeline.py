@@ -445,6 +445,47 @@ def test_stage_times_and_balancer_pick_a_legal_split():
     print("balance", best, rows)
 
 
+def test_stage_times_shared_and_alone():
+    """Stage times with every stage replaying at once (the contention of a pipelined run) and
+    alone: both positive; the shared ones are the ones the pipeline actually sees."""
+    wl, inp = _stack_inputs(2, 1024, 13)
+    d = H.dims(wl.shape)
+    out = torch.empty_like(inp.x)
+    res = {}
+    for shared in (0, 1):
+        p = sgp.sgp_pipeline_create(d, _splits(2), 2, 32, wl.n_tokens, wl.cap,
+                                    sgp.make_opts(stage_times_shared=shared))
+        try:
+            res[shared] = sgp.sgp_pipeline_stage_times(p, inp.sgp_layers(), inp.kv_len, inp.x,
+                                                       out, wl.n_tokens, 2, reps=3)
+        finally:
+            sgp.sgp_pipeline_destroy(p)
+    print("stage times alone", res[0], "shared", res[1])
+    assert all(t > 0 for t in res[0] + res[1])
+
+
+def test_refine_three_stage_allocation_on_measured_runs():
+    """Algorithm 2 on measured full pipelined runs of a 3-stage cut: the refined split is legal
+    (entries multiples of the alignment, at least the minimum partition, same total), it was
+    measured, and repeating the search from the refined split stays there or improves."""
+    wl, inp = _stack_inputs(2, 1024, 16)
+    d = H.dims(wl.shape)
+    info = sgp.sgp_device_info_get()
+    a = max(1, info.sm_alignment)
+    start = _splits(3)
+    out = torch.empty_like(inp.x)
+    split, t, n = sgp.sgp_pipeline_refine(d, inp.sgp_layers(), inp.kv_len, inp.x, out,
+                                          wl.n_tokens, start, 16, wl.cap, quantum=a, reps=2,
+                                          pass_limit=2)
+    print("refined", start, "->", split, f"{t:.1f} us", n, "evaluations")
+    assert sum(split) == sum(start) and n >= 1 and t > 0
+    assert all(v % a == 0 and v >= max(a, info.sm_min_partition) for v in split)
+    # the refined split runs and gives the temporal output
+    ref = _temporal(inp, d)
+    got = _pipelined(inp, d, 3, 16, split=split)
+    assert torch.equal(got[0], ref[0])
+
+
 def _time_temporal(inp, d, reps=5):
     wl = inp.wl
     T = wl.n_tokens
