@@ -552,8 +552,31 @@ __global__ void __launch_bounds__(256, U <= 4 ? 4 : 2)
 }
 
 // ---------------------------------------------------------------------------------------
-// CUDA-core GEMV path: one warp per output feature, 8 tokens per pass, 16-byte loads.
+// GEMV path (fewer than gemv_max_tokens tokens per weight matrix): a skinny product whose
+// weights stream straight from HBM into registers.  A warp owns a tile of 16 weight rows --
+// 16 output features, or 8 SwiGLU features as 8 gate rows over 8 up rows -- and one eighth of
+// K; the CTA's 8 warps cover all of K and add their partial tiles in warp order through
+// shared memory.  The per-lane product is a warp-level bf16 MMA (m16n8k16, fp32 accumulate)
+// over 8 tokens per n-tile, which does the K reduction without shuffles.  Its operands come
+// straight from 16-byte loads: in every 32-wide K block, lane (g, t) loads K positions
+// [8t, 8t + 8) of weight rows g and g + 8 and of token g's activation row, and the two MMAs
+// of the block take positions 8t..8t+3 and 8t+4..8t+7 as the fragment columns
+// {2t, 2t+1, 2t+8, 2t+9} -- the same permutation of K for both operands, so each MMA still
+// sums products of matching elements.  kGemvU blocks of loads (4 x 16 bytes per lane each)
+// are issued before their MMAs.  A token's result never depends on the other tokens.
 // ---------------------------------------------------------------------------------------
+constexpr int kGemvWarps = 8;  // K split of a tile (one warp per part)
+constexpr int kGemvU = 4;      // 32-wide K blocks whose loads are in flight together
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ void gemv_store(const EpiArgs& e, const KCtx& c, int f, int trow,
                                            float v) {
     if (f >= e.n_out) return;
@@ -589,13 +612,31 @@ __device__ __forceinline__ void gemv_store(const EpiArgs& e, const KCtx& c, int 
     }
 }
 
-__global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KCtx ctx) {
+// NT n-tiles of 8 tokens per pass (1: up to 8 tokens, 2: up to 16)
+template <int NT>
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(const GemvProblem P, const KCtx ctx) {
     griddep_launch();
     griddep_wait();
     task_begin(ctx);
+    __shared__ float red[kGemvWarps][32][4 * NT];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int f = blockIdx.x * 8 + warp;
+    const int gi = lane >> 2, ti = lane & 3;   // fragment row group / column pair
     const int g = blockIdx.y;
+    // the tile's weight rows g and g + 8 of this lane, and the features they feed
+    int row_lo, row_hi, f_lo, f_hi;
+    if (P.swiglu) {
+        f_lo = f_hi = blockIdx.x * 8 + gi;             // gate row over up row of one feature
+        row_lo = f_lo;
+        row_hi = f_lo + P.up_off;
+    } else {
+        f_lo = blockIdx.x * 16 + gi;
+        f_hi = f_lo + 8;
+        row_lo = f_lo;
+        row_hi = f_hi;
+    }
+    const bool ok_lo = f_lo < P.n_out, ok_hi = f_hi < P.n_out;
+    const uint4* wlo = reinterpret_cast<const uint4*>(P.W + ((size_t)g * P.rows_per_group + row_lo) * P.K);
+    const uint4* whi = reinterpret_cast<const uint4*>(P.W + ((size_t)g * P.rows_per_group + row_hi) * P.K);
     int r0, n;
     if (P.group_offsets != nullptr) {
         r0 = P.group_offsets[g];
@@ -604,55 +645,75 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvProblem P, const KC
         r0 = P.row0;
         n = P.nrows;
     }
-    if (f < P.n_out && n > 0) {
-        const int nv = P.K >> 3;
-        const size_t wrow = (size_t)g * P.rows_per_group + f;
-        const uint4* w1 = reinterpret_cast<const uint4*>(P.W + wrow * P.K);
-        const uint4* w2 = P.swiglu
-                              ? reinterpret_cast<const uint4*>(P.W + (wrow + P.up_off) * P.K)
-                              : nullptr;
-        for (int t0 = 0; t0 < n; t0 += 8) {
-            const int nt = min(8, n - t0);
-            float a1[8], a2[8];
+    const int nkb = P.K >> 5;                                   // 32-wide K blocks
+    const int kb0 = warp * nkb / kGemvWarps, kb1 = (warp + 1) * nkb / kGemvWarps;
+    const uint4 z4 = make_uint4(0, 0, 0, 0);
+    for (int t0 = 0; t0 < n; t0 += 8 * NT) {
+        float acc[NT][4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a1[i] = a2[i] = 0.f;
-            for (int v = lane; v < nv; v += 32) {
-                float wf[8], wg[8];
-                unpack8(__ldg(w1 + v), wf);
-                if (w2) unpack8(__ldg(w2 + v), wg);
+        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        const uint4* xr[NT];
+        bool xok[NT];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (i < nt) {
-                        float xf[8];
-                        unpack8(__ldg(reinterpret_cast<const uint4*>(
-                                          P.X + (size_t)(r0 + t0 + i) * P.K) + v),
-                                xf);
+        for (int j = 0; j < NT; ++j) {
+            const int t = t0 + 8 * j + gi;                      // this lane's token of n-tile j
+            xok[j] = t < n;
+            xr[j] = reinterpret_cast<const uint4*>(P.X + (size_t)(r0 + (xok[j] ? t : 0)) * P.K);
+        }
+        for (int kb = kb0; kb < kb1; kb += kGemvU) {
+            uint4 alo[kGemvU], ahi[kGemvU], b[kGemvU][NT];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            a1[i] = fmaf(wf[q], xf[q], a1[i]);
-                            if (w2) a2[i] = fmaf(wg[q], xf[q], a2[i]);
-                        }
-                    }
+            for (int u = 0; u < kGemvU; ++u) {
+                const bool in = kb + u < kb1;
+                const int c = (kb + u) * 4 + ti;                // 16-byte chunk of the row
+                alo[u] = (in && ok_lo) ? __ldg(wlo + c) : z4;
+                ahi[u] = (in && ok_hi) ? __ldg(whi + c) : z4;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) b[u][j] = (in && xok[j]) ? __ldg(xr[j] + c) : z4;
+            }
+#pragma unroll
+            for (int u = 0; u < kGemvU; ++u) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    mma16816(acc[j], alo[u].x, ahi[u].x, alo[u].y, ahi[u].y, b[u][j].x, b[u][j].y);
+                    mma16816(acc[j], alo[u].z, ahi[u].z, alo[u].w, ahi[u].w, b[u][j].z, b[u][j].w);
                 }
             }
+        }
+        // the 8 K parts of the tile, added in warp order
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                a1[i] = warp_sum(a1[i]);
-                if (w2) a2[i] = warp_sum(a2[i]);
-            }
-            if (lane == 0) {
-                for (int i = 0; i < nt; ++i) {
-                    const int trow = r0 + t0 + i;
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[warp][lane][4 * j + i] = acc[j][i];
+        __syncthreads();
+        if (warp == 0) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                float v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[i] = red[0][lane][4 * j + i];
+#pragma unroll
+                    for (int w = 1; w < kGemvWarps; ++w) v[i] += red[w][lane][4 * j + i];
+                }
+                // fragment: rows gi (v0, v1) and gi + 8 (v2, v3), tokens 2 ti and 2 ti + 1
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int t = t0 + 8 * j + 2 * ti + c;
+                    if (t >= n) continue;
+                    const int trow = r0 + t;
                     if (P.swiglu) {
-                        if (f < P.epi.n_out)
-                            P.epi.out[(size_t)trow * P.epi.ld + f] =
-                                __float2bfloat16_rn(silu_f(a1[i]) * a2[i]);
+                        if (ok_lo)
+                            P.epi.out[(size_t)trow * P.epi.ld + f_lo] =
+                                __float2bfloat16_rn(silu_f(v[c]) * v[2 + c]);
                     } else {
-                        gemv_store(P.epi, ctx, f, trow, a1[i]);
+                        if (ok_lo) gemv_store(P.epi, ctx, f_lo, trow, v[c]);
+                        if (ok_hi) gemv_store(P.epi, ctx, f_hi, trow, v[2 + c]);
                     }
                 }
             }
         }
+        __syncthreads();  // red is reused by the next token pass
     }
     task_end(ctx);
 }
@@ -706,9 +767,14 @@ int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c) {
 }
 
 int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c) {
-    dim3 grid((p.n_out + 7) / 8, p.n_groups), block(256);
+    if (p.K % 32) return (int)cudaErrorInvalidValue;  // 32-wide K blocks
+    const int per_tile = p.swiglu ? 8 : 16;          // output features per 16-row tile
+    dim3 grid((p.n_out + per_tile - 1) / per_tile, p.n_groups), block(kGemvWarps * 32);
     void* args[] = {(void*)&p, (void*)&c};
-    return L.launch((const void*)gemv_kernel, grid, block, 0, args);
+    // two n-tiles per pass when a matrix may see more than 8 tokens
+    const int most = p.group_offsets ? 16 : p.nrows;
+    return L.launch(most > 8 ? (const void*)gemv_kernel<2> : (const void*)gemv_kernel<1>, grid,
+                    block, 0, args);
 }
 
 }  // namespace sgp

@@ -100,12 +100,15 @@ def test_tiny_layer_vs_oracle(path):
     H.assert_close("k_new", kn, ref["k_new"].reshape(wl.n_tokens, -1))
 
 
-def test_gptoss_layer_vs_oracle():
+@pytest.mark.parametrize("path", [sgp.PATH_AUTO, sgp.PATH_GEMV])
+def test_gptoss_layer_vs_oracle(path):
+    """Full C1 layer; forced onto the GEMV path it also covers several 16-token passes per
+    matrix (64 tokens dense, about 64 routed rows per expert slot)."""
     wl = synth.WORKLOADS["gptoss_layer"]
     inp, ref = H.make_inputs_with_margin(wl, 2)
-    res = H.run_temporal_layer(inp, H.dims(wl.shape))
+    res = H.run_temporal_layer(inp, H.dims(wl.shape, path))
     errs = _check_layer(inp, ref, res, wl.n_tokens)
-    print("gptoss_layer", {k: f"{v:.2e}" for k, v in errs.items()})
+    print("gptoss_layer", path, {k: f"{v:.2e}" for k, v in errs.items()})
 
 
 @pytest.mark.parametrize("window", [0, 16, 200])

@@ -197,7 +197,7 @@ def test_paper_shape_two_layers():
 @pytest.mark.parametrize("n_tokens", [8, 16, 32, 64, 128, 256])
 def test_batch_length_sweep(n_tokens):
     """Batch/length sweep shapes: ragged KV lengths uniform in [512, 16384], one sliding and
-    one full layer; 8 sequences take the CUDA-core GEMV path, 16 and more the tcgen05 path."""
+    one full layer; 8 sequences take the GEMV path, 16 and more the tcgen05 path."""
     wl = synth.sweep_workload(n_tokens, n_layers=2)
     inp = H.make_inputs(wl, 14)
     seqs = sorted({0, n_tokens // 2, n_tokens - 1})
