@@ -64,6 +64,14 @@ def parse():
     ap.add_argument("--virtual-comm", action="store_true",
                     help="add the pages' virtual communication kernels (3 us + bytes / 900 GB/s "
                          "for the attention all-reduce, MoE dispatch and MoE combine)")
+    ap.add_argument("--weight-reuse", action="store_true",
+                    help="load the weights of every microbatch but the last with an L2 "
+                         "evict-last hint (sgp_pipeline_opts.weight_reuse)")
+    ap.add_argument("--no-paper-shape", action="store_true",
+                    help="skip the secondary measurement at the pages' own decode shape")
+    ap.add_argument("--frontier", action="store_true",
+                    help="per-user vs per-GPU throughput frontier over 8..256 sequences with "
+                         "ragged KV lengths in [512, 16384] (one JSON line per point)")
     return ap.parse_args()
 
 
@@ -348,6 +356,104 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------------------------------
+# secondary shapes: one workload timed pipelined and temporally, then freed
+# ------------------------------------------------------------------------------------------
+def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None):
+    """Times one workload on this GPU: the two-stage pipeline (macro cut, `split` or the
+    contention-aware balancer's pick checked by full runs of its three best candidates) and
+    temporal execution.  Sliding-window layers share one KV buffer: each reads only the last
+    128 positions of every sequence, so sharing changes no timing and halves the memory of
+    the large shapes.  Returns a dict; every tensor is freed before it returns."""
+    import torch
+
+    from intra_spatial_pipelining_gb300 import sgp, synth
+    T = wl.n_tokens
+    micro = micro or T // 2
+    x = synth.x_in(wl, seed, dev)
+    kv_len = synth.kv_len(wl, seed, dev)
+    weights = [synth.layer_weights(wl, l, seed, dev) for l in range(wl.n_layers)]
+    caches, slide = [], None
+    for l in range(wl.n_layers):
+        if wl.layer_window(l):
+            slide = slide or synth.kv_cache(wl, l, seed, dev)
+            caches.append(slide)
+        else:
+            caches.append(synth.kv_cache(wl, l, seed, dev))
+    layers = sgp.layer_array([sgp.make_layer(w, k, v, wl.layer_window(l))
+                              for l, (w, (k, v)) in enumerate(zip(weights, caches))])
+    d = sgp.make_dims(wl.shape)
+    out = x.clone()
+    N = sgp.sgp_device_info_get().sm_count
+    stream = torch.cuda.current_stream()
+    full = [1] * sgp.N_OPS
+    full[sgp.OPS.index("attention")] = 0
+    cut = [full, [1] * sgp.N_OPS]
+
+    def run_ms(nst, spl, mb, opts, n, w):
+        p = sgp.sgp_pipeline_create(d, spl, nst, mb, T, wl.cap, opts)
+        try:
+            for _ in range(w):
+                sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
+            sgp.check(sgp.sgp_pipeline_sync(p), "warm-up")
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
+            e1.record(stream)
+            e1.synchronize()
+            sgp.check(sgp.sgp_pipeline_sync(p), "timed runs")
+        finally:
+            sgp.sgp_pipeline_destroy(p)
+        return e0.elapsed_time(e1) / n
+
+    picked = "given"
+    if split is None:
+        _, rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro, wl.cap,
+                                           quantum=8, reps=2,
+                                           opts=sgp.make_opts(stage_of_op=cut, stage_times_shared=1))
+        cands = [r[0] for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:3]]
+        best = min(cands, key=lambda pa: run_ms(2, [pa, N - pa], micro,
+                                                 sgp.make_opts(stage_of_op=cut), 2, 1))
+        split = [best, N - best]
+        picked = "contention-aware balancer, best of its 3 best candidates by full runs"
+    ms_pipe = run_ms(2, split, micro, sgp.make_opts(stage_of_op=cut), steps, warmup)
+    ms_temp = run_ms(1, [N], T, None, steps, warmup)
+    nbytes = algorithmic_bytes(wl)
+    res = {"workload": describe(wl, {})["workload"], "n_tokens": T,
+           "sm_split": split, "split_from": picked, "microbatch": micro,
+           "pipeline_us": ms_pipe * 1e3, "temporal_us": ms_temp * 1e3,
+           "pipeline_speedup": ms_temp / ms_pipe,
+           "tokens_per_s_per_gpu": {"pipeline": T / (ms_pipe * 1e-3), "temporal": T / (ms_temp * 1e-3)},
+           "tokens_per_s_per_user": {"pipeline": 1e3 / ms_pipe, "temporal": 1e3 / ms_temp},
+           "algorithmic_bytes_per_step": nbytes,
+           "sliding_layers": "share one KV buffer (timing only)"}
+    if peak:
+        res["dram_pct_of_peak"] = {"pipeline": 100.0 * nbytes / (ms_pipe * 1e-3) / 1e9 / peak,
+                                   "temporal": 100.0 * nbytes / (ms_temp * 1e-3) / 1e9 / peak}
+    del layers, x, kv_len, weights, caches, slide, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_frontier(args):
+    """Batch/length sweep: sequences in {8, ..., 256}, ragged KV lengths uniform in
+    [512, 16384], 36 alternating layers; one JSON line per point, pipeline (balanced) and
+    temporal, tokens/s/user = 1 / iteration and tokens/s/GPU = sequences / iteration."""
+    import torch
+
+    from intra_spatial_pipelining_gb300 import sgp, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sgp.lib()
+    synth._CHUNK = 1 << 28
+    peak, _ = read_peaks()
+    for b in (8, 16, 32, 64, 128, 256):
+        wl = synth.sweep_workload(b)
+        r = shape_point(wl, dev, args.seed, args.steps, args.warmup, peak=peak)
+        print(json.dumps({"frontier_point": r}), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------
 def run_sgp(args, rank, world, local_rank):
@@ -387,11 +493,12 @@ def run_sgp(args, rank, world, local_rank):
     n_stages = args.stages
     micro = args.micro or (T // max(1, wl.microbatches))
     opts = None
-    opts_kw = {}
+    opts_kw = {"weight_reuse": 1} if args.weight_reuse else {}
     if args.cut == "macro" and n_stages == 2:   # 3 stages use A | o-proj+router | experts
         full = [1] * sgp.N_OPS
         full[sgp.OPS.index("attention")] = 0
-        opts_kw = {"stage_of_op": [full, [1] * sgp.N_OPS]}
+        opts_kw["stage_of_op"] = [full, [1] * sgp.N_OPS]
+    if opts_kw:
         opts = sgp.make_opts(**opts_kw)
     balance_rows = None
     balance_shared_rows = None
@@ -568,6 +675,15 @@ def run_sgp(args, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": ab, "launch_us": attn_ms * 1e3,
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs copy bandwidth)"}
 
+    paper = None
+    if world == 1 and not args.no_paper_shape and args.workload == "gptoss_36l":
+        # the pages' own per-GPU decode shape, after the main workload's tensors are freed
+        del layers, weights, caches, x, out, ws
+        torch.cuda.empty_cache()
+        pwl = synth.WORKLOADS["paper_32k"]
+        paper = shape_point(pwl, dev, args.seed, max(3, args.steps // 2), 3, split=[56, 96],
+                            micro=pwl.n_tokens // 2, peak=read_peaks()[0])
+        paper["split_from"] = "fixed 56 | 96 (the balancer's pick at this shape)"
     if rank != 0:
         return
     total_bytes = algorithmic_bytes(wl)
@@ -589,6 +705,7 @@ def run_sgp(args, rank, world, local_rank):
                                 "microbatches": T // micro, "microbatch": micro,
                                 "virtual_comm": ("3 us + payload / 900 GB/s per collective"
                                                  if args.virtual_comm else None),
+                                "weight_reuse": bool(args.weight_reuse),
                                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
         "iteration_us": iter_us,
         "tokens_per_s_per_user": 1e6 / iter_us,
@@ -611,6 +728,7 @@ def run_sgp(args, rank, world, local_rank):
             "sweep_best": min(sweep_rows, key=lambda r: r[1])[0],
             "full_run_us": [{"p_A": pa, "us": ms * 1e3} for pa, ms in sweep_rows]},
         "roofline": roofline,
+        "paper_shape": paper,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * n_launch,
@@ -650,6 +768,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.frontier:
+        run_frontier(args)
         return
     if world > 1:
         import torch
