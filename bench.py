@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--virtual-comm", action="store_true",
                     help="add the pages' virtual communication kernels (3 us + bytes / 900 GB/s "
                          "for the attention all-reduce, MoE dispatch and MoE combine)")
+    ap.add_argument("--lanes", type=int, default=2, choices=[1, 2],
+                    help="FIFOs per stage: 1 = the pages' model, 2 = one per microbatch parity "
+                         "(two streams per SM pool, as the pages' prototype runs)")
     ap.add_argument("--weight-reuse", action="store_true",
                     help="load the weights of every microbatch but the last with an L2 "
                          "evict-last hint (sgp_pipeline_opts.weight_reuse)")
@@ -126,19 +129,21 @@ def describe(wl, extra):
     return cfg
 
 
-def algorithmic_bytes(wl):
+def algorithmic_bytes(wl, kv_lens=None):
     """Unique bytes of one iteration: every weight and KV element read once, the KV append,
-    and the per-layer activations (x in/out, a, q, o, h, u, routed rows)."""
+    and the per-layer activations (x in/out, a, q, o, h, u, routed rows).  kv_lens: the
+    sequences' KV lengths (ragged workloads); default: every sequence at wl.kv_len."""
     s = wl.shape
     per_layer_w = 2 * (s.qkv_rows * s.hidden + s.hidden * s.q_width + s.n_experts * s.hidden
                        + s.n_local_experts * 3 * s.hidden * s.inter + 2 * s.hidden)
     T = wl.n_tokens
+    lens = [wl.kv_len] * T if kv_lens is None else [int(v) for v in kv_lens]
     act = 2 * T * (6 * s.hidden + 2 * s.q_width) + T * s.top_k * (2 * s.hidden + 2 * s.inter + 4 * s.hidden)
     tot = 0
     for l in range(wl.n_layers):
         w = wl.layer_window(l)
-        span = min(w, wl.kv_len) if w else wl.kv_len
-        kv = T * s.n_kv_heads * span * s.head_dim * 2 * 2
+        positions = sum(min(w, L) if w else L for L in lens)
+        kv = s.n_kv_heads * positions * s.head_dim * 2 * 2
         tot += per_layer_w + kv + T * s.n_kv_heads * s.head_dim * 2 * 2 + act
     return tot
 
@@ -389,6 +394,9 @@ def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None)
     full[sgp.OPS.index("attention")] = 0
     cut = [full, [1] * sgp.N_OPS]
 
+    def popts(**kw):
+        return sgp.make_opts(stage_of_op=cut, stage_lanes=2, **kw)
+
     def run_ms(nst, spl, mb, opts, n, w):
         p = sgp.sgp_pipeline_create(d, spl, nst, mb, T, wl.cap, opts)
         try:
@@ -410,17 +418,16 @@ def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None)
     if split is None:
         _, rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro, wl.cap,
                                            quantum=8, reps=2,
-                                           opts=sgp.make_opts(stage_of_op=cut, stage_times_shared=1))
+                                           opts=popts(stage_times_shared=1))
         cands = [r[0] for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:3]]
-        best = min(cands, key=lambda pa: run_ms(2, [pa, N - pa], micro,
-                                                 sgp.make_opts(stage_of_op=cut), 2, 1))
+        best = min(cands, key=lambda pa: run_ms(2, [pa, N - pa], micro, popts(), 2, 1))
         split = [best, N - best]
         picked = "contention-aware balancer, best of its 3 best candidates by full runs"
-    ms_pipe = run_ms(2, split, micro, sgp.make_opts(stage_of_op=cut), steps, warmup)
+    ms_pipe = run_ms(2, split, micro, popts(), steps, warmup)
     ms_temp = run_ms(1, [N], T, None, steps, warmup)
-    nbytes = algorithmic_bytes(wl)
+    nbytes = algorithmic_bytes(wl, kv_len.cpu().tolist())
     res = {"workload": describe(wl, {})["workload"], "n_tokens": T,
-           "sm_split": split, "split_from": picked, "microbatch": micro,
+           "sm_split": split, "split_from": picked, "microbatch": micro, "lanes_per_stage": 2,
            "pipeline_us": ms_pipe * 1e3, "temporal_us": ms_temp * 1e3,
            "pipeline_speedup": ms_temp / ms_pipe,
            "tokens_per_s_per_gpu": {"pipeline": T / (ms_pipe * 1e-3), "temporal": T / (ms_temp * 1e-3)},
@@ -474,6 +481,7 @@ def run_sgp(args, rank, world, local_rank):
     synth._CHUNK = 1 << 28
     x = synth.x_in(wl, seed, dev)
     kv_len = synth.kv_len(wl, seed, dev)
+    kv_lens = kv_len.cpu().tolist()
     weights = [synth.layer_weights(wl, l, seed, dev) for l in range(wl.n_layers)]
     caches = [synth.kv_cache(wl, l, seed, dev) for l in range(wl.n_layers)]
     layers = sgp.layer_array([sgp.make_layer(w, k, v, wl.layer_window(l))
@@ -494,6 +502,8 @@ def run_sgp(args, rank, world, local_rank):
     micro = args.micro or (T // max(1, wl.microbatches))
     opts = None
     opts_kw = {"weight_reuse": 1} if args.weight_reuse else {}
+    if n_stages > 1 and args.lanes == 2:
+        opts_kw["stage_lanes"] = 2
     if args.cut == "macro" and n_stages == 2:   # 3 stages use A | o-proj+router | experts
         full = [1] * sgp.N_OPS
         full[sgp.OPS.index("attention")] = 0
@@ -686,7 +696,7 @@ def run_sgp(args, rank, world, local_rank):
         paper["split_from"] = "fixed 56 | 96 (the balancer's pick at this shape)"
     if rank != 0:
         return
-    total_bytes = algorithmic_bytes(wl)
+    total_bytes = algorithmic_bytes(wl, kv_lens)
     value = job_tokens_per_s(T, world, ms_pipe)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -706,6 +716,7 @@ def run_sgp(args, rank, world, local_rank):
                                 "virtual_comm": ("3 us + payload / 900 GB/s per collective"
                                                  if args.virtual_comm else None),
                                 "weight_reuse": bool(args.weight_reuse),
+                                "lanes_per_stage": args.lanes if n_stages > 1 else 1,
                                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
         "iteration_us": iter_us,
         "tokens_per_s_per_user": 1e6 / iter_us,

@@ -294,6 +294,12 @@ typedef struct sgp_pipeline_opts {
                                    matrices up to this many MB; 0 = default (off: measured
                                    slower on the 36-layer slice).  Only timing changes;
                                    results are bit-identical                                  */
+    int stage_lanes;            /* FIFOs per stage: 0 or 1 = default, one (every task of a stage
+                                   waits for the task before it on that stage, Section 3.2);
+                                   2 = one per microbatch parity, i.e. two streams per SM pool
+                                   (the pages' prototype runs two stream rows per green
+                                   context, Section 5.3): tasks of the other parity may run
+                                   beside them on the same SMs.  Results are identical        */
     int stage_times_shared;     /* sgp_pipeline_stage_times and the balancer: 0 = default, each
                                    stage timed alone on the GPU; 1 = all stages replay their
                                    tasks at the same time, so each is timed while the others

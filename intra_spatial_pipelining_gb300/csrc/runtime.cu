@@ -1191,12 +1191,16 @@ std::vector<PTask> build_tasks(const sgp_pipeline& p, const sgp_layer* layers, i
     std::vector<int> newidx(all.size());
     for (size_t i = 0; i < order.size(); ++i) newidx[order[i]] = (int)i;
     std::vector<PTask> out(all.size());
-    int last_on_stage[4] = {-1, -1, -1, -1};
+    // one FIFO per stage, or (stage_lanes = 2) one per stage and microbatch parity: the
+    // stage's two lanes share its SM pool, as two streams of one green context do
+    const int lanes = p.opts.stage_lanes == 2 ? 2 : 1;
+    int last_on_lane[4][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};
     for (size_t i = 0; i < order.size(); ++i) {
         PTask t = all[order[i]];
         t.pred_data = t.pred_data >= 0 ? newidx[t.pred_data] : -1;
-        t.pred_stage = last_on_stage[t.stage];
-        last_on_stage[t.stage] = (int)i;
+        int& last = last_on_lane[t.stage][t.mu % lanes];
+        t.pred_stage = last;
+        last = (int)i;
         out[i] = t;
     }
     return out;

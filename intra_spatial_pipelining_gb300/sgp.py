@@ -62,7 +62,7 @@ class sgp_pipeline_opts(C.Structure):
                 ("fault_inject", C.c_uint32), ("fault_task", C.c_int),
                 ("programmatic_launch", C.c_int), ("trace", C.c_int),
                 ("weight_reuse", C.c_int), ("l2_prefetch_mb", C.c_int),
-                ("stage_times_shared", C.c_int)]
+                ("stage_lanes", C.c_int), ("stage_times_shared", C.c_int)]
 
 
 _lib = None
@@ -199,7 +199,7 @@ def make_opts(stage_of_op=None, use_green_contexts: int = 0, green_ctx_flags: in
               serpentine_experts: int = 0, wait_timeout_ns: int = 0, fault_inject: int = 0,
               fault_task: int = 0, programmatic_launch: int = 0,
               trace: int = 0, weight_reuse: int = 0, l2_prefetch_mb: int = 0,
-              stage_times_shared: int = 0) -> sgp_pipeline_opts:
+              stage_lanes: int = 0, stage_times_shared: int = 0) -> sgp_pipeline_opts:
     o = sgp_pipeline_opts()
     if stage_of_op is not None:
         o.custom_cut = 1
@@ -216,6 +216,7 @@ def make_opts(stage_of_op=None, use_green_contexts: int = 0, green_ctx_flags: in
     o.trace = trace
     o.weight_reuse = weight_reuse
     o.l2_prefetch_mb = l2_prefetch_mb
+    o.stage_lanes = stage_lanes
     o.stage_times_shared = stage_times_shared
     return o
 

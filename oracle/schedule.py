@@ -32,9 +32,14 @@ def binding(k: int, n_segments: int, w: int) -> int:
     return 1 if (w == 1 and k == n_segments) else k
 
 
-def build_tasks(n_layers: int, n_micro: int, n_segments: int, w: int = 0):
+def build_tasks(n_layers: int, n_micro: int, n_segments: int, w: int = 0, lanes: int = 1):
     """Tasks of the unrolled forward pass in the global dispatch order
     (layer-major, then microbatch, then segment).
+
+    lanes = 1 is the pages' model: one FIFO per stage.  lanes = 2 gives each stage one FIFO
+    per microbatch parity (two streams sharing the stage's SM pool, as the pages' prototype
+    runs two stream rows per green context, Section 5.3); the stage edge of a task then
+    points to the previous task of its own lane.
 
     Returns a list of dicts with keys: id, layer, micro, seg (1-based), stage,
     data (list of predecessor ids), stage_pred (id or None)."""
@@ -54,9 +59,10 @@ def build_tasks(n_layers: int, n_micro: int, n_segments: int, w: int = 0):
         else:
             data = []
         st = binding(k, n_segments, w)
+        lane = (st, mu % lanes)
         tasks.append({"id": i, "layer": l, "micro": mu, "seg": k, "stage": st,
-                      "data": data, "stage_pred": last_on_stage.get(st)})
-        last_on_stage[st] = i
+                      "data": data, "stage_pred": last_on_stage.get(lane)})
+        last_on_stage[lane] = i
     return tasks
 
 

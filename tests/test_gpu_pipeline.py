@@ -223,13 +223,15 @@ def test_skewed_routing_block_slots():
     assert torch.equal(got[0], out_t)
 
 
-def test_task_dag_matches_schedule_model():
+@pytest.mark.parametrize("lanes", [1, 2])
+def test_task_dag_matches_schedule_model(lanes):
     """Same tasks, data edges and per-stage FIFO edges as the schedule model (task ids
-    may differ: any topological dispatch order is allowed; compare by task key)."""
+    may differ: any topological dispatch order is allowed; compare by task key); with two
+    lanes per stage, one FIFO per stage and microbatch parity."""
     wl, inp = _stack_inputs(3, 256, 9, n_tokens=32)
     d = H.dims(wl.shape)
-    _, _, _, tasks = _pipelined(inp, d, 2, 8, reps=1)
-    model = S.build_tasks(3, 4, 2)
+    _, _, _, tasks = _pipelined(inp, d, 2, 8, sgp.make_opts(stage_lanes=lanes), reps=1)
+    model = S.build_tasks(3, 4, 2, lanes=lanes)
     assert len(tasks) == len(model)
     gkey = [(t[0], t[1], t[2]) for t in tasks]
     mkey = [(m["stage"] - 1, m["layer"], m["micro"]) for m in model]
@@ -366,6 +368,22 @@ def test_weight_reuse_and_serpentine_orders_are_bit_identical(opt):
         assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2]), (opt, micro)
         for (k0, v0), (k1, v1) in zip(ref[3], inp.caches):
             assert torch.equal(k0, k1) and torch.equal(v0, v1), (opt, micro)
+
+
+def test_two_lanes_per_stage_bit_identical():
+    """Two FIFOs per stage (tasks of the other microbatch parity may run beside them on the
+    same SM pool): default and macro cut, 2 and 4 microbatches, bit-identical to temporal."""
+    wl, inp = _stack_inputs(4, 1024, 8)
+    d = H.dims(wl.shape)
+    ref = _temporal(inp, d)
+    full = [1] * sgp.N_OPS
+    full[2] = 0
+    for micro, cut in ((32, None), (16, None), (16, [full, [1] * sgp.N_OPS])):
+        got = _pipelined(inp, d, 2, micro, sgp.make_opts(stage_of_op=cut, stage_lanes=2))
+        assert torch.equal(got[0], ref[0]), micro
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2]), micro
+        for (k0, v0), (k1, v1) in zip(ref[3], inp.caches):
+            assert torch.equal(k0, k1) and torch.equal(v0, v1), micro
 
 
 def test_runs_on_different_streams_are_ordered():

@@ -509,3 +509,18 @@ def test_steady_state_period_is_the_growth_rate_of_the_makespan():
             tasks = S.build_tasks(1, m, K)
             spans.append(S.makespan(tasks, [tau_st[t["seg"] - 1] for t in tasks])[0])
         assert math.isclose(spans[1] - spans[0], S.steady_state_period(tau_st), rel_tol=1e-12)
+
+
+def test_two_lanes_per_stage_hand_example():
+    """Two FIFOs per stage (microbatch parity): one layer, 2 microbatches, 2 segments,
+    tau_A = 3, tau_B = 2.  With one lane microbatch 1's stage-A task waits for microbatch 0's
+    (it starts at 3); with two lanes it starts at 0, and both finish at 5 -- the model then
+    assumes the pool fits both tasks at full speed, a bound the measurement checks."""
+    one = S.build_tasks(1, 2, 2)
+    two = S.build_tasks(1, 2, 2, lanes=2)
+    assert S.makespan(one, [3, 2, 3, 2])[0] == 8
+    T, A, C = S.makespan(two, [3, 2, 3, 2])
+    assert (A, C, T) == ([0, 3, 0, 3], [3, 5, 3, 5], 5)
+    assert [t["stage_pred"] for t in two] == [None, None, None, None]
+    four = S.build_tasks(1, 4, 2, lanes=2)
+    assert [t["stage_pred"] for t in four] == [None, None, None, None, 0, 1, 2, 3]
