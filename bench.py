@@ -512,6 +512,9 @@ def run_sgp(args, rank, world, local_rank):
         opts = sgp.make_opts(**opts_kw)
     balance_rows = None
     balance_shared_rows = None
+    predicted_rows = None
+    balancer_predicted_pick = None
+    fifo_measured_us = None
     sweep_rows = None
     balancer_pick = None
     balancer_shared_pick = None
@@ -547,6 +550,37 @@ def run_sgp(args, rank, world, local_rank):
         shared_opts = sgp.make_opts(stage_times_shared=1, **opts_kw)
         balancer_shared_pick, balance_shared_rows = sgp.sgp_pipeline_balance(
             d, layers, kv_len, x, out, T, micro, wl.cap, quantum=8, reps=3, opts=shared_opts)
+        # Eq. 4-5 makespan from task durations measured under contention, for every split, in
+        # the pages' model (one FIFO per stage); one full run of that model checks the
+        # prediction at its pick
+        fifo_kw = {k: v for k, v in opts_kw.items() if k != "stage_lanes"}
+        fifo_opts = sgp.make_opts(**fifo_kw)
+        predicted_rows = []
+        for r in balance_rows:
+            pp = sgp.sgp_pipeline_create(d, [r[0], N - r[0]], 2, micro, T, wl.cap, fifo_opts)
+            try:
+                t_pred, _ = sgp.sgp_pipeline_predict(pp, layers, kv_len, x, out, T, 2,
+                                                     handoff_us=10.0)
+            finally:
+                sgp.sgp_pipeline_destroy(pp)
+            predicted_rows.append((r[0], t_pred))
+        balancer_predicted_pick = min(predicted_rows, key=lambda r: r[1])[0]
+        pp = sgp.sgp_pipeline_create(d, [balancer_predicted_pick, N - balancer_predicted_pick], 2,
+                                     micro, T, wl.cap, fifo_opts)
+        try:
+            for _ in range(2):
+                sgp.sgp_pipeline_run(pp, layers, kv_len, x, out, T)
+            sgp.check(sgp.sgp_pipeline_sync(pp), "one-FIFO check run")
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(3):
+                sgp.sgp_pipeline_run(pp, layers, kv_len, x, out, T)
+            ev1.record(stream)
+            ev1.synchronize()
+            sgp.check(sgp.sgp_pipeline_sync(pp), "one-FIFO check run")
+            fifo_measured_us = ev0.elapsed_time(ev1) / 3 * 1e3
+        finally:
+            sgp.sgp_pipeline_destroy(pp)
         if args.split == "sweep":
             # every legal split as a full pipelined run: the balancer's picks against the best
             sweep_rows = [(r[0], full_run_ms([r[0], N - r[0]])) for r in balance_rows]
@@ -554,6 +588,8 @@ def run_sgp(args, rank, world, local_rank):
         else:
             # check each model's best few candidates with full pipelined runs
             cands = []
+            for r in sorted(predicted_rows, key=lambda r: r[1])[:3]:
+                cands.append(r[0])
             for rows in (balance_shared_rows, balance_rows):
                 for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:3]:
                     if r[0] not in cands:
@@ -730,8 +766,16 @@ def run_sgp(args, rank, world, local_rank):
             {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in balance_rows],
         "balance_shared": None if balance_shared_rows is None else [
             {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in balance_shared_rows],
+        "predicted_makespan": None if predicted_rows is None else {
+            "model": "Eq. 4-5 over task durations measured with every stage replaying at once, "
+                     "one FIFO per stage, 10 us per cross-stage handoff",
+            "rows": [{"p_A": pa, "us": t} for pa, t in predicted_rows],
+            "at_pick": {"p_A": balancer_predicted_pick,
+                        "predicted_us": dict(predicted_rows)[balancer_predicted_pick],
+                        "measured_us_one_fifo": fifo_measured_us}},
         "balancer_picks": None if balancer_pick is None else {
-            "alone": balancer_pick, "shared": balancer_shared_pick, "chosen": split[0],
+            "alone": balancer_pick, "shared": balancer_shared_pick,
+            "predicted": balancer_predicted_pick, "chosen": split[0],
             "full_run_us": {str(k[0]): v * 1e3 for k, v in sorted(full_runs.items())}},
         "refine_3_stage": refine,
         "split_sweep": None if sweep_rows is None else {

@@ -378,6 +378,20 @@ int sgp_pipeline_trace_sms(sgp_pipeline* p, uint32_t* masks, int max_entries, in
  * Returns SGP_OK, SGP_ERR_INVALID_ARG or SGP_ERR_CUDA. */
 int sgp_pipeline_task_spans(sgp_pipeline* p, uint64_t* spans, int max_tasks, int* n_tasks);
 
+/* Predicts the makespan of a run with the timing recurrence of "SubGPU Pipelining:
+ * Intra-GPU Fine-Grained Spatial Parallelism for LLM Inference", Section 3.2, Eq. 4-5, from
+ * task durations measured under contention: all stages replay their tasks at the same time
+ * (one stream each, data edges dropped, launch trace on), and a task's duration runs from its
+ * start to the start of the next task of its stage FIFO (so it includes the gap between
+ * tasks).  Then A_i = max(C of the data predecessor + handoff_us when it ran on another stage,
+ * C of the stage predecessor), C_i = A_i + tau_i, and *t_pred_us = max C_i.  t_stage_us (host
+ * float[n_stages] or NULL) receives each stage's summed task durations.  The caller's buffers
+ * are written as by a run; outputs are meaningless.  Synchronous.
+ * Returns SGP_OK, SGP_ERR_INVALID_ARG, SGP_ERR_CUDA or a device status of the replays. */
+int sgp_pipeline_predict(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
+                         const int32_t* kv_len, const void* x_in, void* x_out, int n_tokens,
+                         float handoff_us, float* t_pred_us, float* t_stage_us);
+
 /* Number of tasks of the last run's DAG and, when stamps != NULL, per-task
  * {stage, layer_first, micro, pred_data, pred_stage} as int32[5] rows (host memory). */
 int sgp_pipeline_tasks(sgp_pipeline* p, int* n_tasks, int32_t* rows, int max_rows);

@@ -1229,9 +1229,11 @@ int ensure_ws(sgp_pipeline* p, int T, int nflags, int ntrace = 0) {
 
 // Builds the graph of the given tasks.  stage_only >= 0 keeps only that stage's tasks and
 // drops their cross-stage data edges (used for timing one stage alone).
+// zero_first: the graph starts with a memset node that clears the workspace's zeroed region
+// (counters, flags, trace); without it the caller clears that region before launching.
 int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_layer* layers,
                 const int32_t* kv_len, const void* x_in, void* x_out, int T, int32_t* tki,
-                float* tkw, int stage_only, cudaGraph_t* out_graph) {
+                float* tkw, int stage_only, cudaGraph_t* out_graph, bool zero_first = true) {
     const sgp_dims& d = p->dims;
     cudaGraph_t g;
     CK(cudaGraphCreate(&g, 0));
@@ -1245,7 +1247,7 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
     ms.width = p->lay.zero_end - p->lay.zero_beg;
     ms.height = 1;
     ms.pitch = 0;
-    cudaError_t ce = cudaGraphAddMemsetNode(&zero, g, nullptr, 0, &ms);
+    cudaError_t ce = zero_first ? cudaGraphAddMemsetNode(&zero, g, nullptr, 0, &ms) : cudaSuccess;
     if (ce != cudaSuccess) {
         cudaGraphDestroy(g);
         return fail_cuda(ce, "cudaGraphAddMemsetNode");
@@ -1274,7 +1276,7 @@ int build_graph(sgp_pipeline* p, const std::vector<PTask>& tasks, const sgp_laye
         const bool keep_data = stage_only < 0;
         if (keep_data && t.pred_data >= 0) L.deps.push_back(last[t.pred_data]);
         if (t.pred_stage >= 0 && last[t.pred_stage]) L.deps.push_back(last[t.pred_stage]);
-        if (L.deps.empty()) L.deps.push_back((CUgraphNode)zero);
+        if (L.deps.empty() && zero_first) L.deps.push_back((CUgraphNode)zero);
         int l = t.l0, op = t.op0;
         bool first = true;
         while (true) {
@@ -1713,19 +1715,14 @@ extern "C" int sgp_pipeline_trace_sms(sgp_pipeline* p, uint32_t* masks, int max_
     return SGP_OK;
 }
 
-extern "C" int sgp_pipeline_task_spans(sgp_pipeline* p, uint64_t* spans, int max_tasks,
-                                       int* n_tasks) {
-    if (!p || !n_tasks) return fail_arg("NULL");
-    if (!p->opts.trace) return fail_arg("pipeline was created without opts.trace");
-    if (!p->exec) return fail_arg("no run yet");
-    *n_tasks = (int)p->tasks.size();
-    if (!spans || max_tasks <= 0) return SGP_OK;
-    if (p->launched) CK(cudaEventSynchronize(p->done));
-    std::vector<unsigned long long> h((size_t)p->trace_pairs * 2);
-    CK(cudaMemcpy(h.data(), p->ws + p->lay.trace, h.size() * 8, cudaMemcpyDeviceToHost));
-    const int m = p->lay.m;
-    for (int i = 0; i < (int)p->tasks.size() && i < max_tasks; ++i) {
-        const PTask& t = p->tasks[i];
+namespace {
+// Span {first-CTA start, last-CTA end} (ns) of every task, from a copy h of the launch trace
+// ([layer][microbatch][op][part] pairs; the start is stored complemented).  {0, 0}: no launch.
+void spans_from_trace(const std::vector<PTask>& tasks, int m,
+                      const std::vector<unsigned long long>& h, std::vector<uint64_t>& spans) {
+    spans.assign(tasks.size() * 2, 0);
+    for (size_t i = 0; i < tasks.size(); ++i) {
+        const PTask& t = tasks[i];
         uint64_t first = 0, last = 0;
         int l = t.l0, op = t.op0;
         while (true) {
@@ -1745,7 +1742,128 @@ extern "C" int sgp_pipeline_task_spans(sgp_pipeline* p, uint64_t* spans, int max
         spans[2 * i] = first;
         spans[2 * i + 1] = last;
     }
+}
+}  // namespace
+
+extern "C" int sgp_pipeline_task_spans(sgp_pipeline* p, uint64_t* spans, int max_tasks,
+                                       int* n_tasks) {
+    if (!p || !n_tasks) return fail_arg("NULL");
+    if (!p->opts.trace) return fail_arg("pipeline was created without opts.trace");
+    if (!p->exec) return fail_arg("no run yet");
+    *n_tasks = (int)p->tasks.size();
+    if (!spans || max_tasks <= 0) return SGP_OK;
+    if (p->launched) CK(cudaEventSynchronize(p->done));
+    std::vector<unsigned long long> h((size_t)p->trace_pairs * 2);
+    CK(cudaMemcpy(h.data(), p->ws + p->lay.trace, h.size() * 8, cudaMemcpyDeviceToHost));
+    std::vector<uint64_t> sp;
+    spans_from_trace(p->tasks, p->lay.m, h, sp);
+    for (int i = 0; i < (int)p->tasks.size() && i < max_tasks; ++i) {
+        spans[2 * i] = sp[2 * i];
+        spans[2 * i + 1] = sp[2 * i + 1];
+    }
     return SGP_OK;
+}
+
+// Makespan of a run predicted by the pages' timing recurrence (Eq. 4-5) from task durations
+// measured under contention: every stage replays its tasks at the same time, each on its own
+// stream and pool, with the launch trace on; a task's duration tau_i runs from its start to
+// the start of the next task of its FIFO (the last one: to its end), so it includes the gap
+// a stage pays between tasks.  Then A_i = max(C_data + handoff (cross-stage), C_stage),
+// C_i = A_i + tau_i, T = max C_i.
+extern "C" int sgp_pipeline_predict(sgp_pipeline* p, const sgp_layer* layers, int n_layers,
+                                    const int32_t* kv_len, const void* x_in, void* x_out,
+                                    int n_tokens, float handoff_us, float* t_pred_us,
+                                    float* t_stage_us) {
+    int r;
+    if ((r = pipeline_prepare(p, layers, n_layers, kv_len, x_in, x_out, n_tokens)) != SGP_OK)
+        return r;
+    if (!t_pred_us || !(handoff_us >= 0.f)) return fail_arg("t_pred_us / handoff_us");
+    if (p->launched) CK(cudaEventSynchronize(p->done));  // the last run shares the scratch
+    const int m = n_tokens / p->micro;
+    std::vector<PTask> tasks = build_tasks(*p, layers, n_layers, m);
+    const int ntrace = n_layers * m * SGP_N_OPS * 2;
+    if (!p->ws || p->lay.m != m || p->ws_T != n_tokens || p->ws_nflags < (int)tasks.size() ||
+        p->lay.n_trace < ntrace) {
+        if (p->ws) {
+            cudaFree(p->ws);
+            p->ws = nullptr;
+        }
+        if (p->exec) {
+            cudaGraphExecDestroy(p->exec);
+            p->exec = nullptr;
+        }
+        if ((r = ensure_ws(p, n_tokens, (int)tasks.size(), ntrace)) != SGP_OK) return r;
+    }
+    const int n = p->n_stages;
+    std::vector<cudaGraphExec_t> ex(n, nullptr);
+    std::vector<cudaStream_t> st(n, nullptr);
+    cudaEvent_t ev = nullptr;
+    cudaError_t ce = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    for (int i = 0; i < n && r == SGP_OK && ce == cudaSuccess; ++i) {
+        cudaGraph_t g;
+        if ((r = build_graph(p, tasks, layers, kv_len, x_in, x_out, n_tokens, nullptr, nullptr, i,
+                             &g, false)) != SGP_OK)
+            break;
+        ce = cudaGraphInstantiate(&ex[i], g, 0);
+        cudaGraphDestroy(g);
+        if (ce == cudaSuccess) ce = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking);
+    }
+    // two replays (the first warms up), each after one clear of counters, flags and trace
+    for (int rep = 0; rep < 2 && r == SGP_OK && ce == cudaSuccess; ++rep) {
+        ce = cudaMemsetAsync(p->ws + p->lay.zero_beg, 0, p->lay.zero_end - p->lay.zero_beg, st[0]);
+        if (ce == cudaSuccess) ce = cudaEventRecord(ev, st[0]);
+        for (int i = 0; i < n && ce == cudaSuccess; ++i) {
+            if (i > 0) ce = cudaStreamWaitEvent(st[i], ev, 0);
+            if (ce == cudaSuccess) ce = cudaGraphLaunch(ex[i], st[i]);
+        }
+        for (int i = 0; i < n && ce == cudaSuccess; ++i) ce = cudaStreamSynchronize(st[i]);
+    }
+    std::vector<unsigned long long> h((size_t)ntrace * 2);
+    if (r == SGP_OK && ce == cudaSuccess)
+        ce = cudaMemcpy(h.data(), p->ws + p->lay.trace, h.size() * 8, cudaMemcpyDeviceToHost);
+    for (int i = 0; i < n; ++i) {
+        if (ex[i]) cudaGraphExecDestroy(ex[i]);
+        if (st[i]) cudaStreamDestroy(st[i]);
+    }
+    if (ev) cudaEventDestroy(ev);
+    if (r != SGP_OK) return r;
+    if (ce != cudaSuccess) return fail_cuda(ce, "prediction replay");
+    std::vector<uint64_t> sp;
+    spans_from_trace(tasks, m, h, sp);
+    // durations: start to the next start on the same FIFO (stage and lane)
+    const int lanes = p->opts.stage_lanes == 2 ? 2 : 1;
+    std::vector<double> tau(tasks.size(), 0.0);
+    std::vector<int> next(tasks.size(), -1);
+    int last_on[4][2] = {{-1, -1}, {-1, -1}, {-1, -1}, {-1, -1}};
+    for (size_t i = 0; i < tasks.size(); ++i) {
+        int& prev = last_on[tasks[i].stage][tasks[i].mu % lanes];
+        if (prev >= 0) next[prev] = (int)i;
+        prev = (int)i;
+    }
+    double t_st[4] = {0, 0, 0, 0};
+    for (size_t i = 0; i < tasks.size(); ++i) {
+        const double s0 = (double)sp[2 * i], e0 = (double)sp[2 * i + 1];
+        if (e0 == 0) continue;  // a task with no launch takes no time
+        double t = e0 - s0;
+        if (next[i] >= 0 && sp[2 * next[i] + 1] != 0) t = std::max(t, (double)sp[2 * next[i]] - s0);
+        tau[i] = t * 1e-3;
+        t_st[tasks[i].stage] += tau[i];
+    }
+    std::vector<double> C(tasks.size(), 0.0);
+    double T = 0.0;
+    for (size_t i = 0; i < tasks.size(); ++i) {  // tasks are in a topological order
+        const PTask& t = tasks[i];
+        double A = 0.0;
+        if (t.pred_data >= 0)
+            A = std::max(A, C[t.pred_data] + (tasks[t.pred_data].stage != t.stage ? handoff_us : 0.0));
+        if (t.pred_stage >= 0) A = std::max(A, C[t.pred_stage]);
+        C[i] = A + tau[i];
+        T = std::max(T, C[i]);
+    }
+    *t_pred_us = (float)T;
+    if (t_stage_us)
+        for (int i = 0; i < n; ++i) t_stage_us[i] = (float)t_st[i];
+    return read_status(p);
 }
 
 extern "C" void sgp_pipeline_destroy(sgp_pipeline* p) {

@@ -113,6 +113,9 @@ _SIGS = {
                                        C.POINTER(C.c_float), C.c_int, C.POINTER(C.c_int)]),
 }
 
+_SIGS["sgp_pipeline_predict"] = (C.c_int, [C.c_void_p, C.POINTER(sgp_layer), C.c_int, C.c_void_p,
+                                           C.c_void_p, C.c_void_p, C.c_int, C.c_float,
+                                           C.POINTER(C.c_float), C.POINTER(C.c_float)])
 _SIGS["sgp_pipeline_refine"] = (C.c_int, [C.POINTER(sgp_dims), C.POINTER(sgp_layer), C.c_int,
                                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                           C.c_int, C.c_int, C.c_int, C.c_int, C.c_int,
@@ -392,6 +395,18 @@ def sgp_refine_allocation(p0: Sequence[int], quantum: int, p_min: int, objective
     if r < 0:
         raise SgpError(r, "sgp_refine_allocation")
     return tuple(p), t.value, r
+
+
+def sgp_pipeline_predict(p, layers, kv_len, x_in, x_out, n_tokens: int, n_stages: int,
+                         handoff_us: float = 0.0):
+    """Eq. 4-5 makespan (us) predicted from task durations measured under contention, and
+    each stage's summed task durations."""
+    arr = layers if isinstance(layers, C.Array) else layer_array(layers)
+    t = C.c_float()
+    st = (C.c_float * n_stages)()
+    check(lib().sgp_pipeline_predict(p, arr, len(arr), _p(kv_len), _p(x_in), _p(x_out), n_tokens,
+                                     float(handoff_us), C.byref(t), st), "sgp_pipeline_predict")
+    return t.value, list(st)
 
 
 def sgp_pipeline_refine(dims, layers, kv_len, x_in, x_out, n_tokens: int, split: Sequence[int],

@@ -482,6 +482,39 @@ def test_stage_times_shared_and_alone():
     assert all(t > 0 for t in res[0] + res[1])
 
 
+def test_predicted_makespan_from_contended_task_times():
+    """Eq. 4-5 over task durations measured with all stages replaying at once (one FIFO per
+    stage, the pages' model): a positive prediction, at least the busiest stage's summed
+    durations, and close to the measured run (a loose bound)."""
+    wl, inp = _stack_inputs(4, 1024, 18)
+    d = H.dims(wl.shape)
+    T = wl.n_tokens
+    full = [1] * sgp.N_OPS
+    full[2] = 0
+    opts = sgp.make_opts(stage_of_op=[full, [1] * sgp.N_OPS])
+    p = sgp.sgp_pipeline_create(d, _splits(2), 2, 32, T, wl.cap, opts)
+    try:
+        out = torch.empty_like(inp.x)
+        t_pred, t_stage = sgp.sgp_pipeline_predict(p, inp.sgp_layers(), inp.kv_len, inp.x, out, T,
+                                                   2, handoff_us=10.0)
+        for _ in range(3):
+            sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, T)
+        assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(5):
+            sgp.sgp_pipeline_run(p, inp.sgp_layers(), inp.kv_len, inp.x, out, T)
+        e1.record()
+        e1.synchronize()
+        assert sgp.sgp_pipeline_sync(p) == sgp.SGP_OK
+        t_meas = e0.elapsed_time(e1) * 1e3 / 5
+    finally:
+        sgp.sgp_pipeline_destroy(p)
+    print(f"predicted {t_pred:.1f} us (stages {t_stage[0]:.1f}, {t_stage[1]:.1f}), measured {t_meas:.1f} us")
+    assert t_pred > 0 and t_pred >= max(t_stage)
+    assert 0.5 * t_meas <= t_pred <= 2.0 * t_meas
+
+
 def test_refine_three_stage_allocation_on_measured_runs():
     """Algorithm 2 on measured full pipelined runs of a 3-stage cut: the refined split is legal
     (entries multiples of the alignment, at least the minimum partition, same total), it was
