@@ -378,6 +378,17 @@ int sgp_pipeline_trace_sms(sgp_pipeline* p, uint32_t* masks, int max_entries, in
  * Returns SGP_OK, SGP_ERR_INVALID_ARG or SGP_ERR_CUDA. */
 int sgp_pipeline_task_spans(sgp_pipeline* p, uint64_t* spans, int max_tasks, int* n_tasks);
 
+/* The timing recurrence of "SubGPU Pipelining: Intra-GPU Fine-Grained Spatial Parallelism
+ * for LLM Inference", Section 3.2, Eq. 4-5, on a task DAG given as arrays (host memory):
+ * task i (in a topological order: every predecessor index is below i, -1 for none) starts at
+ * A_i = max(C_{pred_data[i]} + handoff when stage[pred_data[i]] != stage[i],
+ * C_{pred_stage[i]}), an empty maximum being 0, and finishes at C_i = A_i + tau[i];
+ * *makespan = max_i C_i, and finish (host double[n_tasks] or NULL) receives every C_i.
+ * Host only.  Returns SGP_OK or SGP_ERR_INVALID_ARG. */
+int sgp_makespan(int n_tasks, const int32_t* pred_data, const int32_t* pred_stage,
+                 const int32_t* stage, const double* tau, double handoff, double* makespan,
+                 double* finish);
+
 /* Predicts the makespan of a run with the timing recurrence of "SubGPU Pipelining:
  * Intra-GPU Fine-Grained Spatial Parallelism for LLM Inference", Section 3.2, Eq. 4-5, from
  * task durations measured under contention: all stages replay their tasks at the same time

@@ -1715,6 +1715,28 @@ extern "C" int sgp_pipeline_trace_sms(sgp_pipeline* p, uint32_t* masks, int max_
     return SGP_OK;
 }
 
+extern "C" int sgp_makespan(int n_tasks, const int32_t* pred_data, const int32_t* pred_stage,
+                            const int32_t* stage, const double* tau, double handoff,
+                            double* makespan, double* finish) {
+    if (n_tasks < 0 || (n_tasks > 0 && (!pred_data || !pred_stage || !stage || !tau)) ||
+        !makespan || !(handoff >= 0.0))
+        return fail_arg("makespan arguments");
+    std::vector<double> C((size_t)n_tasks, 0.0);
+    double T = 0.0;
+    for (int i = 0; i < n_tasks; ++i) {
+        const int d = pred_data[i], q = pred_stage[i];
+        if (d >= i || q >= i) return fail_arg("tasks are not in a topological order");
+        double A = 0.0;
+        if (d >= 0) A = std::max(A, C[d] + (stage[d] != stage[i] ? handoff : 0.0));
+        if (q >= 0) A = std::max(A, C[q]);
+        C[i] = A + tau[i];
+        T = std::max(T, C[i]);
+        if (finish) finish[i] = C[i];
+    }
+    *makespan = T;
+    return SGP_OK;
+}
+
 namespace {
 // Span {first-CTA start, last-CTA end} (ns) of every task, from a copy h of the launch trace
 // ([layer][microbatch][op][part] pairs; the start is stored complemented).  {0, 0}: no launch.
@@ -1849,17 +1871,16 @@ extern "C" int sgp_pipeline_predict(sgp_pipeline* p, const sgp_layer* layers, in
         tau[i] = t * 1e-3;
         t_st[tasks[i].stage] += tau[i];
     }
-    std::vector<double> C(tasks.size(), 0.0);
-    double T = 0.0;
-    for (size_t i = 0; i < tasks.size(); ++i) {  // tasks are in a topological order
-        const PTask& t = tasks[i];
-        double A = 0.0;
-        if (t.pred_data >= 0)
-            A = std::max(A, C[t.pred_data] + (tasks[t.pred_data].stage != t.stage ? handoff_us : 0.0));
-        if (t.pred_stage >= 0) A = std::max(A, C[t.pred_stage]);
-        C[i] = A + tau[i];
-        T = std::max(T, C[i]);
+    std::vector<int32_t> pd(tasks.size()), ps(tasks.size()), stg(tasks.size());
+    for (size_t i = 0; i < tasks.size(); ++i) {
+        pd[i] = tasks[i].pred_data;
+        ps[i] = tasks[i].pred_stage;
+        stg[i] = tasks[i].stage;
     }
+    double T = 0.0;
+    if ((r = sgp_makespan((int)tasks.size(), pd.data(), ps.data(), stg.data(), tau.data(),
+                          handoff_us, &T, nullptr)) != SGP_OK)
+        return r;
     *t_pred_us = (float)T;
     if (t_stage_us)
         for (int i = 0; i < n; ++i) t_stage_us[i] = (float)t_st[i];

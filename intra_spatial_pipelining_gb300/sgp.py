@@ -113,6 +113,9 @@ _SIGS = {
                                        C.POINTER(C.c_float), C.c_int, C.POINTER(C.c_int)]),
 }
 
+_SIGS["sgp_makespan"] = (C.c_int, [C.c_int, C.POINTER(C.c_int32), C.POINTER(C.c_int32),
+                                   C.POINTER(C.c_int32), C.POINTER(C.c_double), C.c_double,
+                                   C.POINTER(C.c_double), C.POINTER(C.c_double)])
 _SIGS["sgp_pipeline_predict"] = (C.c_int, [C.c_void_p, C.POINTER(sgp_layer), C.c_int, C.c_void_p,
                                            C.c_void_p, C.c_void_p, C.c_int, C.c_float,
                                            C.POINTER(C.c_float), C.POINTER(C.c_float)])
@@ -395,6 +398,19 @@ def sgp_refine_allocation(p0: Sequence[int], quantum: int, p_min: int, objective
     if r < 0:
         raise SgpError(r, "sgp_refine_allocation")
     return tuple(p), t.value, r
+
+
+def sgp_makespan(pred_data, pred_stage, stage, tau, handoff: float = 0.0):
+    """Eq. 4-5 on a task DAG (lists in a topological order, -1 = no predecessor); returns
+    (makespan, per-task finish times)."""
+    n = len(tau)
+    arr = lambda v, t: (t * max(1, n))(*v)
+    fin = (C.c_double * max(1, n))()
+    T = C.c_double()
+    check(lib().sgp_makespan(n, arr(pred_data, C.c_int32), arr(pred_stage, C.c_int32),
+                             arr(stage, C.c_int32), arr(tau, C.c_double), float(handoff),
+                             C.byref(T), fin), "sgp_makespan")
+    return T.value, list(fin[:n])
 
 
 def sgp_pipeline_predict(p, layers, kv_len, x_in, x_out, n_tokens: int, n_stages: int,

@@ -120,3 +120,39 @@ def test_library_refuses_bad_arguments(lib):
         sgp.sgp_refine_allocation((152,), 8, 8, lambda p: 1.0)          # one stage
     with pytest.raises(sgp.SgpError):
         sgp.sgp_refine_allocation((4, 148), 8, 8, lambda p: 1.0)        # below p_min
+
+
+# ----------------------------------------------------------------------------- Eq. 4-5
+def _model_arrays(tasks):
+    return ([t["data"][0] if t["data"] else -1 for t in tasks],
+            [t["stage_pred"] if t["stage_pred"] is not None else -1 for t in tasks],
+            [t["stage"] for t in tasks])
+
+
+def test_library_makespan_equals_the_schedule_model(lib):
+    """The recurrence the makespan predictor runs equals the schedule model's Eq. 4-5 (no
+    handoff) on random DAGs of 1-4 layers, 1-4 microbatches, 2-4 segments, with and without
+    boundary reuse and with one or two lanes per stage."""
+    rnd = random.Random(9)
+    for _ in range(40):
+        L, m, K = rnd.randint(1, 4), rnd.randint(1, 4), rnd.randint(2, 4)
+        w = rnd.randint(0, 1) if K > 2 else 0
+        tasks = S.build_tasks(L, m, K, w, lanes=rnd.choice([1, 2]))
+        tau = [rnd.uniform(0.1, 3.0) for _ in tasks]
+        pd, ps, st = _model_arrays(tasks)
+        T, fin = sgp.sgp_makespan(pd, ps, st, tau)
+        T_model, _, C_model = S.makespan(tasks, tau)
+        assert math.isclose(T, T_model, rel_tol=1e-12)
+        assert all(math.isclose(a, b, rel_tol=1e-12) for a, b in zip(fin, C_model))
+
+
+def test_library_makespan_handoff_hand_example(lib):
+    """One layer, 2 microbatches, 2 stages, tau_A = 3, tau_B = 2, handoff 1 on the A -> B edges:
+    A0 [0, 3], B0 [4, 6], A1 [3, 6], B1 [7, 9] -> 9 (8 without the handoff)."""
+    tasks = S.build_tasks(1, 2, 2)
+    pd, ps, st = _model_arrays(tasks)
+    T, fin = sgp.sgp_makespan(pd, ps, st, [3, 2, 3, 2], handoff=1.0)
+    assert T == 9.0 and fin == [3.0, 6.0, 6.0, 9.0]
+    assert sgp.sgp_makespan(pd, ps, st, [3, 2, 3, 2])[0] == 8.0
+    with pytest.raises(sgp.SgpError):             # a predecessor after its successor
+        sgp.sgp_makespan([1, -1], [-1, -1], [0, 1], [1.0, 1.0])
