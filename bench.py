@@ -55,8 +55,11 @@ def parse():
     ap.add_argument("--split", default="auto",
                     help="'auto' (balancer, checked on its 4 best picks), 'sweep' (every legal "
                          "split as a full run) or a comma list of SMs")
-    ap.add_argument("--cut", default="macro", choices=["layer", "macro"],
-                    help="macro: full-attention decode alone on stage A, everything else on B")
+    ap.add_argument("--cut", default="auto", choices=["auto", "layer", "macro", "macro_qkv"],
+                    help="macro: full-attention decode alone on stage A, everything else on B; "
+                         "macro_qkv: also the full layers' RMSNorm-1 and QKV projection on A; "
+                         "layer: ops 0-2 of every layer on A; auto: the faster of macro and "
+                         "macro_qkv after each one's split search")
     ap.add_argument("--no-temporal", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -500,105 +503,99 @@ def run_sgp(args, rank, world, local_rank):
     # ---- pipeline configuration ----
     n_stages = args.stages
     micro = args.micro or (T // max(1, wl.microbatches))
-    opts = None
-    opts_kw = {"weight_reuse": 1} if args.weight_reuse else {}
+    base_kw = {"weight_reuse": 1} if args.weight_reuse else {}
     if n_stages > 1 and args.lanes == 2:
-        opts_kw["stage_lanes"] = 2
-    if args.cut == "macro" and n_stages == 2:   # 3 stages use A | o-proj+router | experts
-        full = [1] * sgp.N_OPS
-        full[sgp.OPS.index("attention")] = 0
-        opts_kw["stage_of_op"] = [full, [1] * sgp.N_OPS]
-    if opts_kw:
-        opts = sgp.make_opts(**opts_kw)
-    balance_rows = None
-    balance_shared_rows = None
-    predicted_rows = None
-    balancer_predicted_pick = None
-    fifo_measured_us = None
-    sweep_rows = None
-    balancer_pick = None
-    balancer_shared_pick = None
-    full_runs = {}
-    refine = None
+        base_kw["stage_lanes"] = 2
 
-    def full_run_ms(spl):
-        key = tuple(spl)
-        if key not in full_runs:
-            p = sgp.sgp_pipeline_create(d, list(spl), len(spl), micro, T, wl.cap, opts)
+    def cut_kw(cut):
+        """Options of a cut (3 stages keep their fixed cut A | B1-B4 | B5-B8)."""
+        kw = dict(base_kw)
+        if cut in ("macro", "macro_qkv") and n_stages == 2:
+            full = [1] * sgp.N_OPS
+            full[sgp.OPS.index("attention")] = 0
+            if cut == "macro_qkv":
+                full[sgp.OPS.index("rmsnorm_attn")] = full[sgp.OPS.index("qkv")] = 0
+            kw["stage_of_op"] = [full, [1] * sgp.N_OPS]
+        return kw
+
+    def run_ms_opts(spl, o, reps=3):
+        p = sgp.sgp_pipeline_create(d, list(spl), len(spl), micro, T, wl.cap, o)
+        try:
             sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
             sgp.check(sgp.sgp_pipeline_sync(p), "pipeline")
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
-            for _ in range(3):
+            for _ in range(reps):
                 sgp.sgp_pipeline_run(p, layers, kv_len, x, out, T)
             t1.record(stream)
             t1.synchronize()
             sgp.check(sgp.sgp_pipeline_sync(p), "pipeline")
+        finally:
             sgp.sgp_pipeline_destroy(p)
-            full_runs[key] = t0.elapsed_time(t1) / 3
-        return full_runs[key]
+        return t0.elapsed_time(t1) / reps
 
-    if n_stages == 1:
-        split = [N]
-    elif args.split in ("auto", "sweep") and n_stages == 2:
-        # the t_A / t_B balancer, with each stage timed alone and with both stages running
-        # at once (sharing HBM and L2 as in a pipelined run)
-        best, balance_rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro,
-                                                      wl.cap, quantum=8, reps=3, opts=opts)
-        balancer_pick = best
-        shared_opts = sgp.make_opts(stage_times_shared=1, **opts_kw)
-        balancer_shared_pick, balance_shared_rows = sgp.sgp_pipeline_balance(
-            d, layers, kv_len, x, out, T, micro, wl.cap, quantum=8, reps=3, opts=shared_opts)
-        # Eq. 4-5 makespan from task durations measured under contention, for every split, in
-        # the pages' model (one FIFO per stage); one full run of that model checks the
-        # prediction at its pick
-        fifo_kw = {k: v for k, v in opts_kw.items() if k != "stage_lanes"}
-        fifo_opts = sgp.make_opts(**fifo_kw)
-        predicted_rows = []
-        for r in balance_rows:
+    def search_two_stage(cut, sweep):
+        """The SM split of a 2-stage cut: the t_A / t_B balancer with stages timed alone and
+        under contention, and the Eq. 4-5 makespan from contended task times; each model's best
+        candidates (or, with sweep, every legal split) are checked by full pipelined runs."""
+        kw = cut_kw(cut)
+        o = sgp.make_opts(**kw) if kw else None
+        res = {"cut": cut, "full_runs": {}}
+        best_alone, rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro,
+                                                    wl.cap, quantum=8, reps=3, opts=o)
+        best_shared, rows_shared = sgp.sgp_pipeline_balance(
+            d, layers, kv_len, x, out, T, micro, wl.cap, quantum=8, reps=3,
+            opts=sgp.make_opts(stage_times_shared=1, **kw))
+        # the pages' model (one FIFO per stage): the prediction, checked at its pick by a run
+        fifo_opts = sgp.make_opts(**{k: v for k, v in kw.items() if k != "stage_lanes"})
+        pred = []
+        for r in rows:
             pp = sgp.sgp_pipeline_create(d, [r[0], N - r[0]], 2, micro, T, wl.cap, fifo_opts)
             try:
                 t_pred, _ = sgp.sgp_pipeline_predict(pp, layers, kv_len, x, out, T, 2,
                                                      handoff_us=10.0)
             finally:
                 sgp.sgp_pipeline_destroy(pp)
-            predicted_rows.append((r[0], t_pred))
-        balancer_predicted_pick = min(predicted_rows, key=lambda r: r[1])[0]
-        pp = sgp.sgp_pipeline_create(d, [balancer_predicted_pick, N - balancer_predicted_pick], 2,
-                                     micro, T, wl.cap, fifo_opts)
-        try:
-            for _ in range(2):
-                sgp.sgp_pipeline_run(pp, layers, kv_len, x, out, T)
-            sgp.check(sgp.sgp_pipeline_sync(pp), "one-FIFO check run")
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ev0.record(stream)
-            for _ in range(3):
-                sgp.sgp_pipeline_run(pp, layers, kv_len, x, out, T)
-            ev1.record(stream)
-            ev1.synchronize()
-            sgp.check(sgp.sgp_pipeline_sync(pp), "one-FIFO check run")
-            fifo_measured_us = ev0.elapsed_time(ev1) / 3 * 1e3
-        finally:
-            sgp.sgp_pipeline_destroy(pp)
-        if args.split == "sweep":
-            # every legal split as a full pipelined run: the balancer's picks against the best
-            sweep_rows = [(r[0], full_run_ms([r[0], N - r[0]])) for r in balance_rows]
-            best = min(sweep_rows, key=lambda r: r[1])[0]
+            pred.append((r[0], t_pred))
+        best_pred = min(pred, key=lambda r: r[1])[0]
+        fifo_us = run_ms_opts([best_pred, N - best_pred], fifo_opts) * 1e3
+
+        def full(pa):
+            if pa not in res["full_runs"]:
+                res["full_runs"][pa] = run_ms_opts([pa, N - pa], o)
+            return res["full_runs"][pa]
+        if sweep:
+            cands = [r[0] for r in rows]
         else:
-            # check each model's best few candidates with full pipelined runs
-            cands = []
-            for r in sorted(predicted_rows, key=lambda r: r[1])[:3]:
-                cands.append(r[0])
-            for rows in (balance_shared_rows, balance_rows):
-                for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:3]:
+            cands = [r[0] for r in sorted(pred, key=lambda r: r[1])[:3]]
+            for rr in (rows_shared, rows):
+                for r in sorted(rr, key=lambda r: max(r[1], r[2]))[:3]:
                     if r[0] not in cands:
                         cands.append(r[0])
-            best = min(cands, key=lambda pa: full_run_ms([pa, N - pa]))
-        split = [best, N - best]
+        best = min(cands, key=full)
+        res.update(split=[best, N - best], ms=full(best), opts_kw=kw, balance=rows,
+                   balance_shared=rows_shared, predicted=pred,
+                   picks={"alone": best_alone, "shared": best_shared, "predicted": best_pred},
+                   fifo_check={"p_A": best_pred, "predicted_us": dict(pred)[best_pred],
+                               "measured_us_one_fifo": fifo_us})
+        return res
+
+    refine = None
+    search = None
+    cut_results = None
+    opts_kw = cut_kw(args.cut)
+    if n_stages == 1:
+        split = [N]
+    elif args.split in ("auto", "sweep") and n_stages == 2:
+        cuts = ["macro", "macro_qkv"] if args.cut == "auto" else [args.cut]
+        cut_results = [search_two_stage(c, args.split == "sweep") for c in cuts]
+        search = min(cut_results, key=lambda r: r["ms"])
+        split, opts_kw = search["split"], search["opts_kw"]
     elif args.split == "auto":
         # 3 stages: pairwise-line refinement (Algorithm 2) on measured full runs, from a uniform
         # seed and from a service-proportional one (SMs in proportion to each stage's work)
+        opts = sgp.make_opts(**opts_kw) if opts_kw else None
         a = max(1, info.sm_alignment)
         pmin = max(a, info.sm_min_partition)
         p0 = max(a, (N // 3 // a) * a)
@@ -622,6 +619,9 @@ def run_sgp(args, rank, world, local_rank):
                 best_t, split = t_us, spl
     else:
         split = [int(v) for v in args.split.split(",")]
+        if args.cut == "auto":
+            opts_kw = cut_kw("macro")
+    opts = sgp.make_opts(**opts_kw) if opts_kw else None
 
     def make(nst, spl, mb, o):
         return sgp.sgp_pipeline_create(d, spl, nst, mb, T, wl.cap, o)
@@ -746,7 +746,8 @@ def run_sgp(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms_pipe, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": describe(wl, {"mode": f"spatial pipeline, {n_stages} stages",
-                                "cut": args.cut if n_stages == 2 else "A | B1-B4 | B5-B8",
+                                "cut": ((search["cut"] if search else args.cut)
+                                        if n_stages == 2 else "A | B1-B4 | B5-B8"),
                                 "sm_split": split,
                                 "microbatches": T // micro, "microbatch": micro,
                                 "virtual_comm": ("3 us + payload / 900 GB/s per collective"
@@ -762,26 +763,26 @@ def run_sgp(args, rank, world, local_rank):
             "iteration_us": ms_temp * 1e3, "tokens_per_s": job_tokens_per_s(T, world, ms_temp),
             "dram_pct_of_peak": 100.0 * total_bytes / (ms_temp * 1e-3) / 1e9 / peak,
             "pipeline_speedup": ms_temp / ms_pipe},
-        "balance": None if balance_rows is None else [
-            {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in balance_rows],
-        "balance_shared": None if balance_shared_rows is None else [
-            {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in balance_shared_rows],
-        "predicted_makespan": None if predicted_rows is None else {
+        "balance": None if search is None else [
+            {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in search["balance"]],
+        "balance_shared": None if search is None else [
+            {"p_A": r[0], "t_A_us": r[1], "t_B_us": r[2]} for r in search["balance_shared"]],
+        "predicted_makespan": None if search is None else {
             "model": "Eq. 4-5 over task durations measured with every stage replaying at once, "
                      "one FIFO per stage, 10 us per cross-stage handoff",
-            "rows": [{"p_A": pa, "us": t} for pa, t in predicted_rows],
-            "at_pick": {"p_A": balancer_predicted_pick,
-                        "predicted_us": dict(predicted_rows)[balancer_predicted_pick],
-                        "measured_us_one_fifo": fifo_measured_us}},
-        "balancer_picks": None if balancer_pick is None else {
-            "alone": balancer_pick, "shared": balancer_shared_pick,
-            "predicted": balancer_predicted_pick, "chosen": split[0],
-            "full_run_us": {str(k[0]): v * 1e3 for k, v in sorted(full_runs.items())}},
+            "rows": [{"p_A": pa, "us": t} for pa, t in search["predicted"]],
+            "at_pick": search["fifo_check"]},
+        "balancer_picks": None if search is None or args.split == "sweep" else dict(
+            search["picks"], chosen=split[0],
+            full_run_us={str(k): v * 1e3 for k, v in sorted(search["full_runs"].items())}),
+        "cut_search": None if cut_results is None else [
+            {"cut": r["cut"], "sm_split": r["split"], "us": r["ms"] * 1e3} for r in cut_results],
         "refine_3_stage": refine,
-        "split_sweep": None if sweep_rows is None else {
-            "balancer_pick": balancer_pick,
-            "sweep_best": min(sweep_rows, key=lambda r: r[1])[0],
-            "full_run_us": [{"p_A": pa, "us": ms * 1e3} for pa, ms in sweep_rows]},
+        "split_sweep": None if search is None or args.split != "sweep" else {
+            "balancer_pick": search["picks"]["alone"],
+            "sweep_best": split[0],
+            "full_run_us": [{"p_A": pa, "us": ms * 1e3}
+                            for pa, ms in sorted(search["full_runs"].items())]},
         "roofline": roofline,
         "paper_shape": paper,
         "cpu_baseline": cpu,
