@@ -55,9 +55,10 @@ def parse():
     ap.add_argument("--split", default="auto",
                     help="'auto' (balancer, checked on its 4 best picks), 'sweep' (every legal "
                          "split as a full run) or a comma list of SMs")
-    ap.add_argument("--cut", default="auto", choices=["auto", "layer", "macro", "macro_qkv"],
+    ap.add_argument("--cut", default="auto", choices=["auto", "layer", "macro", "macro_qkv", "macro_oproj"],
                     help="macro: full-attention decode alone on stage A, everything else on B; "
                          "macro_qkv: also the full layers' RMSNorm-1 and QKV projection on A; "
+                         "macro_oproj: the full layers' ops up to the output projection on A; "
                          "layer: ops 0-2 of every layer on A; auto: the faster of macro and "
                          "macro_qkv after each one's split search")
     ap.add_argument("--no-temporal", action="store_true")
@@ -510,11 +511,13 @@ def run_sgp(args, rank, world, local_rank):
     def cut_kw(cut):
         """Options of a cut (3 stages keep their fixed cut A | B1-B4 | B5-B8)."""
         kw = dict(base_kw)
-        if cut in ("macro", "macro_qkv") and n_stages == 2:
+        if cut in ("macro", "macro_qkv", "macro_oproj") and n_stages == 2:
             full = [1] * sgp.N_OPS
             full[sgp.OPS.index("attention")] = 0
-            if cut == "macro_qkv":
+            if cut in ("macro_qkv", "macro_oproj"):
                 full[sgp.OPS.index("rmsnorm_attn")] = full[sgp.OPS.index("qkv")] = 0
+            if cut == "macro_oproj":
+                full[sgp.OPS.index("oproj")] = 0
             kw["stage_of_op"] = [full, [1] * sgp.N_OPS]
         return kw
 
