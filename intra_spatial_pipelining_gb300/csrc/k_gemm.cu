@@ -121,9 +121,11 @@ __device__ __forceinline__ void store_swiglu4(const EpiArgs& e, int trow, int i0
     *reinterpret_cast<uint2*>(e.out + (size_t)trow * e.ld + i0) = o;
 }
 
-// One work unit = (group, 128-row weight tile, K segment) and its token range.
+// One work unit = (group, 128-row weight tile, K segment) and its token range, covered in
+// npass passes of up to n_cap tokens; the last pass also carries `tail` more rows (0: none)
+// when the rows past its end fit tail_cap.
 struct Unit {
-    int g, mt, ks, kb0, nk, n, npass, tma_r0, lr0;
+    int g, mt, ks, kb0, nk, n, npass, tail, tma_r0, lr0;
 };
 
 __device__ __forceinline__ Unit unit_info(const GemmProblem& P, int u, const KCtx& c) {
@@ -152,7 +154,13 @@ __device__ __forceinline__ Unit unit_info(const GemmProblem& P, int u, const KCt
         x.n = 0;
     }
     if (x.nk <= 0) x.n = 0;
-    x.npass = (((x.n + 15) & ~15) + P.n_cap - 1) / P.n_cap;
+    const int n_pad = (x.n + 15) & ~15;
+    x.npass = (n_pad + P.n_cap - 1) / P.n_cap;
+    x.tail = 0;
+    if (P.tail_cap > 0 && x.npass >= 2 && n_pad - (x.npass - 1) * P.n_cap <= P.tail_cap) {
+        x.tail = n_pad - (x.npass - 1) * P.n_cap;
+        x.npass -= 1;
+    }
     return x;
 }
 
@@ -166,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int S = P.stages;
     const int stage_a = P.kps * 128 * 128;      // A: kps k-blocks of 128 rows x 64 bf16
     const int stage_b = P.kps * P.n_cap * 128;  // B: kps k-blocks of n_cap rows
-    const int stage_bytes = stage_a + stage_b;
+    const int stage_t = P.kps * P.tail_cap * 128;  // tail rows (after B)
+    const int stage_bytes = stage_a + stage_b + stage_t;
     float* Ts = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);  // [n_cap][128]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + P.ring_bytes);
     uint64_t* empty = full + S;
@@ -179,6 +188,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     griddep_launch();
     uint32_t acc_cols = 32;
     while (acc_cols < (uint32_t)P.n_cap) acc_cols <<= 1;
+    // accumulators: two buffers (the epilogue drains one while the next job accumulates into
+    // the other); with tail passes one buffer of the main and the tail accumulator side by
+    // side (the tail's columns follow the main ones)
+    const uint32_t nbuf = P.tail_cap > 0 ? 1u : 2u;
+    uint32_t tmem_cols = 2 * acc_cols;
+    if (P.tail_cap > 0) {
+        tmem_cols = 32;
+        while (tmem_cols < acc_cols + (uint32_t)P.tail_cap) tmem_cols <<= 1;
+    }
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -195,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&P.tmB);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 2 * acc_cols);
+        tmem_alloc(tmem_slot, tmem_cols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -253,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int pass = 0; pass < x.npass; ++pass) {
                     const int c0 = pass * P.n_cap;
                     const uint64_t pol_w = pass + 1 < x.npass ? pol_keep : pol_drop;
+                    const bool with_tail = x.tail > 0 && pass + 1 == x.npass;
+                    const uint32_t tx = (uint32_t)(stage_a + stage_b + (with_tail ? stage_t : 0));
                     for (int i = 0; i < x.nk; ++i, ++it) {
                         const int s = it % S;
                         const uint32_t j = it / S;
@@ -289,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint8_t* sa = smem + (size_t)s * stage_bytes;
                         uint8_t* sb = sa + stage_a;
                         const int kb = x.kb0 + i * P.kps;
-                        mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+                        mbar_arrive_expect_tx(&full[s], tx);
                         if (P.a_4d)
                             tma_load_4d(sa, &P.tmA, &full[s], 0, rowA1, 0, kb, pol_w);
                         else
@@ -302,6 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
                             tma_load_3d(sb, &P.tmB, &full[s], 0, x.tma_r0 + c0, kb, pol_x);
                         }
+                        if (with_tail)  // grouped problems only: never deferred
+                            tma_load_3d(sb + stage_b, &P.tmB2, &full[s], 0, x.tma_r0 + c0 + P.n_cap,
+                                        kb, pol_x);
                         issued_mask |= 1u << s;
                         issued_par = (issued_par & ~(1u << s)) | ((j & 1u) << s);
                     }
@@ -333,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n_pad = (x.n + 15) & ~15;
                 for (int pass = 0; pass < x.npass && ok; ++pass, ++job) {
                     const int np = min(P.n_cap, n_pad - pass * P.n_cap);
-                    const uint32_t b = job & 1u, jb = job >> 1;
+                    const bool with_tail = x.tail > 0 && pass + 1 == x.npass;
+                    const uint32_t b = job % nbuf, jb = job / nbuf;
                     if (jb > 0 && !mbar_wait(&tempty[b], (jb - 1) & 1u, ctx.timeout_ns)) {
                         report(ctx, ST_TIMEOUT, 5);
                         atomicExch(sh_err, 1);
@@ -343,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t acc = tmem + b * acc_cols;
                     const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)np);
+                    const uint32_t idesc_t = idesc_bf16_f32(128, (uint32_t)max(16, x.tail));
                     for (int i = 0; i < x.nk; ++i, ++it) {
                         const int s = it % S;
                         const uint32_t j = it / S;
@@ -359,10 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int kk = 0; kk < kGemmKpsMax; ++kk)
                             if (kk < P.kps) {
 #pragma unroll
-                                for (int k = 0; k < 4; ++k)
+                                for (int k = 0; k < 4; ++k) {
                                     tc_mma_bf16(acc, smem_desc_sw128(sa + kk * 16384 + 32 * k),
                                                 smem_desc_sw128(sb + kk * (P.n_cap * 128) + 32 * k),
                                                 idesc, (i > 0 || kk > 0 || k > 0) ? 1u : 0u);
+                                    // the tail rows take the same k steps in the same order
+                                    if (with_tail)
+                                        tc_mma_bf16(acc + acc_cols,
+                                                    smem_desc_sw128(sa + kk * 16384 + 32 * k),
+                                                    smem_desc_sw128(sb + stage_b + kk * (P.tail_cap * 128) + 32 * k),
+                                                    idesc_t, (i > 0 || kk > 0 || k > 0) ? 1u : 0u);
+                                }
                             }
                         tc_commit(&empty[s]);
                     }
@@ -382,9 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Unit x = unit_info(P, u, ctx);
             const int n_pad = (x.n + 15) & ~15;
             for (int pass = 0; pass < x.npass; ++pass, ++job) {
-                const int c0 = pass * P.n_cap;
-                const int np = min(P.n_cap, n_pad - c0);
-                const uint32_t b = job & 1u, jb = job >> 1;
+                const uint32_t b = job % nbuf, jb = job / nbuf;
+                const bool with_tail = x.tail > 0 && pass + 1 == x.npass;
                 const bool w = mbar_wait(&tfull[b], jb & 1u, ctx.timeout_ns);
                 if (!w) {
                     report(ctx, ST_TIMEOUT, 3);
@@ -398,70 +429,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tbase = tmem + b * acc_cols + ((uint32_t)(q * 32) << 16);
-                const int nv = min(np, x.n - c0);
-                // the accumulator leaves TMEM in chunks of kTsRows tokens through Ts
-                for (int ch = 0; ch < np; ch += kTsRows) {
-                    const int cn = min(kTsRows, np - ch);
-                    if (ch > 0) {
-                        // the previous chunk's readers (bulk store / epilogue) are done with Ts
-                        if (issuer) bulk_wait_read();
-                        epi_bar();
-                    }
-                    for (int cc = 0; cc < cn; cc += 16) {
-                        uint32_t v[16];
-                        tmem_ld_x16(tbase + (uint32_t)(ch + cc), v);
-                        tmem_ld_wait();
+                // part 0: the pass's own accumulator; part 1: the tail rows that follow it
+                for (int part = 0; part < (with_tail ? 2 : 1); ++part) {
+                    const int c0 = pass * P.n_cap + part * P.n_cap;
+                    const int np = part ? x.tail : min(P.n_cap, n_pad - c0);
+                    const uint32_t tbase = tmem + (part ? acc_cols : b * acc_cols) +
+                                           ((uint32_t)(q * 32) << 16);
+                    const int nv = min(np, x.n - c0);
+                    const bool last_part = part + 1 == (with_tail ? 2 : 1);
+                    // the accumulator leaves TMEM in chunks of ts_rows tokens through Ts
+                    for (int ch = 0; ch < np; ch += P.ts_rows) {
+                        const int cn = min(P.ts_rows, np - ch);
+                        if (ch > 0 || part > 0) {
+                            // the previous chunk's readers (bulk store / epilogue) are done with Ts
+                            if (issuer) bulk_wait_read();
+                            epi_bar();
+                        }
+                        for (int cc = 0; cc < cn; cc += 16) {
+                            uint32_t v[16];
+                            tmem_ld_x16(tbase + (uint32_t)(ch + cc), v);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) Ts[(cc + t) * 128 + row] = __uint_as_float(v[t]);
-                    }
-                    if (ch + kTsRows >= np) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty[b]);  // the accumulator may be reused
-                    }
-                    const int cv = min(cn, nv - ch);  // valid tokens of this chunk
-                    if (P.fused_epi) {
-                        // K split 1: the tile is the final sum; apply the epilogue from Ts
-                        // (the next chunk's or job's barrier keeps Ts until every warp is done)
-                        epi_bar();
-                        const EpiArgs& e = P.epi;
-                        const int ew = warp - 2;  // 0..3
-                        const int prow0 = x.lr0 + c0 + ch;  // partial-row numbering of token 0
-                        if (e.mode == EPI_SWIGLU) {
-                            const int h = lane >> 4, q4 = lane & 15;
-                            const int i0 = x.mt * 64 + 4 * q4;
-                            for (int t = 2 * ew + h; t < cv; t += 8) {
-                                if (i0 < e.n_out) {
-                                    const float4 g = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * q4);
-                                    const float4 up = *reinterpret_cast<const float4*>(Ts + t * 128 + 64 + 4 * q4);
-                                    store_swiglu4(e, P.out_row0 + prow0 + t, i0, g, up);
+                            for (int t = 0; t < 16; ++t) Ts[(cc + t) * 128 + row] = __uint_as_float(v[t]);
+                        }
+                        if (last_part && ch + P.ts_rows >= np) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[b]);  // the accumulator may be reused
+                        }
+                        const int cv = min(cn, nv - ch);  // valid tokens of this chunk
+                        if (P.fused_epi) {
+                            // K split 1: the tile is the final sum; apply the epilogue from Ts
+                            // (the next chunk's or job's barrier keeps Ts until every warp is done)
+                            epi_bar();
+                            const EpiArgs& e = P.epi;
+                            const int ew = warp - 2;  // 0..3
+                            const int prow0 = x.lr0 + c0 + ch;  // partial-row numbering of token 0
+                            if (e.mode == EPI_SWIGLU) {
+                                const int h = lane >> 4, q4 = lane & 15;
+                                const int i0 = x.mt * 64 + 4 * q4;
+                                for (int t = 2 * ew + h; t < cv; t += 8) {
+                                    if (i0 < e.n_out) {
+                                        const float4 g = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * q4);
+                                        const float4 up = *reinterpret_cast<const float4*>(Ts + t * 128 + 64 + 4 * q4);
+                                        store_swiglu4(e, P.out_row0 + prow0 + t, i0, g, up);
+                                    }
                                 }
+                            } else {
+                                const int f0 = x.mt * 128 + 4 * lane;
+                                for (int t = ew; t < cv; t += 4) {
+                                    const int trow = P.out_row0 + prow0 + t;
+                                    float4 v = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * lane);
+                                    if (e.mode == EPI_QKV && e.rope_theta > 0.f) {
+                                        // pair partner (feature +-32 of the same head): lane ^ 8
+                                        const float4 pv = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * (lane ^ 8));
+                                        if (f0 < e.n_out && f0 < e.q_width + e.nkv * e.d)
+                                            rope_rotate(v, pv, f0 & 63, e.kv_len[trow] - 1, e);
+                                    }
+                                    if (f0 < e.n_out) store_out4(e, ctx, e.mode, trow, f0, v);
+                                }
+                            }
+                        } else if (cv > 0) {
+                            fence_proxy_async();
+                            epi_bar();
+                            if (issuer) {
+                                bulk_store(P.partial + (((size_t)x.mt * P.ksplit + x.ks) * P.R + x.lr0 + c0 + ch) * 128,
+                                           Ts, (uint32_t)cv * 512u);
+                                bulk_commit();
                             }
                         } else {
-                            const int f0 = x.mt * 128 + 4 * lane;
-                            for (int t = ew; t < cv; t += 4) {
-                                const int trow = P.out_row0 + prow0 + t;
-                                float4 v = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * lane);
-                                if (e.mode == EPI_QKV && e.rope_theta > 0.f) {
-                                    // pair partner (feature +-32 of the same head): lane ^ 8
-                                    const float4 pv = *reinterpret_cast<const float4*>(Ts + t * 128 + 4 * (lane ^ 8));
-                                    if (f0 < e.n_out && f0 < e.q_width + e.nkv * e.d)
-                                        rope_rotate(v, pv, f0 & 63, e.kv_len[trow] - 1, e);
-                                }
-                                if (f0 < e.n_out) store_out4(e, ctx, e.mode, trow, f0, v);
-                            }
+                            epi_bar();
                         }
-                    } else if (cv > 0) {
-                        fence_proxy_async();
-                        epi_bar();
-                        if (issuer) {
-                            bulk_store(P.partial + (((size_t)x.mt * P.ksplit + x.ks) * P.R + x.lr0 + c0 + ch) * 128,
-                                       Ts, (uint32_t)cv * 512u);
-                            bulk_commit();
-                        }
-                    } else {
-                        epi_bar();
                     }
                 }
             }
@@ -471,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 2 * acc_cols);
+        tmem_dealloc(tmem, tmem_cols);
     }
     task_end(ctx);
 }
@@ -720,24 +758,27 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(const GemvProblem
 
 }  // namespace
 
-size_t gemm_tc_ring_bytes(int n_cap, int stages, int kps) {
-    // stage ring, then the accumulator staging area [min(n_cap, kTsRows)][128] fp32
-    return (size_t)stages * kps * (128 * 128 + n_cap * 128) +
-           (size_t)std::min(n_cap, kTsRows) * 512;
+size_t gemm_tc_ring_bytes(int n_cap, int stages, int kps, int tail_cap, int ts_rows) {
+    // stage ring, then the accumulator staging area [min(n_cap, ts_rows)][128] fp32
+    return (size_t)stages * kps * (128 * 128 + (n_cap + tail_cap) * 128) +
+           (size_t)std::min(n_cap, ts_rows) * 512;
 }
 
-size_t gemm_tc_smem_bytes(int n_cap, int stages, int kps) {
-    return gemm_tc_ring_bytes(n_cap, stages, kps) + 1024 + 256;
+size_t gemm_tc_smem_bytes(int n_cap, int stages, int kps, int tail_cap, int ts_rows) {
+    return gemm_tc_ring_bytes(n_cap, stages, kps, tail_cap, ts_rows) + 1024 + 256;
 }
 
 int enqueue_gemm_tc(Launcher& L, const GemmProblem& p, const KCtx& c) {
     dim3 grid(std::max(1, std::min(p.n_units, p.grid))), block(kThreads);
-    if ((p.kps != 1 && p.kps != 2) ||
-        (size_t)p.ring_bytes != gemm_tc_ring_bytes(p.n_cap, p.stages, p.kps))
+    // the tail accumulator sits beside a single main buffer in the 512 TMEM columns
+    if ((p.kps != 1 && p.kps != 2) || (p.ts_rows != 32 && p.ts_rows != 64) ||
+        p.tail_cap < 0 || (p.tail_cap & 15) || p.tail_cap + p.n_cap > 512 ||
+        (p.tail_cap > 0 && p.group_offsets == nullptr) ||
+        (size_t)p.ring_bytes != gemm_tc_ring_bytes(p.n_cap, p.stages, p.kps, p.tail_cap, p.ts_rows))
         return (int)cudaErrorInvalidValue;
     void* args[] = {(void*)&p, (void*)&c};
     return L.launch((const void*)gemm_tc_kernel, grid, block,
-                    gemm_tc_smem_bytes(p.n_cap, p.stages, p.kps), args, true);
+                    gemm_tc_smem_bytes(p.n_cap, p.stages, p.kps, p.tail_cap, p.ts_rows), args, true);
 }
 
 int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c) {

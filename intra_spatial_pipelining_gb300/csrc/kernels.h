@@ -77,6 +77,7 @@ struct GemmProblem {
     //          SwiGLU 4-D {64, rows, half, k-blocks} box {64, 64, 2, 2}, half = gate/up (I rows)
     CUtensorMap tmA;
     CUtensorMap tmB;        // activations, 3-D {64, rows, k-blocks}, box {64, n_cap, 2}, SW128
+    CUtensorMap tmB2;       // the same activations, box {64, tail_cap, kps} (tail_cap > 0)
     int a_4d;               // 1: SwiGLU (4-D weight map)
     int K, kb_total, ksplit;
     int kps;                // k-blocks per stage (1 or 2)
@@ -90,6 +91,11 @@ struct GemmProblem {
     int row0, nrows;        // dense: token rows [row0, row0 + nrows)
     int R;                  // rows of the partial-sum buffer
     int n_cap;              // tokens per pass (multiple of 16, <= kGemmMaxN)
+    int tail_cap;           // grouped only: a last pass of at most tail_cap rows joins the pass
+                            //    before it (a second accumulator fed by its own rows in every
+                            //    stage), so the weight tile is not streamed once more for a few
+                            //    rows; 0 = off.  Multiple of 16.
+    int ts_rows;            // tokens per chunk of the accumulator's way out through shared memory
     int stages;             // shared-memory pipeline depth
     int ring_bytes;         // bytes of the stage ring (also holds the staged accumulator)
     int serpentine;         // visit groups in reverse order
@@ -223,8 +229,8 @@ int enqueue_gemm_finish(Launcher& L, const FinishProblem& p, const KCtx& c);
 int enqueue_gemv(Launcher& L, const GemvProblem& p, const KCtx& c);
 
 // shared-memory bytes a tcgen05 GEMM launch needs for (n_cap, stages)
-size_t gemm_tc_ring_bytes(int n_cap, int stages, int kps);
-size_t gemm_tc_smem_bytes(int n_cap, int stages, int kps);
+size_t gemm_tc_ring_bytes(int n_cap, int stages, int kps, int tail_cap, int ts_rows);
+size_t gemm_tc_smem_bytes(int n_cap, int stages, int kps, int tail_cap, int ts_rows);
 // attention chunk length (positions per split-KV work item); fixed, never SM-dependent
 constexpr int kAttnChunk = 1024;
 // Positions per attention stage for a call: 64 (12 warps per CTA) when the full batch has at

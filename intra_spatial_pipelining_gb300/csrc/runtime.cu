@@ -663,7 +663,20 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
         const uint64_t str[2] = {rowb, 128};
         const uint32_t box[3] = {64, (uint32_t)p.n_cap, (uint32_t)gs.kps};
         if ((r = make_tmap_nd(&p.tmB, xb, 3, dims, str, box)) != SGP_OK) return r;
+        // A slot that overflows a full pass by a few rows: those rows ride along with the last
+        // full pass (second accumulator) instead of a pass of their own, which would stream
+        // the weight tile once more.  For grouped passes capped at the MMA's 256 tokens when
+        // a slot is expected to fit one pass: the tail accumulator leaves room for only one
+        // accumulator buffer, so every further pass would wait for the previous one's drain
+        // (measured at 512 rows per slot: expert gate/up 101 -> 125 us).  The staging chunk
+        // shrinks to 32 tokens so that the ring keeps its depth.
+        if (grouped && p.n_cap == kGemmMaxN && cdiv(R, gs.n_groups) <= kGemmMaxN + 16) {
+            p.tail_cap = 32;
+            const uint32_t box2[3] = {64, (uint32_t)p.tail_cap, (uint32_t)gs.kps};
+            if ((r = make_tmap_nd(&p.tmB2, xb, 3, dims, str, box2)) != SGP_OK) return r;
+        }
     }
+    p.ts_rows = p.tail_cap > 0 ? 32 : kTsRows;
     p.K = gs.K;
     p.kb_total = gs.K / 64;
     p.kps = gs.kps;
@@ -678,15 +691,15 @@ int gemm_op(Launcher& L, const RunEnv& e, int op, int mu, const KCtx& c) {
     p.row0 = row0;
     p.nrows = b;
     p.R = grouped ? R : b;
-    const int stage_bytes = p.kps * (16384 + p.n_cap * 128);
+    const int stage_bytes = p.kps * (16384 + (p.n_cap + p.tail_cap) * 128);
     // one persistent CTA per SM: ring + accumulator staging within kGemmSmemBudget, which
     // leaves room beside it for a CTA of the small kernel before it (a programmatic launch
     // lets this kernel's CTAs start, and prefetch weights, while that kernel still runs).
     // Passes of 128+ tokens take the whole 227 KB instead: there a deep ring matters more.
     const int budget = p.n_cap >= 128 ? 232448 : kGemmSmemBudget;
-    p.stages = std::max(2, std::min(8, (budget - 2304 - std::min(p.n_cap, kTsRows) * 512) /
+    p.stages = std::max(2, std::min(8, (budget - 2304 - std::min(p.n_cap, p.ts_rows) * 512) /
                                           stage_bytes));
-    p.ring_bytes = (int)gemm_tc_ring_bytes(p.n_cap, p.stages, p.kps);
+    p.ring_bytes = (int)gemm_tc_ring_bytes(p.n_cap, p.stages, p.kps, p.tail_cap, p.ts_rows);
     p.n_units = gs.n_groups * gs.m_tiles * gs.ksplit;
     p.grid = e.pool_sms;
     p.serpentine = grouped && e.serpentine && (mu & 1);

@@ -86,6 +86,52 @@ def test_gptoss_stack_pipeline_bit_identical(n_stages, micro):
         assert torch.equal(k0, k1) and torch.equal(v0, v1), "KV append differs"
 
 
+def test_slot_rows_past_a_full_pass():
+    """Slots that overflow one full pass (256 rows): up to 32 rows past it ride along with the
+    pass as a second accumulator, more take a pass of their own.  Every routed row's SwiGLU
+    and expert-down outputs against the oracle's expert on the same row and token, and the
+    layer pipelined in 2 microbatches (no slot overflows there) == temporal.  8 picks per
+    token over 8 local slots give about 272 rows per slot; the first seed whose routing shows
+    all three cases (one pass, a tail riding along, a second pass) is used."""
+    shape = synth.LayerShape(hidden=256, n_q_heads=4, n_kv_heads=1, head_dim=64,
+                             n_experts=16, top_k=8, n_local_experts=8, inter=256)
+    wl = synth.WORKLOADS["tiny"].with_(shape=shape, n_tokens=272, kv_len=64, kv_cap=64)
+    s = wl.shape
+    d = H.dims(s, sgp.PATH_TC)
+    for seed in range(21, 29):
+        inp = H.make_inputs(wl, seed)
+        res = H.run_temporal_layer(inp, d)
+        assert res["status"] == sgp.SGP_OK, sgp.sgp_status_string(res["status"])
+        off = res["dump"]["slot_offsets"].cpu().numpy()
+        counts = np.diff(off)
+        if (counts <= 256).any() and ((counts > 256) & (counts <= 288)).any() \
+                and (counts > 288).any():
+            break
+    else:
+        pytest.fail(f"no seed covers all three cases (last slot rows {counts})")
+    dmp = res["dump"]
+    T = wl.n_tokens
+    pos = dmp["pair_pos"].cpu().numpy().reshape(T, s.top_k)
+    idx = res["idx"].cpu().numpy()
+    u = O.f64(dmp["u"])
+    z = O.f64(dmp["z"])
+    y = dmp["y"].cpu().numpy().astype(np.float64)
+    wgu = O.f64(inp.weights[0]["w_gate_up"])
+    wd = O.f64(inp.weights[0]["w_down"])
+    zr = np.zeros_like(z)
+    yr = np.zeros_like(y)
+    for t in range(T):
+        for j in range(s.top_k):
+            sl = O.slot_of(int(idx[t, j]), s.n_experts, s.n_local_experts, s.slot_map)
+            assert off[sl] <= pos[t, j] < off[sl + 1]
+            zr[pos[t, j]], yr[pos[t, j]] = O.swiglu_expert(u[t], wgu[sl], wd[sl], s.inter)
+    H.assert_close("z", z, zr)
+    H.assert_close("y", y, yr)
+    ref = _temporal(inp, H.dims(s))
+    got = _pipelined(inp, H.dims(s), 2, T // 2)
+    assert torch.equal(got[0], ref[0]), "x_out differs"
+
+
 def test_pipeline_bit_identical_across_sm_splits():
     """The SM split decides where and when the work runs, never what it computes: the smallest,
     a middle and the largest legal stage-A pool (attention on as few as 8-16 SMs, or on almost
