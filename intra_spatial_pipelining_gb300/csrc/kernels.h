@@ -71,6 +71,8 @@ constexpr int kTsRows = 64;
 // shared memory of one projection CTA (ring + staging + barriers): well under the SM's
 // 228 KB, so that a small kernel's CTA fits beside it
 constexpr int kGemmSmemBudget = 200 * 1024;
+// a grouped (expert) projection's kernel before it needs only a few KB of shared memory
+constexpr int kGemmSmemBudgetGrouped = 221 * 1024;
 
 struct GemmProblem {
     // weights: plain  3-D {64, rows, k-blocks} box {64, 128, 2};
