@@ -159,6 +159,42 @@ def test_attention_group_sizes(G):
     H.assert_close("o", bufs["o"], ref["o"])
 
 
+@pytest.mark.parametrize("path", [sgp.PATH_GEMV, sgp.PATH_TC])
+def test_single_sequence_layer_vs_oracle(path):
+    """One sequence: a single token row in every projection (one valid row of a 16-row MMA
+    tile on the tensor-core path), one routed row per picked slot and empty slots elsewhere;
+    a C1-shaped layer against the oracle on both projection paths."""
+    wl = synth.WORKLOADS["gptoss_layer"].with_(n_tokens=1)
+    inp, ref = H.make_inputs_with_margin(wl, 19)
+    res = H.run_temporal_layer(inp, H.dims(wl.shape, path))
+    errs = _check_layer(inp, ref, res, wl.n_tokens)
+    print("one sequence", path, {k: f"{v:.2e}" for k, v in errs.items()})
+
+
+@pytest.mark.parametrize("path", [sgp.PATH_GEMV, sgp.PATH_TC])
+def test_largest_hidden_layer_vs_oracle(path):
+    """hidden = 4096, the largest the library takes: the router's RMSNorm then loops over the
+    row instead of holding it in registers, its shared-memory rows are at their widest, and
+    the combine's fused next-layer RMSNorm keeps all 4096 features; every tensor against the
+    oracle, on both projection paths."""
+    shape = dataclasses.replace(synth.SHAPE_TINY, hidden=4096)
+    wl = synth.WORKLOADS["tiny"].with_(shape=shape, n_tokens=24)
+    inp, ref = H.make_inputs_with_margin(wl, 18)
+    res = H.run_temporal_layer(inp, H.dims(wl.shape, path))
+    errs = _check_layer(inp, ref, res, wl.n_tokens)
+    print("hidden 4096", path, {k: f"{v:.2e}" for k, v in errs.items()})
+    # a stack of two such layers: the combine also writes the next layer's RMSNorm input
+    wl2 = wl.with_(n_layers=2)
+    inp2, ref2 = H.make_stack_inputs_with_margin(wl2, 18)
+    d = H.dims(wl2.shape, path)
+    ws = H.workspace(d, wl2.n_tokens, wl2.cap)
+    out = torch.empty_like(inp2.x)
+    sgp.sgp_stack_temporal(d, inp2.sgp_layers(), inp2.kv_len, inp2.x, out, wl2.n_tokens,
+                           None, None, ws)
+    assert sgp.sgp_status_from_workspace(ws) == sgp.SGP_OK
+    H.assert_close("x_out (2 layers)", out, ref2["x_out"])
+
+
 def test_rope_layer_vs_oracle_long_positions():
     """RoPE on q and the new key (tensor-core QKV path) at positions up to 32,767."""
     shape = dataclasses.replace(synth.SHAPE_TINY, rope_theta=150000.0)
