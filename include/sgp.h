@@ -327,7 +327,9 @@ int sgp_pipeline_create(const sgp_dims* dims, const int* sm_split, int n_stages,
  * already queued on `stream` and `stream` waits for it.  Runs of one pipeline may use
  * different streams: each run is also ordered after the pipeline's previous run (an event
  * wait), since they share its flags and scratch.  The call does not wait for the GPU and
- * makes no host round trip inside a run.
+ * makes no host round trip inside a run; only a call whose arguments differ from the
+ * previous run's (a graph rebuild, which may reallocate the scratch) first waits for the
+ * previous run to complete.
  * Arguments as sgp_stack_temporal; layers is a host array read during this call only.
  * Returns SGP_OK, SGP_ERR_INVALID_ARG, SGP_ERR_CUDA, or the device status left by an earlier
  * run that has already completed (read from a host copy, without waiting; a run still in

@@ -1565,6 +1565,8 @@ extern "C" int sgp_pipeline_run(sgp_pipeline* p, const sgp_layer* layers, int n_
     add(&topk_idx, sizeof(topk_idx));
     add(&topk_w, sizeof(topk_w));
     if (!p->exec || key != p->key) {
+        // a rebuild may reallocate the scratch the previous run still uses: wait for it
+        if (p->launched) CK(cudaEventSynchronize(p->done));
         const int m = n_tokens / p->micro;
         std::vector<PTask> tasks = build_tasks(*p, layers, n_layers, m);
         const int ntrace = p->opts.trace ? n_layers * m * SGP_N_OPS * 2 : 0;
