@@ -367,12 +367,14 @@ def run_reference(args, rank, world):
 # ------------------------------------------------------------------------------------------
 # secondary shapes: one workload timed pipelined and temporally, then freed
 # ------------------------------------------------------------------------------------------
-def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None):
-    """Times one workload on this GPU: the two-stage pipeline (macro cut, `split` or the
-    contention-aware balancer's pick checked by full runs of its three best candidates) and
-    temporal execution.  Sliding-window layers share one KV buffer: each reads only the last
-    128 positions of every sequence, so sharing changes no timing and halves the memory of
-    the large shapes.  Returns a dict; every tensor is freed before it returns."""
+def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None,
+                cuts=("macro",)):
+    """Times one workload on this GPU: the two-stage pipeline (for each cut in `cuts`,
+    `split` or the contention-aware balancer's pick checked by full runs of its three best
+    candidates; the fastest cut is kept) and temporal execution.  Sliding-window layers share
+    one KV buffer: each reads only the last 128 positions of every sequence, so sharing
+    changes no timing and halves the memory of the large shapes.  Returns a dict; every
+    tensor is freed before it returns."""
     import torch
 
     from intra_spatial_pipelining_gb300 import sgp, synth
@@ -394,9 +396,14 @@ def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None)
     out = x.clone()
     N = sgp.sgp_device_info_get().sm_count
     stream = torch.cuda.current_stream()
-    full = [1] * sgp.N_OPS
-    full[sgp.OPS.index("attention")] = 0
-    cut = [full, [1] * sgp.N_OPS]
+    def cut_of(name):
+        full = [1] * sgp.N_OPS
+        full[sgp.OPS.index("attention")] = 0
+        if name == "macro_qkv":
+            full[sgp.OPS.index("rmsnorm_attn")] = full[sgp.OPS.index("qkv")] = 0
+        return [full, [1] * sgp.N_OPS]
+
+    cut = cut_of(cuts[0])
 
     def popts(**kw):
         return sgp.make_opts(stage_of_op=cut, stage_lanes=2, **kw)
@@ -419,19 +426,28 @@ def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None)
         return e0.elapsed_time(e1) / n
 
     picked = "given"
-    if split is None:
-        _, rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro, wl.cap,
-                                           quantum=8, reps=2,
-                                           opts=popts(stage_times_shared=1))
-        cands = [r[0] for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:3]]
-        best = min(cands, key=lambda pa: run_ms(2, [pa, N - pa], micro, popts(), 2, 1))
-        split = [best, N - best]
-        picked = "contention-aware balancer, best of its 3 best candidates by full runs"
-    ms_pipe = run_ms(2, split, micro, popts(), steps, warmup)
+    given = split
+    best_ms = None
+    for name in cuts:
+        cut = cut_of(name)
+        spl = given
+        if spl is None:
+            _, rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro, wl.cap,
+                                               quantum=8, reps=2,
+                                               opts=popts(stage_times_shared=1))
+            cands = [r[0] for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:3]]
+            best = min(cands, key=lambda pa: run_ms(2, [pa, N - pa], micro, popts(), 2, 1))
+            spl = [best, N - best]
+            picked = "contention-aware balancer, best of its 3 best candidates by full runs"
+        ms = run_ms(2, spl, micro, popts(), steps, warmup)
+        if best_ms is None or ms < best_ms:
+            best_ms, split, best_cut = ms, spl, name
+    ms_pipe = best_ms
     ms_temp = run_ms(1, [N], T, None, steps, warmup)
     nbytes = algorithmic_bytes(wl, kv_len.cpu().tolist())
     res = {"workload": describe(wl, {})["workload"], "n_tokens": T,
-           "sm_split": split, "split_from": picked, "microbatch": micro, "lanes_per_stage": 2,
+           "sm_split": split, "split_from": picked, "cut": best_cut,
+           "microbatch": micro, "lanes_per_stage": 2,
            "pipeline_us": ms_pipe * 1e3, "temporal_us": ms_temp * 1e3,
            "pipeline_speedup": ms_temp / ms_pipe,
            "tokens_per_s_per_gpu": {"pipeline": T / (ms_pipe * 1e-3), "temporal": T / (ms_temp * 1e-3)},
@@ -460,7 +476,8 @@ def run_frontier(args):
     peak, _ = read_peaks()
     for b in (8, 16, 32, 64, 128, 256):
         wl = synth.sweep_workload(b)
-        r = shape_point(wl, dev, args.seed, args.steps, args.warmup, peak=peak)
+        r = shape_point(wl, dev, args.seed, args.steps, args.warmup, peak=peak,
+                        cuts=("macro", "macro_qkv"))
         print(json.dumps({"frontier_point": r}), flush=True)
 
 
