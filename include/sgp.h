@@ -91,7 +91,9 @@ typedef struct sgp_dims {
     int slot_map;         /* 0: global expert g -> slot g % E_local;
                              1: g -> g * E_local / E (expert-parallel loopback)      */
     int path;             /* SGP_PATH_*                                              */
-    int gemv_max_tokens;  /* threshold of SGP_PATH_AUTO (16)                         */
+    int gemv_max_tokens;  /* threshold of SGP_PATH_AUTO; 2 is measured best for
+                             temporal execution on GB300 (36 layers: the GEMV wins
+                             at 1 sequence, the tcgen05 GEMM from 2 on)             */
     float rope_theta;     /* RoPE base for q and the new key at position kv_len-1
                              (half-split pairs i, i + d/2); 0 = no rotation.  Needs the
                              tensor-core QKV path (SGP_ERR_UNSUPPORTED otherwise)      */

@@ -11,6 +11,7 @@ Used to time and profile single kernels, e.g. a profiler restricted to one kerne
 skips the launches of the set-up layer and captures the first launch of the operator:
 
     python -m intra_spatial_pipelining_gb300.opbench --op qkv --reps 3
+    python -m intra_spatial_pipelining_gb300.opbench --op all --tokens 8 --path gemv
 
     ops: rmsnorm_attn qkv attention oproj router dispatch expert_up expert_down combine
 """
@@ -63,6 +64,8 @@ def main():
     ap.add_argument("--op", default="all")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tc"],
+                    help="projection path (auto: the library's default threshold)")
     args = ap.parse_args()
 
     import torch
@@ -81,7 +84,8 @@ def main():
     w = synth.layer_weights(wl, args.layer, args.seed, dev)
     kc, vc = synth.kv_cache(wl, args.layer, args.seed, dev)
     layer = sgp.make_layer(w, kc, vc, wl.layer_window(args.layer))
-    d = sgp.make_dims(wl.shape)
+    d = sgp.make_dims(wl.shape, {"auto": sgp.PATH_AUTO, "gemv": sgp.PATH_GEMV,
+                                 "tc": sgp.PATH_TC}[args.path])
     ws = torch.zeros(sgp.sgp_workspace_bytes(d, T, wl.cap), dtype=torch.uint8, device=dev)
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()

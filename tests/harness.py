@@ -147,6 +147,8 @@ def routing_sets(idx) -> list:
 
 
 def dims(shape, path=sgp.PATH_AUTO, gemv_max_tokens=16):
+    """The tests' threshold (16) keeps their 6-12-sequence cases on the GEMV path, so both
+    projection paths are covered; the library's default is lower."""
     return sgp.make_dims(shape, path, gemv_max_tokens)
 
 
