@@ -370,7 +370,7 @@ def run_reference(args, rank, world):
 def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None,
                 cuts=("macro",)):
     """Times one workload on this GPU: the two-stage pipeline (for each cut in `cuts`,
-    `split` or the contention-aware balancer's pick checked by full runs of its three best
+    `split` or the contention-aware balancer's pick checked by full runs of its five best
     candidates; the fastest cut is kept) and temporal execution.  Sliding-window layers share
     one KV buffer: each reads only the last 128 positions of every sequence, so sharing
     changes no timing and halves the memory of the large shapes.  Returns a dict; every
@@ -435,10 +435,10 @@ def shape_point(wl, dev, seed, steps, warmup, split=None, micro=None, peak=None,
             _, rows = sgp.sgp_pipeline_balance(d, layers, kv_len, x, out, T, micro, wl.cap,
                                                quantum=8, reps=2,
                                                opts=popts(stage_times_shared=1))
-            cands = [r[0] for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:3]]
+            cands = [r[0] for r in sorted(rows, key=lambda r: max(r[1], r[2]))[:5]]
             best = min(cands, key=lambda pa: run_ms(2, [pa, N - pa], micro, popts(), 2, 1))
             spl = [best, N - best]
-            picked = "contention-aware balancer, best of its 3 best candidates by full runs"
+            picked = "contention-aware balancer, best of its 5 best candidates by full runs"
         ms = run_ms(2, spl, micro, popts(), steps, warmup)
         if best_ms is None or ms < best_ms:
             best_ms, split, best_cut = ms, spl, name
