@@ -49,6 +49,8 @@ def main():
     ap.add_argument("--split", default="56,96", help="SMs of stage A, stage B")
     ap.add_argument("--cut", default="macro_qkv", choices=["macro", "macro_qkv", "layer"])
     ap.add_argument("--micro", type=int, default=None, help="sequences per microbatch")
+    ap.add_argument("--weight-reuse", action="store_true",
+                    help="L2 evict-last hint on the weights a later microbatch reads again")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--seed", type=int, default=0)
     args = ap.parse_args()
@@ -84,7 +86,8 @@ def main():
             if args.cut == "macro_qkv":
                 full[sgp.OPS.index("rmsnorm_attn")] = full[sgp.OPS.index("qkv")] = 0
             slide = [1] * sgp.N_OPS
-        opts = sgp.make_opts(stage_of_op=[full, slide], stage_lanes=2)
+        opts = sgp.make_opts(stage_of_op=[full, slide], stage_lanes=2,
+                             **({"weight_reuse": 1} if args.weight_reuse else {}))
     p = sgp.sgp_pipeline_create(d, split, len(split), micro, T, wl.cap, opts)
     try:
         for _ in range(args.warmup):
@@ -106,6 +109,7 @@ def main():
     print(json.dumps({"mode": "temporal" if args.temporal else "pipeline", "workload": wl.name,
                       "layers": wl.n_layers, "n_tokens": T, "sm_split": split,
                       "microbatch": micro, "cut": None if args.temporal else args.cut,
+                      "weight_reuse": bool(args.weight_reuse),
                       "run_us": e0.elapsed_time(e1) * 1e3,
                       "algorithmic_bytes": algorithmic_bytes(wl, kv_len.cpu().tolist())}),
           flush=True)
