@@ -16,7 +16,8 @@ def test_c2_bytes_written_out_by_hand():
     """36 layers x (W_qkv 5120 x 2880 + W_o 2880 x 4096 + W_r 128 x 2880 + 4 experts x 3 x
     2880 x 2880 + two gains), bf16; 18 full layers read 64 x 8 KV heads x 8192 positions x
     64 x (K, V) bf16, 18 sliding layers the last 128 positions; every layer appends one K and
-    one V row per sequence and head.  Activations are the small rest (under 1 %)."""
+    one V row per sequence and head.  Activations are the small rest (about 1 %: 9.2 MB per
+    layer, the token rows in and out of each op and the routed rows)."""
     wl = synth.WORKLOADS["gptoss_36l"]
     weights = 36 * 2 * (5120 * 2880 + 2880 * 4096 + 128 * 2880 + 4 * 3 * 2880 * 2880 + 2 * 2880)
     kv_full = 18 * 64 * 8 * 8192 * 64 * 2 * 2
@@ -26,7 +27,7 @@ def test_c2_bytes_written_out_by_hand():
     rest = total - (weights + kv_full + kv_slide + append)
     assert weights == 9_104_348_160          # 9.10 GB
     assert kv_full == 19_327_352_832         # 19.33 GB
-    assert 0 < rest < 0.01 * total
+    assert 0 < rest < 0.02 * total
     # the 4.28 ms floor at the measured 6,795.1 GB/s
     assert abs(total / 6795.1e9 * 1e3 - 4.28) < 0.005
 
