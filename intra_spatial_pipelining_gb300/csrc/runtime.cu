@@ -1457,7 +1457,13 @@ extern "C" int sgp_pipeline_create(const sgp_dims* d, const int* sm_split, int n
                 p->stage_of_op[s][op] = st;
             }
     }
-    CK(cudaGetDevice(&p->dev));
+    {
+        const cudaError_t ge = cudaGetDevice(&p->dev);
+        if (ge != cudaSuccess) {
+            delete p;
+            return fail_cuda(ge, "cudaGetDevice");
+        }
+    }
     const bool green = n_stages >= 2 && p->opts.use_green_contexts >= 0;
     if (green) {
         if (!sm_split) {
