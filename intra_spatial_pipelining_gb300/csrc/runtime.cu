@@ -1235,7 +1235,12 @@ int ensure_ws(sgp_pipeline* p, int T, int nflags, int ntrace = 0) {
         g_err = std::string("cudaMalloc: ") + cudaGetErrorString(e);
         return SGP_ERR_OOM;
     }
-    CK(cudaMemset(p->ws, 0, L.total));
+    e = cudaMemset(p->ws, 0, L.total);
+    if (e != cudaSuccess) {
+        cudaFree(p->ws);
+        p->ws = nullptr;
+        return fail_cuda(e, "cudaMemset");
+    }
     p->lay = L;
     p->ws_bytes = L.total;
     p->ws_T = T;
